@@ -1,0 +1,190 @@
+"""Planted mistakes: each plausible bug in the oracle must trip at least one pin.
+
+Every mutant below is planted in the oracle module on the CPU (monkeypatch) and
+the compact pin set ``pin_failures`` is run against it; an unmutated oracle
+passes every pin, each mutant fails at least one.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.mla_oracle as om
+import test_oracle_pins as pins
+from brute_force import partial_brute
+
+_orig_attend = om.attend
+
+
+def _pin_brute(base):
+    rng = np.random.default_rng(5)
+    q, kv, bt, sl = pins.tiny_case(rng, [0, 3, 9, 21], heads=2, num_parts=3, dk=10,
+                                   page_size=4)
+    for r in range(3):
+        out, lse = oracle.decode_partial(q, kv, bt, sl, r, 3, 0.41, base, page_size=4,
+                                         d_v=6)
+        bo, bl = partial_brute(q.tolist(), kv.tolist(), bt.tolist(), sl.tolist(), r, 3,
+                               0.41, 6, 4, base2=bool(base))
+        np.testing.assert_allclose(out, np.array(bo), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse, np.array(bl), rtol=1e-10, atol=1e-12)
+
+
+def _pin_full_dims():
+    pins.test_partial_matches_brute_force_full_dims()
+
+
+def _pin_closed_forms():
+    pins.test_single_token_returns_its_value_and_score()
+    pins.test_equal_scores_average_the_values()
+    pins.test_equal_values_return_that_value()
+    pins.test_zero_query_gives_uniform_weights()
+
+
+def _pin_partitions():
+    pins.test_merging_partials_gives_unpartitioned_result(3)
+    pins.test_partition_owning_nothing_is_exactly_neutral()
+    pins.test_base2_lse_is_natural_times_log2e()
+
+
+def _pin_combine():
+    for base in (0, 1):
+        pins.test_combine_matches_brute_force(base)
+    pins.test_combine_single_finite_lse_selects_its_partial()
+    pins.test_combine_all_empty_is_neutral()
+
+
+def _pin_formats():
+    pins.test_e4m3_decode_matches_torch_on_every_pattern()
+    pins.test_fp8_partial_matches_brute_force()
+
+
+PINS = [lambda: _pin_brute(0), lambda: _pin_brute(1), _pin_full_dims, _pin_closed_forms,
+        _pin_partitions, _pin_combine, _pin_formats]
+
+
+def pin_failures() -> int:
+    bad = 0
+    for pin in PINS:
+        try:
+            pin()
+        except Exception:  # an assertion, or a mutant that no longer runs
+            bad += 1
+    return bad
+
+
+# ---------------------------------------------------------------- the mutants
+
+def _blocked_owner(seq_len, num_parts, part_id):
+    per = -(-seq_len // num_parts)
+    return np.arange(part_id * per, min(seq_len, (part_id + 1) * per), dtype=np.int64)
+
+
+def _off_by_one_owner(seq_len, num_parts, part_id):
+    return np.arange(part_id + 1, seq_len, num_parts, dtype=np.int64)
+
+
+def _swapped_page_row(kv_bits, bt_row, tokens, page_size):
+    pages = np.asarray(bt_row)[tokens % page_size % len(bt_row)].astype(np.int64)
+    return kv_bits[pages, tokens // page_size % page_size]
+
+
+def _identity_placement(kv_bits, bt_row, tokens, page_size):
+    return kv_bits[(tokens // page_size).astype(np.int64), tokens % page_size]
+
+
+def _drop_rope(q, k, sm_scale, d_v=om.D_V):
+    keep = d_v if q.shape[1] > d_v else q.shape[1] - 2
+    return _orig_attend(q[:, :keep], k[:, :keep], sm_scale, d_v)
+
+
+def _value_from_tail(q, k, sm_scale, d_v=om.D_V):
+    out, lse = _orig_attend(q, k, sm_scale, d_v)
+    if k.shape[0] == 0:
+        return out, lse
+    s = sm_scale * (q @ k.T)
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    return (w @ k[:, -d_v:]) / w.sum(axis=1, keepdims=True), lse
+
+
+def _lse_without_scale(q, k, sm_scale, d_v=om.D_V):
+    out, lse = _orig_attend(q, k, sm_scale, d_v)
+    if k.shape[0] == 0:
+        return out, lse
+    s = q @ k.T
+    mu = s.max(axis=1)
+    return out, mu + np.log(np.exp(s - mu[:, None]).sum(axis=1))
+
+
+def _normalised_over_heads(q, k, sm_scale, d_v=om.D_V):
+    if k.shape[0] == 0:
+        return _orig_attend(q, k, sm_scale, d_v)
+    s = sm_scale * (q @ k.T)
+    w = np.exp(s - s.max())
+    out = (w @ k[:, :d_v]) / w.sum(axis=0).sum()
+    return out, s.max() + np.log(w.sum(axis=1))
+
+
+def _zero_lse_when_empty(q, k, sm_scale, d_v=om.D_V):
+    out, lse = _orig_attend(q, k, sm_scale, d_v)
+    return out, (np.zeros_like(lse) if k.shape[0] == 0 else lse)
+
+
+def _base2_divides(lse_natural, lse_base):
+    return lse_natural if lse_base == 0 else lse_natural / om.LOG2E
+
+
+def _combine_wrong_sign(partials, lses, lse_base=0):
+    lam = om.lse_to_natural(lses, lse_base)
+    big = lam.max(axis=0)
+    w = np.where(np.isfinite(lam), np.exp(big[None] - lam), 0.0)
+    z = w.sum(axis=0)
+    return (w[..., None] * partials).sum(axis=0) / z[..., None], om.lse_to_base(
+        big + np.log(z), lse_base)
+
+
+def _combine_unnormalised(partials, lses, lse_base=0):
+    lam = om.lse_to_natural(lses, lse_base)
+    big = lam.max(axis=0)
+    safe = np.where(np.isfinite(big), big, 0.0)
+    w = np.where(np.isfinite(lam), np.exp(lam - safe[None]), 0.0)
+    z = w.sum(axis=0)
+    lse = np.where(np.isfinite(big), safe + np.log(np.where(z > 0, z, 1)), -np.inf)
+    return (w[..., None] * partials).sum(axis=0), om.lse_to_base(lse, lse_base)
+
+
+def _e4m3_bias8(bits):
+    return om.e4m3_to_f64(bits) / 2.0
+
+
+MUTANTS = {
+    "blocked owner rule": ("owned_tokens", _blocked_owner),
+    "owner off by one": ("owned_tokens", _off_by_one_owner),
+    "page / row swapped": ("gather_rows", _swapped_page_row),
+    "block table ignored": ("gather_rows", _identity_placement),
+    "rope dims dropped from the score": ("attend", _drop_rope),
+    "value taken from the tail dims": ("attend", _value_from_tail),
+    "lse without sm_scale": ("attend", _lse_without_scale),
+    "softmax normalised over heads": ("attend", _normalised_over_heads),
+    "empty partition lse = 0": ("attend", _zero_lse_when_empty),
+    "base-2 conversion inverted": ("lse_to_base", _base2_divides),
+    "combine weight sign flipped": ("lse_combine", _combine_wrong_sign),
+    "combine not normalised": ("lse_combine", _combine_unnormalised),
+    "e4m3 exponent bias 8": ("e4m3_to_f64", _e4m3_bias8),
+}
+
+
+def _patch(monkeypatch, name, fn):
+    monkeypatch.setattr(om, name, fn)
+    monkeypatch.setattr(oracle, name, fn)
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert pin_failures() == 0
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_planted_mistake_is_caught(monkeypatch, mutant):
+    name, fn = MUTANTS[mutant]
+    _patch(monkeypatch, name, fn)
+    assert pin_failures() >= 1, f"no pin caught: {mutant}"
