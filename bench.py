@@ -1,0 +1,400 @@
+"""Benchmark of the MLA absorbed paged-decode hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one ``mla_decode_partial`` call (P = 1) over the 32K-context batch:
+B = 64 requests, H = 64 heads, L ~ U{4096..32768}, bf16 latent KV in a
+40,000-page pool, page size 64.  It reads ~1.36 GB of KV per step, far more
+than the 129 MB L2, so no flush is needed between steps.  Prints one JSON line:
+tokens/s (one new token per request per step), KV GB/s and its fraction of
+the measured HBM copy peak, the end-to-end figure through the C ABI with host
+buffers, the fp64 CPU oracle timed on the host cores, and SM clocks sampled
+during the timed region.
+
+N > 1 (torchrun, one process per GPU): every rank runs its own replica of the
+workload (the method's partitions are emulated on one GPU; there is no
+exchange), time is the max over ranks, value the sum over ranks.
+
+``--impl reference`` times the fp64 CPU oracle instead (rank 0 only): each
+step is one DCP partition (1 of 64) of one request of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MLA decode tokens/s and KV-read HBM GB/s (fraction of roofline) on 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+ROW_BYTES = {"bf16": 576 * 2, "e4m3": 576}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_partial_long32k_traffic.txt")
+
+
+# ---------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Maximum of a per-rank float over all ranks (identity at world 1)."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(ms_per_rank_max: float, steps: int, units_per_step_per_rank: int, world: int):
+    """Whole-job throughput: units of all ranks / the slowest rank's time."""
+    secs = ms_per_rank_max / 1e3
+    return units_per_step_per_rank * steps * world / secs
+
+
+# ---------------------------------------------------------------- measurement helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_paged_decode_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    for line in open(TRAFFIC_FILE):
+        if "=" in line and not line.startswith("#"):
+            k, v = line.strip().split("=", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_digest") != kernel_digest():
+        return None
+    try:
+        return int(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            uuid = None
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", str(period_ms)]
+        if uuid:
+            cmd[1:1] = ["-i", uuid]
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(case, seconds: float):
+    """The fp64 oracle, as it stands, on whole requests of the same workload
+    until ``seconds`` of CPU time have passed."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from casebits import subcase_bits
+    done, spent = 0, 0.0
+    tokens = 0
+    while spent < seconds and done < case.batch:
+        q, kv, bt, lens = subcase_bits(case, [done])
+        t0 = time.perf_counter()
+        oracle.decode_partial(q, kv, bt, lens, 0, 1, case.sm_scale, 0)
+        spent += time.perf_counter() - t0
+        tokens += int(lens[0])
+        done += 1
+    return {"value": done / spent, "unit": "tokens/s", "cores": _oracle_threads(),
+            "kind": "oracle",
+            "sample": f"first {done} of {case.batch} requests of the same batch "
+                      f"({tokens} cached tokens, all {case.heads} heads), fp64 numpy, "
+                      f"{spent:.1f} s"}
+
+
+def _oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 1) for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- the two arms
+
+def run_ours(args, world, rank, local):
+    import mla_paged_decode_gb300 as mla
+    from mla_paged_decode_gb300 import build
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    if rank == 0 or not os.path.exists(mla.library_path()):
+        build.build()
+    barrier(world)
+    mla.load_library()
+
+    case = workloads.config_long32k(device=dev, seed=args.seed)
+    B, H = case.batch, case.heads
+    kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
+    out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mla.decode_partial(case.q, case.kv_pages, case.block_table, case.seq_lens, 0, 1,
+                           case.sm_scale, 0, out, lse, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clock_info = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    ms_max = max_over_ranks(ms, world, dev)
+    assert mla.check_workspace(ws) == 0
+
+    # end to end through the C ABI with host buffers: pinned H2D inputs, D2H results
+    q_h = case.q.cpu().pin_memory()
+    bt_h = case.block_table.cpu().pin_memory()
+    sl_h = case.seq_lens.cpu().pin_memory()
+    q_d, bt_d, sl_d = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        mla.decode_partial(q_d, case.kv_pages, bt_d, sl_d, 0, 1, case.sm_scale, 0, out, lse,
+                           workspace=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e_ms_max = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
+    assert torch.isfinite(out_h.float()).all()
+
+    value = aggregate(ms_max, args.steps, B, world)
+    avg_launch_s = ms / 1e3 / args.steps
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / avg_launch_s / 1e9
+    traffic = recorded_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": case.name, "batch": B, "heads": H, "q_len": 1,
+                   "seq_lens": "uniform 4096..32768 (seed %d)" % args.seed,
+                   "mean_seq_len": kv_bytes / ROW_BYTES[case.kv_dtype] / B,
+                   "page_size": 64, "pool_pages": case.num_pages, "num_parts": 1,
+                   "kv_dtype": "bf16", "kv_bytes_per_step": kv_bytes,
+                   "l2": "inputs larger than L2: %.2f GB of KV read per step, no flush" % (kv_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "kv_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "frac_of_8tbs": achieved / 8000.0,
+                     "traffic": traffic,
+                     "kernel": "mla_decode_partial (one launch per step)"},
+        "e2e": {"value": aggregate(e_ms_max, args.steps, B, world), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "q, block table and lengths copied from pinned host memory, out and "
+                        "lse read back, every step; the KV cache stays resident in HBM"},
+        "gpu_launches": args.steps,
+        "clocks": clock_info,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle as it stands, one DCP partition (1 of 64) of one
+    request per step, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from casebits import subcase_bits
+    # the same seeded batch as the GPU arm (drawn on the GPU when there is one,
+    # so both arms see identical values); only the sampled pages reach the host
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = workloads.config_long32k(device=gen_dev, seed=args.seed)
+    P = 64
+    B = case.batch
+    subs = {}
+
+    def step(i):
+        b, r = (i // P) % B, i % P
+        if b not in subs:
+            subs.clear()
+            subs[b] = subcase_bits(case, [b])
+        q, kv, bt, lens = subs[b]
+        oracle.decode_partial(q, kv, bt, lens, r, P, case.sm_scale, 0)
+
+    for i in range(args.warmup):
+        step(i)
+    spent = 0.0
+    for i in range(args.steps):
+        b = (i // P) % B
+        if b not in subs:
+            subs.clear()
+            subs[b] = subcase_bits(case, [b])
+        t0 = time.perf_counter()
+        step(i)
+        spent += time.perf_counter() - t0
+    value = (args.steps / P) / spent
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": spent * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": case.name, "batch": B, "heads": case.heads, "page_size": 64,
+                   "num_parts": 1, "seq_lens": "uniform 4096..32768 (seed %d)" % args.seed},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _oracle_threads(),
+                         "kind": "oracle",
+                         "sample": "each step: one round-robin partition (1 of 64) of one "
+                                   "request, all heads; tokens/s counts 1/64 token per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA absorbed paged-decode library.
+ *
+ * Two operations, both from the decode-context-parallel (DCP) pages:
+ *
+ *  mla_decode_partial  one partition's attention over a paged latent KV cache,
+ *                      returning the partition-local pair (out, lse).
+ *                      sglang pull 33926 (trtllm_mla decode path gains DCP):
+ *                      motivation (round-robin owner rule t mod P; a single-token
+ *                      decode needs no causal bound), implementation step 3
+ *                      (rank-local (out, lse); a rank owning nothing returns the
+ *                      neutral (0, -inf)), step 4 (LSE in base 2 or base e).
+ *  mla_lse_combine     the LSE-weighted softmax merge of P partial results.
+ *                      sglang pull 33364 ([Attention][DCP] Add symm_a2a ...),
+ *                      "Modifications", kernel 4 (wait_lse_combine_kernel), here
+ *                      without the cross-GPU exchange: all partials are already
+ *                      in one device buffer.
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers of the current CUDA device unless stated.
+ *    The caller owns every buffer; the library never allocates, never frees
+ *    and never synchronises the host.  Work is enqueued on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream).
+ *  - The return value is a status: MLA_OK (0) or a negative MLA_ERR_* code.
+ *    Argument errors are detected on the host before anything is launched,
+ *    and the outputs are then left untouched.  MLA_ERR_CUDA carries the CUDA
+ *    error text in mla_last_cuda_error().
+ *  - Calls are thread-compatible: concurrent calls must use distinct
+ *    workspaces.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mla_stream_t; /* == cudaStream_t */
+
+enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_NULL = -1,      /* a required pointer is NULL                           */
+  MLA_ERR_SHAPE = -2,     /* unsupported size: q_len != 1, Dqk != 576, Dv != 512,
+                             page_size != 64, heads not in [1, 128], ...          */
+  MLA_ERR_PARTITION = -3, /* num_parts < 1 or part_id outside [0, num_parts)      */
+  MLA_ERR_ALIGN = -4,     /* q / kv_pages / out / partials not 16-byte aligned,
+                             workspace not 256-byte aligned                       */
+  MLA_ERR_WORKSPACE = -5, /* workspace smaller than mla_decode_workspace_size()   */
+  MLA_ERR_ARG = -6,       /* bad enum value, non-finite scale, negative size      */
+  MLA_ERR_CUDA = -7,      /* a CUDA call failed; see mla_last_cuda_error()        */
+  MLA_ERR_DEVICE = -8,    /* current device is not an sm_103 GPU                  */
+  MLA_ERR_BOUNDS = -9     /* (from mla_decode_check_workspace) the kernel met a
+                             block-table entry outside [0, num_pages) or a sequence
+                             length outside [0, 64 * max_pages_per_seq]            */
+};
+
+enum mla_lse_base {
+  MLA_LSE_NATURAL = 0, /* lse = ln(sum_j exp(s_j))                                */
+  MLA_LSE_BASE2 = 1    /* lse = log2(sum_j exp(s_j)) = natural * log2(e)          */
+};
+
+enum mla_kv_dtype {
+  MLA_KV_BF16 = 0, /* cache rows are bf16                                         */
+  MLA_KV_E4M3 = 1  /* cache rows are OCP FP8 e4m3, value = e4m3 * kv_scale        */
+};
+
+/* Sizes that the ten named arguments of mla_decode_partial leave implicit. */
+typedef struct mla_decode_desc {
+  int32_t batch;             /* B, number of requests (0 is a no-op)              */
+  int32_t num_heads;         /* H, query heads per request, 1..128                */
+  int32_t q_len;             /* query tokens per request; must be 1               */
+  int32_t head_dim_qk;       /* must be 576 (512 latent + 64 rope)                */
+  int32_t head_dim_v;        /* must be 512 (the latent)                          */
+  int32_t page_size;         /* tokens per cache page; must be 64                 */
+  int32_t num_pages;         /* physical pages in kv_pages (>= 1)                 */
+  int32_t max_pages_per_seq; /* entries per block_table row (>= 1)                */
+  int32_t kv_dtype;          /* enum mla_kv_dtype                                 */
+  float kv_scale;            /* per-tensor dequant scale for E4M3 (> 0, finite)   */
+} mla_decode_desc;
+
+/*
+ * Bytes of scratch workspace mla_decode_partial needs for `d` on a GPU with
+ * `num_sms` SMs (num_sms <= 0: ask the current device).  Returns 0 if `d` is
+ * NULL or invalid.  The workspace holds per-request split counters, a device
+ * error word and the fp32 partial results of requests split across CTAs.
+ * It must be zero-filled once before its first use; every call leaves the
+ * counters at zero again.
+ */
+size_t mla_decode_workspace_size(const mla_decode_desc *d, int num_sms);
+
+/*
+ * Partition `part_id` of `num_parts` of MLA absorbed decode attention.
+ *
+ *  q           bf16 [B, 1, H, 576], contiguous.  Dims 0..511 latent, 512..575 rope.
+ *  kv_pages    [num_pages, 64, 576] rows of the GLOBAL paged cache, contiguous,
+ *              bf16 or e4m3 bytes per d->kv_dtype.  Row dims 0..511 are also
+ *              the value (the latent).
+ *  block_table int32 [B, max_pages_per_seq]: logical page i of request b lives
+ *              in physical page block_table[b][i].  Entries past the request's
+ *              last page are never read.
+ *  seq_lens    int32 [B]: GLOBAL sequence lengths L_b (tokens 0..L_b-1 exist).
+ *  part_id, num_parts
+ *              the partition attends exactly to the global tokens t < L_b with
+ *              t mod num_parts == part_id (round-robin owner rule).  A real DCP
+ *              rank holding a compacted local cache is num_parts = 1 over its
+ *              local pages and local lengths.
+ *  sm_scale    softmax scale applied to q.k (finite).
+ *  lse_base    enum mla_lse_base of the returned lse.
+ *  out         bf16 [B, 1, H, 512]: softmax(sm_scale q K^T) V over the owned
+ *              tokens, rounded to nearest even.  All of it is written.
+ *  lse         fp32 [B, 1, H]: log-sum-exp of the scaled scores in `lse_base`.
+ *              A request for which the partition owns no token gets out = 0 and
+ *              lse = -inf (the neutral pair of the LSE merge).
+ *  workspace   scratch of >= mla_decode_workspace_size(d, 0) bytes, 256-byte
+ *              aligned, zero-filled before first use (see above).
+ *
+ * Single-token decode only: q_len != 1 is rejected with MLA_ERR_SHAPE, the
+ * analogue of the DCP kernel gate that refuses multi-token (causal) requests.
+ * Block-table entries outside [0, num_pages) and lengths outside
+ * [0, 64 * max_pages_per_seq] are not dereferenced: the kernel skips them and
+ * records MLA_ERR_BOUNDS in the workspace (read it with
+ * mla_decode_check_workspace); the affected outputs are then unspecified.
+ * Outputs are bitwise deterministic for fixed inputs and device.
+ */
+int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block_table,
+                       const int32_t *seq_lens, int part_id, int num_parts, float sm_scale,
+                       int lse_base, void *out, float *lse, const mla_decode_desc *d,
+                       void *workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * Waits for `stream`, reads and clears the device error word of `workspace`.
+ * Returns MLA_OK, MLA_ERR_BOUNDS, or MLA_ERR_CUDA.  (The one call that
+ * synchronises; meant for tests and debugging.)
+ */
+int mla_decode_check_workspace(void *workspace, mla_stream_t stream);
+
+/* Sizes of an LSE combine. */
+typedef struct mla_combine_desc {
+  int32_t num_tokens; /* T (0 is a no-op)                                         */
+  int32_t num_heads;  /* H >= 1                                                   */
+  int32_t head_dim;   /* D, a multiple of 8 in [8, 1024]                          */
+  int32_t lse_base;   /* enum mla_lse_base of `lses` and of `out_lse`             */
+  float *out_lse;     /* optional fp32 [T, H] merged lse (device), or NULL        */
+} mla_combine_desc;
+
+/*
+ * LSE-weighted merge of `num_parts` partial attention results.
+ *
+ *  partials  bf16 [num_parts, T, H, D], contiguous.
+ *  lses      fp32 [num_parts, T, H] in base d->lse_base; -inf marks a partition
+ *            that owned no token (its partial is ignored).
+ *  out       bf16 [T, H, D]:  sum_p w_p o_p / sum_p w_p with
+ *            w_p = base^(lse_p - max_p lse_p).  Rows whose partitions are all
+ *            -inf get out = 0 (and out_lse = -inf), never NaN.
+ */
+int mla_lse_combine(const void *partials, const float *lses, int num_parts, void *out,
+                    const mla_combine_desc *d, mla_stream_t stream);
+
+/* Static text for a status code. */
+const char *mla_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char *mla_last_cuda_error(void);
+
+/* Library version as 10000 * major + 100 * minor + patch. */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

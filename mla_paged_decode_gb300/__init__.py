@@ -1,0 +1,217 @@
+"""Python binding of the GB300 MLA paged-decode C ABI (include/mla_decode.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``_lib/libmla_decode.so``.  PyTorch supplies device memory and the
+current stream.  If the library is not built, every call raises: there is no
+CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "MlaError", "LSE_NATURAL", "LSE_BASE2", "decode_partial", "lse_combine",
+    "workspace_size", "make_workspace", "check_workspace", "library_path", "load_library",
+]
+
+LSE_NATURAL = 0
+LSE_BASE2 = 1
+KV_BF16 = 0
+KV_E4M3 = 1
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libmla_decode.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+class DecodeDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("q_len", ctypes.c_int32), ("head_dim_qk", ctypes.c_int32),
+                ("head_dim_v", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("kv_scale", ctypes.c_float)]
+
+
+class CombineDesc(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("lse_base", ctypes.c_int32),
+                ("out_lse", ctypes.c_void_p)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Loads the built library (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is not built; run `python -m mla_paged_decode_gb300.build`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.mla_decode_partial.argtypes = [vp, vp, vp, vp, i32, i32, f32, i32, vp, vp,
+                                           ctypes.POINTER(DecodeDesc), vp, sz, vp]
+        lib.mla_decode_partial.restype = i32
+        lib.mla_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeDesc), i32]
+        lib.mla_decode_workspace_size.restype = sz
+        lib.mla_decode_check_workspace.argtypes = [vp, vp]
+        lib.mla_decode_check_workspace.restype = i32
+        lib.mla_lse_combine.argtypes = [vp, vp, i32, vp, ctypes.POINTER(CombineDesc), vp]
+        lib.mla_lse_combine.restype = i32
+        lib.mla_status_string.argtypes = [i32]
+        lib.mla_status_string.restype = ctypes.c_char_p
+        lib.mla_last_cuda_error.argtypes = []
+        lib.mla_last_cuda_error.restype = ctypes.c_char_p
+        lib.mla_version.argtypes = []
+        lib.mla_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != 0:
+        lib = load_library()
+        msg = lib.mla_status_string(status).decode()
+        if status == -7:
+            msg += ": " + lib.mla_last_cuda_error().decode()
+        raise MlaError(status, msg)
+
+
+def _stream_ptr(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def _kv_dtype_code(kv_pages: torch.Tensor) -> int:
+    if kv_pages.dtype == torch.bfloat16:
+        return KV_BF16
+    if kv_pages.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return KV_E4M3
+    raise TypeError(f"kv_pages must be bf16 or e4m3 bytes, got {kv_pages.dtype}")
+
+
+def _decode_desc(q, kv_pages, block_table, kv_scale) -> DecodeDesc:
+    if q.dim() != 4:
+        raise ValueError("q must be [B, q_len, H, 576]")
+    B, q_len, H, dqk = q.shape
+    if kv_pages.dim() != 3:
+        raise ValueError("kv_pages must be [num_pages, page_size, 576]")
+    return DecodeDesc(batch=B, num_heads=H, q_len=q_len, head_dim_qk=dqk, head_dim_v=512,
+                      page_size=kv_pages.shape[1], num_pages=kv_pages.shape[0],
+                      max_pages_per_seq=block_table.shape[1] if block_table.dim() == 2 else 0,
+                      kv_dtype=_kv_dtype_code(kv_pages), kv_scale=float(kv_scale))
+
+
+def workspace_size(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
+                   kv_scale: float = 1.0) -> int:
+    d = _decode_desc(q, kv_pages, block_table, kv_scale)
+    with torch.cuda.device(q.device):
+        n = load_library().mla_decode_workspace_size(ctypes.byref(d), 0)
+    if n == 0:
+        raise MlaError(-2, "cannot size a workspace for these shapes")
+    return n
+
+
+def make_workspace(q, kv_pages, block_table, kv_scale: float = 1.0) -> torch.Tensor:
+    """A zero-filled workspace for these shapes on q's device."""
+    return torch.zeros(workspace_size(q, kv_pages, block_table, kv_scale), dtype=torch.uint8,
+                       device=q.device)
+
+
+def _need(t: torch.Tensor, name: str, dtypes, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def decode_partial(q, kv_pages, block_table, seq_lens, part_id: int, num_parts: int,
+                   sm_scale: float, lse_base: int, out, lse, *, kv_scale: float = 1.0,
+                   workspace: torch.Tensor | None = None, stream=None):
+    """mla_decode_partial on torch tensors (see include/mla_decode.h).
+
+    q bf16 [B,1,H,576]; kv_pages bf16 [pages,64,576] or uint8/float8_e4m3fn;
+    block_table int32 [B,max_pages]; seq_lens int32 [B] (global lengths);
+    out bf16 [B,1,H,512] and lse fp32 [B,1,H] are written in place.
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("decode_partial runs on CUDA tensors only")
+    _need(q, "q", (torch.bfloat16,), dev)
+    _need(kv_pages, "kv_pages", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn), dev)
+    _need(block_table, "block_table", (torch.int32,), dev)
+    _need(seq_lens, "seq_lens", (torch.int32,), dev)
+    _need(out, "out", (torch.bfloat16,), dev)
+    _need(lse, "lse", (torch.float32,), dev)
+    d = _decode_desc(q, kv_pages, block_table, kv_scale)
+    if seq_lens.numel() != d.batch or block_table.dim() != 2 or block_table.shape[0] != d.batch:
+        raise ValueError("seq_lens / block_table do not match the batch")
+    if out.numel() != d.batch * d.q_len * d.num_heads * 512 or lse.numel() != d.batch * d.q_len * d.num_heads:
+        raise ValueError("out must be [B,1,H,512] and lse [B,1,H]")
+    if workspace is None:
+        workspace = make_workspace(q, kv_pages, block_table, kv_scale)
+    _need(workspace, "workspace", (torch.uint8,), dev)
+    with torch.cuda.device(dev):
+        st = load_library().mla_decode_partial(
+            q.data_ptr(), kv_pages.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+            int(part_id), int(num_parts), float(sm_scale), int(lse_base), out.data_ptr(),
+            lse.data_ptr(), ctypes.byref(d), workspace.data_ptr(), workspace.numel(),
+            _stream_ptr(stream, dev))
+    _check(st)
+    return out, lse
+
+
+def check_workspace(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the kernel's bounds
+    status: 0, or -9 if a block-table entry or a length was out of bounds."""
+    with torch.cuda.device(workspace.device):
+        st = load_library().mla_decode_check_workspace(workspace.data_ptr(),
+                                                       _stream_ptr(stream, workspace.device))
+    if st not in (0, -9):
+        _check(st)
+    return st
+
+
+def lse_combine(partials, lses, num_parts: int, out, *, lse_base: int = LSE_NATURAL,
+                out_lse=None, stream=None):
+    """mla_lse_combine: partials bf16 [P,T,H,D], lses fp32 [P,T,H] -> out bf16 [T,H,D]."""
+    dev = partials.device
+    if dev.type != "cuda":
+        raise ValueError("lse_combine runs on CUDA tensors only")
+    _need(partials, "partials", (torch.bfloat16,), dev)
+    _need(lses, "lses", (torch.float32,), dev)
+    _need(out, "out", (torch.bfloat16,), dev)
+    if partials.dim() != 4 or partials.shape[0] != num_parts:
+        raise ValueError("partials must be [num_parts, T, H, D]")
+    P, T, H, D = partials.shape
+    if lses.numel() != P * T * H or out.numel() != T * H * D:
+        raise ValueError("lses must be [P,T,H] and out [T,H,D]")
+    if out_lse is not None:
+        _need(out_lse, "out_lse", (torch.float32,), dev)
+        if out_lse.numel() != T * H:
+            raise ValueError("out_lse must be [T,H]")
+    d = CombineDesc(num_tokens=T, num_heads=H, head_dim=D, lse_base=int(lse_base),
+                    out_lse=out_lse.data_ptr() if out_lse is not None else None)
+    with torch.cuda.device(dev):
+        st = load_library().mla_lse_combine(partials.data_ptr(), lses.data_ptr(), int(num_parts),
+                                            out.data_ptr(), ctypes.byref(d), _stream_ptr(stream, dev))
+    _check(st)
+    return out

@@ -1,0 +1,211 @@
+// Host side of the C ABI declared in include/mla_decode.h: argument checks,
+// workspace sizing, per-device facts, and kernel dispatch.  Nothing here
+// allocates device memory or synchronises the host (except the explicit
+// mla_decode_check_workspace).
+#include "mla_decode.h"
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace mla {
+cudaError_t launch_decode_simt(const DecodeParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_lse_combine(const void *partials, const float *lses, int num_parts, void *out,
+                               float *out_lse, int rows, int dim, int base2, cudaStream_t stream);
+int combine_max_parts();
+}  // namespace mla
+
+namespace {
+
+thread_local char g_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e) {
+  std::snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return MLA_ERR_CUDA;
+}
+
+struct DeviceFacts {
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceFacts g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Facts of the current device; status in *st.
+DeviceFacts current_device(int *st, int *dev_out = nullptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *st = cuda_fail(e);
+    return {};
+  }
+  if (dev_out) *dev_out = dev;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *st = MLA_ERR_DEVICE;
+    return {};
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceFacts &f = g_dev[dev];
+  if (f.sms == 0) {
+    int sms = 0, mj = 0, mn = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&mj, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&mn, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) {
+      *st = cuda_fail(e);
+      return {};
+    }
+    f.sms = sms;
+    f.major = mj;
+    f.minor = mn;
+  }
+  *st = (f.major == 10 && f.minor == 3) ? MLA_OK : MLA_ERR_DEVICE;
+  return f;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kSimtHeadsPerGroup = 32;
+
+int check_desc(const mla_decode_desc *d) {
+  if (!d) return MLA_ERR_NULL;
+  if (d->batch < 0 || d->num_pages < 1 || d->max_pages_per_seq < 1) return MLA_ERR_SHAPE;
+  if (d->q_len != 1) return MLA_ERR_SHAPE;
+  if (d->head_dim_qk != mla::kDqk || d->head_dim_v != mla::kDv) return MLA_ERR_SHAPE;
+  if (d->page_size != mla::kPage) return MLA_ERR_SHAPE;
+  if (d->num_heads < 1 || d->num_heads > 128) return MLA_ERR_SHAPE;
+  if (d->kv_dtype != MLA_KV_BF16 && d->kv_dtype != MLA_KV_E4M3) return MLA_ERR_ARG;
+  if (d->kv_dtype == MLA_KV_E4M3 && !(std::isfinite(d->kv_scale) && d->kv_scale > 0.f))
+    return MLA_ERR_ARG;
+  return MLA_OK;
+}
+
+int head_groups_of(const mla_decode_desc *d) {
+  return (d->num_heads + kSimtHeadsPerGroup - 1) / kSimtHeadsPerGroup;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_version(void) { return 100; }
+
+const char *mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_NULL: return "a required pointer is NULL";
+    case MLA_ERR_SHAPE: return "unsupported shape (q_len must be 1, Dqk 576, Dv 512, page 64, heads 1..128)";
+    case MLA_ERR_PARTITION: return "bad partition (need num_parts >= 1 and 0 <= part_id < num_parts)";
+    case MLA_ERR_ALIGN: return "misaligned pointer (16 B for tensors, 256 B for the workspace)";
+    case MLA_ERR_WORKSPACE: return "workspace too small";
+    case MLA_ERR_ARG: return "bad argument value";
+    case MLA_ERR_CUDA: return "CUDA error (see mla_last_cuda_error)";
+    case MLA_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    case MLA_ERR_BOUNDS: return "block-table entry or sequence length out of bounds";
+    default: return "unknown status";
+  }
+}
+
+const char *mla_last_cuda_error(void) { return g_cuda_error; }
+
+size_t mla_decode_workspace_size(const mla_decode_desc *d, int num_sms) {
+  if (check_desc(d) != MLA_OK) return 0;
+  if (num_sms <= 0) {
+    int st = 0;
+    DeviceFacts f = current_device(&st);
+    if (f.sms <= 0) return 0;
+    num_sms = f.sms;
+  }
+  const int virt = d->batch * head_groups_of(d);
+  return mla::workspace_layout(virt, num_sms).total;
+}
+
+int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block_table,
+                       const int32_t *seq_lens, int part_id, int num_parts, float sm_scale,
+                       int lse_base, void *out, float *lse, const mla_decode_desc *d,
+                       void *workspace, size_t workspace_bytes, mla_stream_t stream) {
+  int st = check_desc(d);
+  if (st != MLA_OK) return st;
+  if (num_parts < 1 || part_id < 0 || part_id >= num_parts) return MLA_ERR_PARTITION;
+  if (lse_base != MLA_LSE_NATURAL && lse_base != MLA_LSE_BASE2) return MLA_ERR_ARG;
+  if (!std::isfinite(sm_scale)) return MLA_ERR_ARG;
+  if (d->batch == 0) return MLA_OK;
+  if (!q || !kv_pages || !block_table || !seq_lens || !out || !lse || !workspace)
+    return MLA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(kv_pages, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+    return MLA_ERR_ALIGN;
+
+  DeviceFacts f = current_device(&st);
+  if (st != MLA_OK) return st;
+  const int groups = head_groups_of(d);
+  const int grid = f.sms;
+  const mla::WorkspaceLayout wl = mla::workspace_layout(d->batch * groups, grid);
+  if (workspace_bytes < wl.total) return MLA_ERR_WORKSPACE;
+
+  mla::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.kv = kv_pages;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.lse = lse;
+  p.ws = static_cast<unsigned char *>(workspace);
+  p.wl = wl;
+  p.batch = d->batch;
+  p.heads = d->num_heads;
+  p.head_groups = groups;
+  p.heads_per_group = kSimtHeadsPerGroup;
+  p.num_pages = d->num_pages;
+  p.max_pages = d->max_pages_per_seq;
+  p.part_id = part_id;
+  p.num_parts = num_parts;
+  p.kv_e4m3 = d->kv_dtype == MLA_KV_E4M3;
+  p.kv_scale = p.kv_e4m3 ? d->kv_scale : 1.f;
+  p.score_scale_log2 = sm_scale * mla::kLog2e;
+  p.lse_base2 = lse_base == MLA_LSE_BASE2;
+  cudaError_t e = mla::launch_decode_simt(p, grid, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
+int mla_decode_check_workspace(void *workspace, mla_stream_t stream) {
+  if (!workspace) return MLA_ERR_NULL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return word ? MLA_ERR_BOUNDS : MLA_OK;
+}
+
+int mla_lse_combine(const void *partials, const float *lses, int num_parts, void *out,
+                    const mla_combine_desc *d, mla_stream_t stream) {
+  if (!d) return MLA_ERR_NULL;
+  if (num_parts < 1 || num_parts > mla::combine_max_parts()) return MLA_ERR_PARTITION;
+  if (d->num_tokens < 0 || d->num_heads < 1) return MLA_ERR_SHAPE;
+  if (d->head_dim < 8 || d->head_dim > 1024 || d->head_dim % 8) return MLA_ERR_SHAPE;
+  if (d->lse_base != MLA_LSE_NATURAL && d->lse_base != MLA_LSE_BASE2) return MLA_ERR_ARG;
+  if (d->num_tokens == 0) return MLA_OK;
+  if (!partials || !lses || !out) return MLA_ERR_NULL;
+  if (!aligned(partials, 16) || !aligned(out, 16) || !aligned(lses, 4) ||
+      (d->out_lse && !aligned(d->out_lse, 4)))
+    return MLA_ERR_ALIGN;
+  int st = 0;
+  current_device(&st);
+  if (st != MLA_OK) return st;
+  const long long rows = (long long)d->num_tokens * d->num_heads;
+  if (rows > (1LL << 30)) return MLA_ERR_SHAPE;
+  cudaError_t e = mla::launch_lse_combine(partials, lses, num_parts, out, d->out_lse, int(rows),
+                                          d->head_dim, d->lse_base == MLA_LSE_BASE2,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+// Shared definitions of the MLA paged-decode kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int kDqk = 576;        // 512 latent + 64 rope
+constexpr int kDv = 512;         // latent = value
+constexpr int kPage = 64;        // tokens per cache page
+constexpr int kTile = 64;        // partition-local tokens per KV tile
+constexpr int kSlotHeads = 64;   // heads per split-partial slot in the workspace
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device error word bits (workspace header).
+constexpr int kErrBadPage = 1;
+constexpr int kErrBadLen = 2;
+
+// Workspace layout (all offsets multiples of 256 bytes):
+//   [0, 256)                 header: int32 error word
+//   counters                 int32[num_virtual_requests] split tickets
+//   slot lse                 fp32[2 * grid][kSlotHeads]   (base-2 lse of a split)
+//   slot out                 fp32[2 * grid][kSlotHeads][512] (normalised split output)
+struct WorkspaceLayout {
+  size_t counters, slot_lse, slot_out, total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline WorkspaceLayout workspace_layout(int num_virtual, int grid) {
+  WorkspaceLayout w;
+  w.counters = 256;
+  w.slot_lse = align256(w.counters + sizeof(int) * size_t(num_virtual));
+  w.slot_out = align256(w.slot_lse + sizeof(float) * size_t(2 * grid) * kSlotHeads);
+  w.total = align256(w.slot_out + sizeof(float) * size_t(2 * grid) * kSlotHeads * kDv);
+  return w;
+}
+
+struct DecodeParams {
+  const __nv_bfloat16 *q;     // [B, 1, H, 576]
+  const void *kv;             // [num_pages, 64, 576] bf16 or e4m3
+  const int32_t *block_table; // [B, max_pages]
+  const int32_t *seq_lens;    // [B]
+  __nv_bfloat16 *out;         // [B, 1, H, 512]
+  float *lse;                 // [B, 1, H]
+  unsigned char *ws;          // workspace base
+  WorkspaceLayout wl;
+  int batch, heads, head_groups, heads_per_group;
+  int num_pages, max_pages;
+  int part_id, num_parts;
+  int kv_e4m3;
+  float kv_scale;             // 1 for bf16
+  float score_scale_log2;     // sm_scale * log2(e): scores kept in the base-2 domain
+  int lse_base2;              // output lse in base 2 (else natural)
+};
+
+// ---------------------------------------------------------------- partition rule
+
+// Tokens owned by partition r of P out of a global length L: t < L, t mod P == r.
+__device__ __forceinline__ int local_len(int L, int P, int r) {
+  return L / P + (r < L % P ? 1 : 0);
+}
+
+// Clamp a global length to what the block table can hold; flag a bad one.
+__device__ __forceinline__ int checked_len(const DecodeParams &p, int b, int *err) {
+  int L = p.seq_lens[b];
+  int cap = p.max_pages * kPage;
+  if (L < 0 || L > cap) {
+    if (err) atomicOr(err, kErrBadLen);
+    L = L < 0 ? 0 : cap;
+  }
+  return L;
+}
+
+__device__ __forceinline__ int request_tiles(const DecodeParams &p, int v) {
+  int b = v / p.head_groups;
+  int L = checked_len(p, b, nullptr);
+  int n = local_len(L, p.num_parts, p.part_id);
+  return (n + kTile - 1) / kTile;
+}
+
+// ---------------------------------------------------------------- split schedule
+//
+// Stream-K split of the concatenated tile sequence of all virtual requests
+// v = b * head_groups + g (tiles_v = ceil(local_len / 64)) over G_eff =
+// min(gridDim.x, T) CTAs: CTA c owns tiles [c*T/G_eff, (c+1)*T/G_eff).  A
+// request crossing a boundary is split; each split writes a normalised fp32
+// partial into slot 2c (the CTA's first request) or 2c+1 (its last), and the
+// CTA that completes a request's ticket merges the splits.
+
+struct CtaRange {
+  long long start, end;   // global tile range of this CTA
+  long long total;        // T
+  int g_eff;              // CTAs that own tiles
+  int v_begin;            // first virtual request with tiles in range
+  long long p_begin;      // tile prefix of v_begin
+};
+
+__device__ __forceinline__ long long sched_start(long long c, long long T, int g_eff) {
+  return c * T / g_eff;
+}
+
+// Largest c with sched_start(c) <= x.
+__device__ __forceinline__ int sched_owner(long long x, long long T, int g_eff) {
+  return int(((x + 1) * g_eff - 1) / T);
+}
+
+// Block-wide: computes this CTA's range.  All threads must call it.
+// `scratch` needs blockDim.x / 32 + 1 long longs of shared memory.
+__device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long long *scratch) {
+  const int V = p.batch * p.head_groups;
+  const int tid = threadIdx.x, nw = blockDim.x / 32, lane = tid & 31, warp = tid >> 5;
+  // pass 1: total tiles
+  long long mine = 0;
+  for (int v = tid; v < V; v += blockDim.x) mine += request_tiles(p, v);
+  for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) scratch[warp] = mine;
+  __syncthreads();
+  if (tid == 0) {
+    long long T = 0;
+    for (int w = 0; w < nw; ++w) T += scratch[w];
+    r->total = T;
+    r->g_eff = int(T < (long long)gridDim.x ? T : (long long)gridDim.x);
+    r->v_begin = V;
+    r->p_begin = 0;
+    if (r->g_eff > 0 && (int)blockIdx.x < r->g_eff) {
+      r->start = sched_start(blockIdx.x, T, r->g_eff);
+      r->end = sched_start(blockIdx.x + 1, T, r->g_eff);
+    } else {
+      r->start = r->end = 0;
+    }
+  }
+  __syncthreads();
+  const long long start = r->start, end = r->end;
+  if (start >= end) return;
+  // pass 2: locate the request holding tile `start` (chunked block scan)
+  long long base = 0;
+  for (int v0 = 0; v0 < V; v0 += blockDim.x) {
+    int v = v0 + tid;
+    long long t = v < V ? request_tiles(p, v) : 0;
+    long long incl = t;
+    for (int o = 1; o < 32; o <<= 1) {
+      long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    __syncthreads();
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    long long wbase = 0, chunk = 0;
+    for (int w = 0; w < nw; ++w) {
+      if (w < warp) wbase += scratch[w];
+      chunk += scratch[w];
+    }
+    long long excl = base + wbase + incl - t;
+    if (t > 0 && excl <= start && start < excl + t) {
+      r->v_begin = v;
+      r->p_begin = excl;
+    }
+    base += chunk;
+    __syncthreads();
+    if (r->v_begin < V) break;  // uniform: read after the barrier
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- conversions
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(uint32_t(b) << 16);
+}
+
+// Two OCP e4m3 bytes -> two exact f16 values (hardware conversion).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+  uint32_t r;
+  asm("{ cvt.rn.f16x2.e4m3x2 %0, %1; }" : "=r"(r) : "h"(two));
+  return r;
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+  uint32_t h = e4m3x2_to_f16x2(two);
+  __half2 hh = *reinterpret_cast<__half2 *>(&h);
+  return __half22float2(hh);
+}
+
+}  // namespace mla

@@ -1,0 +1,139 @@
+"""The C-ABI library: it loads, exports every function include/*.h declares, and
+rejects bad arguments on the host before anything reaches a GPU.
+
+None of these calls launches work: every one fails argument validation first,
+so they run on machines without a GPU.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import mla_paged_decode_gb300 as mla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"\b(mla_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(mla.library_path()):
+        from mla_paged_decode_gb300 import build
+        build.build()
+    return mla.load_library()
+
+
+def test_header_declares_the_two_operations():
+    names = declared_functions()
+    assert "mla_decode_partial" in names and "mla_lse_combine" in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exported_symbols_are_c_linkage():
+    out = os.popen(f"nm -D --defined-only {mla.library_path()}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def _desc(**kw):
+    base = dict(batch=2, num_heads=16, q_len=1, head_dim_qk=576, head_dim_v=512, page_size=64,
+                num_pages=8, max_pages_per_seq=4, kv_dtype=0, kv_scale=1.0)
+    base.update(kw)
+    return mla.DecodeDesc(**base)
+
+
+FAKE = 1 << 20  # a 256-aligned non-null address that is never dereferenced
+
+
+def _partial(lib, d, *, part_id=0, num_parts=1, lse_base=0, sm_scale=0.1, q=FAKE, ws=FAKE,
+             ws_bytes=1 << 40):
+    return lib.mla_decode_partial(q, FAKE, FAKE, FAKE, part_id, num_parts, sm_scale, lse_base,
+                                  FAKE, FAKE, ctypes.byref(d) if d is not None else None,
+                                  ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q_len=2), -2), (dict(q_len=0), -2), (dict(head_dim_qk=512), -2),
+    (dict(head_dim_v=576), -2), (dict(page_size=32), -2), (dict(num_heads=0), -2),
+    (dict(num_heads=129), -2), (dict(num_pages=0), -2), (dict(max_pages_per_seq=0), -2),
+    (dict(batch=-1), -2), (dict(kv_dtype=7), -6), (dict(kv_dtype=1, kv_scale=0.0), -6),
+    (dict(kv_dtype=1, kv_scale=float("nan")), -6),
+])
+def test_bad_descriptor_is_rejected(lib, kw, code):
+    assert _partial(lib, _desc(**kw)) == code
+
+
+def test_bad_partition_is_rejected(lib):
+    for part_id, num_parts in [(0, 0), (-1, 2), (2, 2), (5, 4)]:
+        assert _partial(lib, _desc(), part_id=part_id, num_parts=num_parts) == -3
+
+
+def test_bad_enum_and_scale_are_rejected(lib):
+    assert _partial(lib, _desc(), lse_base=2) == -6
+    assert _partial(lib, _desc(), sm_scale=float("inf")) == -6
+
+
+def test_null_and_misaligned_pointers_are_rejected(lib):
+    assert _partial(lib, None) == -1
+    assert _partial(lib, _desc(), q=0) == -1
+    assert _partial(lib, _desc(), ws=0) == -1
+    assert _partial(lib, _desc(), q=FAKE + 2) == -4
+    assert _partial(lib, _desc(), ws=FAKE + 16) == -4
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _partial(lib, _desc(batch=0), q=0, ws=0) == 0
+
+
+def test_workspace_size_is_sane(lib):
+    d = _desc(batch=64, num_heads=64)
+    n = lib.mla_decode_workspace_size(ctypes.byref(d), 152)
+    assert n > 0 and n % 256 == 0
+    assert lib.mla_decode_workspace_size(ctypes.byref(_desc(q_len=2)), 152) == 0
+    assert lib.mla_decode_workspace_size(None, 152) == 0
+    more = lib.mla_decode_workspace_size(ctypes.byref(d), 304)
+    assert more > n
+
+
+def test_combine_rejects_bad_arguments(lib):
+    def call(num_parts=2, **kw):
+        base = dict(num_tokens=4, num_heads=16, head_dim=512, lse_base=0, out_lse=None)
+        base.update(kw)
+        d = mla.CombineDesc(**base)
+        return lib.mla_lse_combine(FAKE, FAKE, num_parts, FAKE, ctypes.byref(d), None)
+    assert call(num_parts=0) == -3
+    assert call(num_parts=100000) == -3
+    assert call(head_dim=12) == -2
+    assert call(head_dim=0) == -2
+    assert call(num_heads=0) == -2
+    assert call(lse_base=3) == -6
+    assert call(num_tokens=0) == 0
+    assert lib.mla_lse_combine(0, FAKE, 2, FAKE, ctypes.byref(mla.CombineDesc(
+        num_tokens=1, num_heads=1, head_dim=8, lse_base=0, out_lse=None)), None) == -1
+
+
+def test_status_strings(lib):
+    for code in range(-9, 1):
+        assert lib.mla_status_string(code)
+    assert lib.mla_version() >= 100
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 16, 576, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mla.decode_partial(q, q, q, q, 0, 1, 0.1, 0, q, q)

@@ -1,0 +1,191 @@
+"""GPU parity of mla_decode_partial against the fp64 oracle.
+
+Small cases are compared element by element on every request and partition;
+the full-size workloads (the configuration the bench times, in the same launch
+configuration) on sampled requests the oracle computes one by one, plus the
+properties that hold at any size (finite outputs, exact neutral pairs).
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_paged_decode_gb300 as mla
+import oracle
+import workloads
+from casebits import case_bits
+from gpu_helpers import (FP8_ATOL, assert_lse_close, assert_neutral, assert_out_close,
+                         oracle_partial_sub, run_partial)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_paged_decode_gb300 import build
+    build.build()
+    mla.load_library()
+
+
+def _check_all(case, bases=(0, 1), atol=None):
+    q, kv, bt, lens = case_bits(case)
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table, case.kv_scale)
+    for r in range(case.num_parts):
+        for base in bases:
+            out, lse = run_partial(case, r, base, workspace=ws)
+            ro, rl = oracle.decode_partial(q, kv, bt, lens, r, case.num_parts, case.sm_scale,
+                                           base, kv_dtype=case.kv_dtype, kv_scale=case.kv_scale)
+            what = f"{case.name} part {r} base {base}"
+            assert_out_close(out, ro[:, None], **({"atol": atol} if atol else {}), what=what)
+            assert_lse_close(lse, rl[:, None], base, what=what)
+            empties = [b for b in range(case.batch) if oracle.local_len(int(lens[b]), case.num_parts, r) == 0]
+            assert_neutral(out, lse, empties)
+    assert mla.check_workspace(ws) == 0
+
+
+def test_small_config_partials_then_combine():
+    case = workloads.config_small(device="cuda")
+    _check_all(case)
+    q, kv, bt, lens = case_bits(case)
+    for base in (0, 1):
+        parts = [run_partial(case, r, base) for r in range(2)]
+        P = torch.stack([o.view(1, 16, 512) for o, _ in parts])     # [P, T=1, H, D]
+        L = torch.stack([l.view(1, 16) for _, l in parts])
+        merged = torch.empty(1, 16, 512, dtype=torch.bfloat16, device="cuda")
+        merged_lse = torch.empty(1, 16, dtype=torch.float32, device="cuda")
+        mla.lse_combine(P, L, 2, merged, lse_base=base, out_lse=merged_lse)
+        fo, fl = oracle.decode_full(q, kv, bt, lens, case.sm_scale, base)
+        assert_out_close(merged, fo, what=f"merged base {base}")
+        assert_lse_close(merged_lse, fl, base, what=f"merged base {base}")
+
+
+SHAPES = [
+    # heads, lens, num_parts, kv dtype
+    (16, [0, 1, 63, 64, 65, 129, 300], 1, "bf16"),
+    (64, [5, 64, 200, 1000, 0, 4097], 1, "bf16"),
+    (1, [77, 3000, 2], 2, "bf16"),
+    (32, [1, 2, 3, 8, 130, 999], 3, "bf16"),
+    (16, [1, 3, 5, 7, 511, 1025], 8, "bf16"),
+    (128, [700, 64, 1, 0], 2, "bf16"),
+    (64, [1500, 33, 0, 640], 4, "e4m3"),
+    (128, [900, 1, 65], 1, "e4m3"),
+    (16, [300, 17], 5, "e4m3"),
+]
+
+
+@pytest.mark.parametrize("heads,lens,num_parts,kv_dtype", SHAPES)
+def test_random_shapes_with_poisoned_tails(heads, lens, num_parts, kv_dtype):
+    """Unused rows of the last page and all unowned pages hold NaN: they must
+    never reach an output."""
+    case = workloads.make_decode_case(f"h{heads}_p{num_parts}_{kv_dtype}", heads, lens,
+                                      num_parts=num_parts, kv_dtype=kv_dtype, seed=heads + num_parts,
+                                      device="cuda", tail_poison=True, pool_pages=sum(
+                                          (L + 63) // 64 for L in lens) + 3)
+    _check_all(case, atol=FP8_ATOL if kv_dtype == "e4m3" else None)
+
+
+def test_single_request_spread_over_every_cta():
+    """One long request: every CTA holds a split, the last one merges them."""
+    case = workloads.make_decode_case("one_long", 64, [150000], seed=21, device="cuda")
+    out, lse = run_partial(case, 0, 0)
+    ro, rl = oracle_partial_sub(oracle, case, [0], 0, 0)
+    assert_out_close(out, ro[:, None], what="one long request")
+    assert_lse_close(lse, rl[:, None], 0)
+
+
+def test_long32k_full_size_sampled():
+    case = workloads.config_long32k(device="cuda")
+    out, lse = run_partial(case, 0, 0)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    lens = case.seq_lens.cpu()
+    sample = sorted({0, 31, 63, int(lens.argmax()), int(lens.argmin())})
+    ro, rl = oracle_partial_sub(oracle, case, sample, 0, 0)
+    assert_out_close(out[sample], ro[:, None], what="long32k sample")
+    assert_lse_close(lse[sample], rl[:, None], 0, what="long32k sample")
+
+
+def test_dcp8_full_size_partials_and_combine():
+    case = workloads.config_dcp8(device="cuda")
+    B, H = case.batch, case.heads
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table)
+    outs = torch.empty(8, B, 1, H, 512, dtype=torch.bfloat16, device="cuda")
+    lses = torch.empty(8, B, 1, H, dtype=torch.float32, device="cuda")
+    for r in range(8):
+        run_partial(case, r, 1, workspace=ws, out=outs[r], lse=lses[r])
+    assert mla.check_workspace(ws) == 0
+    short = [60, 61, 62, 63]   # L = 1, 3, 5, 7
+    sample = [0, 59] + short
+    for r in range(8):
+        ro, rl = oracle_partial_sub(oracle, case, sample, r, 1)
+        assert_out_close(outs[r][sample], ro[:, None], what=f"dcp8 part {r}")
+        assert_lse_close(lses[r][sample], rl[:, None], 1, what=f"dcp8 part {r}")
+        lens = case.seq_lens.cpu().tolist()
+        assert_neutral(outs[r], lses[r], [b for b in short if r >= lens[b]])
+    merged = torch.empty(B, H, 512, dtype=torch.bfloat16, device="cuda")
+    mla.lse_combine(outs.view(8, B, H, 512), lses.view(8, B, H), 8, merged, lse_base=1)
+    fo, _ = oracle_partial_sub(oracle, case, sample, 0, 1, num_parts=1)
+    assert_out_close(merged[sample], fo, what="dcp8 merged vs unpartitioned")
+
+
+def test_fp8_full_size_sampled():
+    case = workloads.config_fp8(device="cuda")
+    out, lse = run_partial(case, 0, 0)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    sample = [0, 1, 64, 127]
+    ro, rl = oracle_partial_sub(oracle, case, sample, 0, 0)
+    assert_out_close(out[sample], ro[:, None], atol=FP8_ATOL, what="fp8 sample")
+    assert_lse_close(lse[sample], rl[:, None], 0, what="fp8 sample")
+
+
+def test_outputs_are_deterministic_and_placement_free():
+    case = workloads.make_decode_case("det", 64, [5000, 77, 12000], seed=4, device="cuda",
+                                      num_parts=2, pool_pages=400)
+    a = run_partial(case, 1, 0)
+    b = run_partial(case, 1, 0)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1])
+    perm = torch.randperm(case.num_pages, generator=torch.Generator().manual_seed(1)).cuda()
+    kv2 = torch.empty_like(case.kv_pages)
+    kv2[perm] = case.kv_pages
+    bt2 = perm[case.block_table.long()].to(torch.int32)
+    moved = workloads.DecodeCase(case.name, case.q, kv2, bt2, case.seq_lens, case.kv_dtype,
+                                 case.kv_scale, case.sm_scale, case.num_parts)
+    c = run_partial(moved, 1, 0)
+    assert torch.equal(a[0].view(torch.int16), c[0].view(torch.int16))
+    assert torch.equal(a[1], c[1])
+
+
+def test_bounds_are_checked_in_the_kernel():
+    """An out-of-range page index and an over-long length are skipped and
+    reported, never dereferenced."""
+    case = workloads.make_decode_case("bounds", 16, [130, 64], seed=2, device="cuda")
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table)
+    run_partial(case, 0, 0, workspace=ws)
+    assert mla.check_workspace(ws) == 0
+    bad = case.block_table.clone()
+    bad[0, 1] = case.num_pages + 1000
+    broken = workloads.DecodeCase(case.name, case.q, case.kv_pages, bad, case.seq_lens,
+                                  case.kv_dtype, case.kv_scale, case.sm_scale, 1)
+    run_partial(broken, 0, 0, workspace=ws)
+    assert mla.check_workspace(ws) == -9
+    too_long = case.seq_lens.clone()
+    too_long[1] = 64 * case.block_table.shape[1] + 1
+    broken = workloads.DecodeCase(case.name, case.q, case.kv_pages, case.block_table, too_long,
+                                  case.kv_dtype, case.kv_scale, case.sm_scale, 1)
+    run_partial(broken, 0, 0, workspace=ws)
+    assert mla.check_workspace(ws) == -9
+    run_partial(case, 0, 0, workspace=ws)
+    assert mla.check_workspace(ws) == 0
+
+
+def test_multi_token_query_is_rejected():
+    case = workloads.config_small(device="cuda")
+    q2 = torch.zeros(1, 2, 16, 576, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(1, 2, 16, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(1, 2, 16, dtype=torch.float32, device="cuda")
+    with pytest.raises(mla.MlaError) as e:
+        mla.decode_partial(q2, case.kv_pages, case.block_table, case.seq_lens, 0, 1,
+                           case.sm_scale, 0, out, lse, workspace=torch.zeros(
+                               1 << 20, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == -2
