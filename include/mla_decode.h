@@ -131,6 +131,32 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
                        void *workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /*
+ * mla_decode_partial without a workspace argument.  The method on the pages
+ * has no counterpart of this call: it exists for callers that cannot call
+ * cudaMalloc -- runtimes that give every byte of HBM to their own KV-cache
+ * pool and let no library allocate, decode loops that cannot absorb the
+ * device synchronisation an allocation may cause, and plain-C hosts with no
+ * allocator of their own.
+ *
+ * Same arguments, layouts and results as mla_decode_partial.  Its scratch is
+ * a ~40 MB array built into the library, which every GPU that loads the
+ * library keeps until the process exits; it calls no cudaMalloc, cudaFree or
+ * other allocating routine.  The first call on a device takes that device's
+ * address of the array (the device must be current), so make that first call
+ * before any stream capture.  Limit: batch * ceil(num_heads / 32) <= 16384;
+ * larger batches return MLA_ERR_WORKSPACE without launching.  All calls share
+ * the one array: calls that may overlap on the GPU (different streams, or
+ * different host threads) race and must be serialised by the caller.  Each
+ * call clears the array's counters before its kernel; kernel-side bounds
+ * errors are not reported by this variant (use mla_decode_partial with
+ * mla_decode_check_workspace to diagnose them).
+ */
+int mla_decode_partial_noalloc(const void *q, const void *kv_pages, const int32_t *block_table,
+                               const int32_t *seq_lens, int part_id, int num_parts,
+                               float sm_scale, int lse_base, void *out, float *lse,
+                               const mla_decode_desc *d, mla_stream_t stream);
+
+/*
  * Waits for `stream`, reads and clears the device error word of `workspace`.
  * Returns MLA_OK, MLA_ERR_BOUNDS, or MLA_ERR_CUDA.  (The one call that
  * synchronises; meant for tests and debugging.)

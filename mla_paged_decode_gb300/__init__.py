@@ -16,6 +16,7 @@ import torch
 __all__ = [
     "MlaError", "LSE_NATURAL", "LSE_BASE2", "decode_partial", "lse_combine",
     "workspace_size", "make_workspace", "check_workspace", "library_path", "load_library",
+    "decode_partial_noalloc",
 ]
 
 LSE_NATURAL = 0
@@ -215,3 +216,34 @@ def lse_combine(partials, lses, num_parts: int, out, *, lse_base: int = LSE_NATU
                                             out.data_ptr(), ctypes.byref(d), _stream_ptr(stream, dev))
     _check(st)
     return out
+
+
+def decode_partial_noalloc(q, kv_pages, block_table, seq_lens, part_id: int, num_parts: int,
+                           sm_scale: float, lse_base: int, out, lse, *, kv_scale: float = 1.0,
+                           stream=None):
+    """mla_decode_partial_noalloc: the same call without a workspace, for
+    callers that cannot allocate device memory (see include/mla_decode.h).
+    It uses scratch built into the library, shared by every call: calls that
+    may overlap on the GPU must be serialised by the caller."""
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("decode_partial_noalloc runs on CUDA tensors only")
+    _need(q, "q", (torch.bfloat16,), dev)
+    _need(kv_pages, "kv_pages", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn), dev)
+    _need(block_table, "block_table", (torch.int32,), dev)
+    _need(seq_lens, "seq_lens", (torch.int32,), dev)
+    _need(out, "out", (torch.bfloat16,), dev)
+    _need(lse, "lse", (torch.float32,), dev)
+    d = _decode_desc(q, kv_pages, block_table, kv_scale)
+    lib = load_library()
+    fn = lib.mla_decode_partial_noalloc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, vp, vp,
+                   ctypes.POINTER(DecodeDesc), vp]
+    fn.restype = i32
+    with torch.cuda.device(dev):
+        st = fn(q.data_ptr(), kv_pages.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+                int(part_id), int(num_parts), float(sm_scale), int(lse_base), out.data_ptr(),
+                lse.data_ptr(), ctypes.byref(d), _stream_ptr(stream, dev))
+    _check(st)
+    return out, lse
