@@ -221,7 +221,9 @@ def run_ours(args, world, rank, local):
     barrier(world)
     mla.load_library()
 
-    case = workloads.config_long32k(device=dev, seed=args.seed)
+    case = workloads.config_long32k(device=dev, seed=args.seed, batch=args.batch)
+    if args.batch != 64:
+        case.name += f"_b{args.batch}"
     B, H = case.batch, case.heads
     kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
     out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
@@ -386,6 +388,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=64,
+                    help="requests per step (64 = the headline workload; smaller only for profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -52,9 +52,11 @@ enum mla_status {
   MLA_ERR_ARG = -6,       /* bad enum value, non-finite scale, negative size      */
   MLA_ERR_CUDA = -7,      /* a CUDA call failed; see mla_last_cuda_error()        */
   MLA_ERR_DEVICE = -8,    /* current device is not an sm_103 GPU                  */
-  MLA_ERR_BOUNDS = -9     /* (from mla_decode_check_workspace) the kernel met a
+  MLA_ERR_BOUNDS = -9,    /* (from mla_decode_check_workspace) the kernel met a
                              block-table entry outside [0, num_pages) or a sequence
                              length outside [0, 64 * max_pages_per_seq]            */
+  MLA_ERR_TIMEOUT = -10   /* (from mla_decode_check_workspace) a bounded wait
+                             inside the kernel gave up; outputs are unspecified   */
 };
 
 enum mla_lse_base {
@@ -158,7 +160,7 @@ int mla_decode_partial_noalloc(const void *q, const void *kv_pages, const int32_
 
 /*
  * Waits for `stream`, reads and clears the device error word of `workspace`.
- * Returns MLA_OK, MLA_ERR_BOUNDS, or MLA_ERR_CUDA.  (The one call that
+ * Returns MLA_OK, MLA_ERR_TIMEOUT, MLA_ERR_BOUNDS, or MLA_ERR_CUDA.  (The one call that
  * synchronises; meant for tests and debugging.)
  */
 int mla_decode_check_workspace(void *workspace, mla_stream_t stream);

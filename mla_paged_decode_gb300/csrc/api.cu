@@ -4,6 +4,8 @@
 // mla_decode_check_workspace).
 #include "mla_decode.h"
 
+#include <cuda.h>
+
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -13,6 +15,9 @@
 
 namespace mla {
 cudaError_t launch_decode_simt(const DecodeParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
+                             const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
+                             cudaStream_t stream);
 cudaError_t launch_lse_combine(const void *partials, const float *lses, int num_parts, void *out,
                                float *out_lse, int rows, int dim, int base2, cudaStream_t stream);
 int combine_max_parts();
@@ -70,6 +75,79 @@ DeviceFacts current_device(int *st, int *dev_out = nullptr) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the
+// library does not link the driver library directly).
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(f);
+  });
+  return fn;
+}
+
+int tensor_map_fail(const char *what, CUresult r) {
+  std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled(%s) failed: %d", what,
+                int(r));
+  return MLA_ERR_CUDA;
+}
+
+constexpr int kTcHeadsPerGroup = 64;
+
+// The tensor-core kernel takes bf16 caches and partitions whose owned rows of
+// a page form whole 8-row groups (P | 8).
+bool tensor_core_path(const mla_decode_desc *d, int num_parts) {
+  return d->kv_dtype == MLA_KV_BF16 &&
+         (num_parts == 1 || num_parts == 2 || num_parts == 4 || num_parts == 8);
+}
+
+// Q as [B*H rows, 576] bf16, one 64-column swizzled box of min(64, H) rows;
+// partition r's rows of the cache as a 4-D view (64 dims, 8 rows of stride P,
+// 9 blocks of 64 dims, groups of 8 rows), one box = one page's owned rows.
+int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, int part_id,
+                     int num_parts, CUtensorMap *tm_q, CUtensorMap *tm_kv) {
+  EncodeTiled enc = encode_tiled();
+  if (!enc) {
+    std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled unavailable");
+    return MLA_ERR_CUDA;
+  }
+  const cuuint64_t row = cuuint64_t(mla::kDqk) * 2;
+  {
+    cuuint64_t dims[2] = {cuuint64_t(mla::kDqk), cuuint64_t(d->batch) * cuuint64_t(d->num_heads)};
+    cuuint64_t strides[1] = {row};
+    cuuint32_t box[2] = {64, cuuint32_t(d->num_heads < 64 ? d->num_heads : 64)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return tensor_map_fail("q", r);
+  }
+  {
+    const cuuint64_t P = cuuint64_t(num_parts);
+    const cuuint32_t G = cuuint32_t(8 / num_parts);
+    const char *base = static_cast<const char *>(kv) + size_t(part_id) * row;
+    cuuint64_t dims[4] = {64, 8, cuuint64_t(mla::kDqk / 64), cuuint64_t(d->num_pages) * G};
+    cuuint64_t strides[3] = {P * row, 128, 8 * P * row};
+    cuuint32_t box[4] = {64, 8, cuuint32_t(mla::kDqk / 64), G};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<char *>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return tensor_map_fail("kv", r);
+  }
+  return MLA_OK;
+}
+
 constexpr int kSimtHeadsPerGroup = 32;
 
 int check_desc(const mla_decode_desc *d) {
@@ -107,6 +185,7 @@ const char *mla_status_string(int status) {
     case MLA_ERR_CUDA: return "CUDA error (see mla_last_cuda_error)";
     case MLA_ERR_DEVICE: return "current device is not an sm_103 GPU";
     case MLA_ERR_BOUNDS: return "block-table entry or sequence length out of bounds";
+    case MLA_ERR_TIMEOUT: return "a bounded wait inside the kernel gave up";
     default: return "unknown status";
   }
 }
@@ -143,10 +222,13 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
 
   DeviceFacts f = current_device(&st);
   if (st != MLA_OK) return st;
-  const int groups = head_groups_of(d);
+  const bool tc = tensor_core_path(d, num_parts);
+  const int per_group = tc ? kTcHeadsPerGroup : kSimtHeadsPerGroup;
+  const int groups = (d->num_heads + per_group - 1) / per_group;
   const int grid = f.sms;
+  if (workspace_bytes < mla::workspace_layout(d->batch * head_groups_of(d), grid).total)
+    return MLA_ERR_WORKSPACE;
   const mla::WorkspaceLayout wl = mla::workspace_layout(d->batch * groups, grid);
-  if (workspace_bytes < wl.total) return MLA_ERR_WORKSPACE;
 
   mla::DecodeParams p;
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -160,7 +242,7 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
   p.batch = d->batch;
   p.heads = d->num_heads;
   p.head_groups = groups;
-  p.heads_per_group = kSimtHeadsPerGroup;
+  p.heads_per_group = per_group;
   p.num_pages = d->num_pages;
   p.max_pages = d->max_pages_per_seq;
   p.part_id = part_id;
@@ -169,7 +251,18 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
   p.kv_scale = p.kv_e4m3 ? d->kv_scale : 1.f;
   p.score_scale_log2 = sm_scale * mla::kLog2e;
   p.lse_base2 = lse_base == MLA_LSE_BASE2;
-  cudaError_t e = mla::launch_decode_simt(p, grid, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (tc) {
+    CUtensorMap tm_q, tm_kv;
+    st = make_tensor_maps(q, kv_pages, d, part_id, num_parts, &tm_q, &tm_kv);
+    if (st != MLA_OK) return st;
+    const int h = d->num_heads < kTcHeadsPerGroup ? d->num_heads : kTcHeadsPerGroup;
+    const int npv = ((h + 15) / 16) * 16;
+    e = mla::launch_decode_tc(p, npv, h, 8 / num_parts, tm_q, tm_kv, grid, s);
+  } else {
+    e = mla::launch_decode_simt(p, grid, s);
+  }
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 
@@ -182,6 +275,7 @@ int mla_decode_check_workspace(void *workspace, mla_stream_t stream) {
   if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e);
+  if (word & mla::kErrTimeout) return MLA_ERR_TIMEOUT;
   return word ? MLA_ERR_BOUNDS : MLA_OK;
 }
 

@@ -18,6 +18,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Device error word bits (workspace header).
 constexpr int kErrBadPage = 1;
 constexpr int kErrBadLen = 2;
+constexpr int kErrTimeout = 4;   // a bounded wait inside the kernel gave up
 
 // Workspace layout (all offsets multiples of 256 bytes):
 //   [0, 256)                 header: int32 error word

@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(kSimtThreads, 1) decode_simt_kernel(DecodePara
         if (lane == 0) slot_lse_ptr(p)[si.slot * kSlotHeads + hl] = lse2;
       }
     }
-    if (split && split_ticket(p, v, si.nsplits, &s.flag)) merge_splits(p, r, v, pv, si, s.m, s.inv);
+    if (split && split_ticket(p, v, si.nsplits, &s.flag, tid, CtaSync{}))
+      merge_splits(p, r, v, pv, si, s.m, s.inv, tid, kSimtThreads, CtaSync{});
     pv += tiles;
     ++v;
   }

@@ -1,0 +1,554 @@
+// Tensor-core decode kernel for sm_103a: one CTA per SM walks its stream-K
+// range of 64-token tiles; TMA stages the partition's KV rows, tcgen05 MMAs
+// compute S = Q K^T (heads as M = 64) and O^T = V^T P^T (value dims as M =
+// 128, heads as N) with fp32 accumulators in TMEM, and a warpgroup runs the
+// online softmax between them.
+//
+// Roles (256 threads):
+//   warp 0, lane 0  TMA producer: Q of each request (9 boxes of 64 dims) and,
+//                   per tile, one 4-D box per page holding the 64/P rows the
+//                   partition owns, into a [atom][dim block][8 rows][128 B]
+//                   swizzled layout that serves both MMAs.
+//   warp 1          TMEM owner (alloc/free); lane 0 issues the MMAs.
+//   warps 4..7      softmax and epilogue.  The S accumulator (M = 64) puts
+//                   head 16q + i in TMEM lane 32q + i, so warp q's lanes 0..15
+//                   each own one head's row of 64 token scores.  Every thread
+//                   owns TMEM lane 32q + lane of O^T: one value dimension.
+//
+// Pipeline per tile i (stage / S buffer i mod 2): producer -> kv_full ->
+// MMA S_i (36 MMAs, two interleaved accumulators so consecutive MMAs are
+// independent) -> s_full -> softmax reads S_i, frees it (s_free), waits for
+// PV_{i-1} (p_free), rescales O^T only when some head's running max grew by
+// more than 2^8, writes P_i (bf16) -> p_full -> MMA PV_i (4 independent
+// value-dim chunks) -> kv_empty + p_free.  The MMA thread issues S_{i+1} as
+// soon as tile i+1 lands, so the score MMAs of the next tile overlap this
+// tile's softmax, and the producer keeps the pages of the tile two ahead
+// streaming into L2.
+#include "common.cuh"
+#include "sm100.cuh"
+#include "splits.cuh"
+
+namespace mla {
+using namespace sm100;
+
+namespace tc {
+constexpr int kThreads = 256;
+constexpr int kHeads = 64;                   // heads per virtual request (M of S)
+constexpr int kKb = kDqk / 64;               // 9 blocks of 64 bf16 = 128 B
+constexpr int kQBytes = kKb * 64 * 128;      // [kb][64 rows][128 B]
+constexpr int kAtomBytes = kKb * 1024;       // 8 tokens x 576 dims: [kb][8][128 B]
+constexpr int kStageBytes = 8 * kAtomBytes;  // 64 tokens
+constexpr int kPBytes = 64 * 128;            // P [64 heads][64 tokens] bf16
+constexpr int kOffQ = 0;
+constexpr int kOffKv = kOffQ + kQBytes;
+constexpr int kOffP = kOffKv + 2 * kStageBytes;
+constexpr int kOffMisc = kOffP + kPBytes;
+constexpr int kSmemBytes = 232448;           // per-block maximum on sm_100 parts
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;                // O^T chunk c: columns [64c, 64c + npv)
+constexpr uint32_t kColS = 256;              // S(buffer s, chain k): 256 + 64 (2s + k)
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 200000000ull;
+constexpr float kRescaleThreshold = 8.f;     // base-2 units
+}  // namespace tc
+
+struct TcParams {
+  DecodeParams p;
+  int npv;              // N of the PV MMA: heads rounded up to 16 (16..64)
+  int q_rows;           // rows of one Q box: min(64, H)
+  int groups_per_page;  // 8-row atoms one page holds for this partition: 8 / P
+};
+
+struct TcMisc {
+  uint64_t kv_full[2], kv_empty[2], q_full, q_empty, s_full[2], s_free[2];
+  uint64_t p_full, p_free, o_full, o_free, drain;
+  uint32_t tmem_base;
+  int abort;
+  int flag;
+  float alpha[2][64];
+  float ell[64];
+  float merge_m[kSlotHeads], merge_inv[kSlotHeads];
+  CtaRange range;
+  long long scratch[tc::kThreads / 32 + 1];
+};
+static_assert(sizeof(TcMisc) + 1024 <= tc::kSmemBytes - tc::kOffMisc, "shared memory budget");
+
+// The requests (and tile ranges) this CTA owns, in order; every role walks it.
+struct Walk {
+  const DecodeParams &p;
+  const CtaRange &r;
+  int V, v, b, g, n, tiles;
+  long long pv, t0, t1;
+  __device__ Walk(const DecodeParams &p_, const CtaRange &r_)
+      : p(p_), r(r_), V(p_.batch * p_.head_groups), v(r_.v_begin), pv(r_.p_begin) {}
+  __device__ bool next() {
+    while (v < V && pv < r.end) {
+      tiles = request_tiles(p, v);
+      if (tiles == 0) { ++v; continue; }
+      t0 = max(r.start, pv) - pv;
+      t1 = min(r.end, pv + tiles) - pv;
+      b = v / p.head_groups;
+      g = v % p.head_groups;
+      n = local_len(checked_len(p, b, nullptr), p.num_parts, p.part_id);
+      return true;
+    }
+    return false;
+  }
+  __device__ void advance() { pv += tiles; ++v; }
+};
+
+// One position in the walk: request + tile.
+struct TileCursor {
+  Walk w;
+  long long t;
+  bool live;
+  __device__ TileCursor(const DecodeParams &p, const CtaRange &r) : w(p, r), t(0) {
+    live = w.next();
+    if (live) t = w.t0;
+  }
+  __device__ void step() {
+    if (++t >= w.t1) {
+      w.advance();
+      live = w.next();
+      if (live) t = w.t0;
+    }
+  }
+  __device__ bool first() const { return t == w.t0; }
+  __device__ bool last() const { return t == w.t1 - 1; }
+  __device__ int nv() const { return min(kTile, w.n - int(t) * kTile); }
+};
+
+__device__ __forceinline__ uint32_t bar_addr(uint64_t &b) { return smem_u32(&b); }
+
+// Logical pages [lp0, lp1] that hold tile t's owned tokens (n tokens owned).
+__device__ __forceinline__ void tile_pages(const DecodeParams &p, long long t, int n, int *lp0,
+                                           int *lp1) {
+  const int jl = min(int(t) * kTile + kTile, n) - 1;
+  *lp0 = int(t) * p.num_parts;
+  *lp1 = int((p.part_id + (long long)p.num_parts * jl) / kPage);
+}
+
+// ------------------------------------------------------------------ producer
+
+constexpr int kPrefetchAhead = 2;  // tiles whose pages are pulled into L2 ahead of the stage
+
+__device__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
+                            uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
+                            int *err) {
+  using namespace tc;
+  const DecodeParams &p = tp.p;
+  volatile int *abort = &m.abort;
+  uint32_t kv_it = 0, q_it = 0;
+  int last_q = -1, last_kv[2] = {-1, -1};
+  const uint32_t page_bytes = uint32_t(tp.groups_per_page) * kAtomBytes;
+  bool ok = true;
+
+  // L2 prefetch of the pages of the tile kPrefetchAhead positions ahead: the
+  // 129 MB L2 gives the two shared-memory stages more HBM requests in flight.
+  TileCursor ahead(p, r);
+  auto prefetch = [&]() {
+    if (!ahead.live) return;
+    int lp0, lp1;
+    tile_pages(p, ahead.t, ahead.w.n, &lp0, &lp1);
+    for (int k = 0; k <= lp1 - lp0; ++k) {
+      const int pg = p.block_table[size_t(ahead.w.b) * p.max_pages + lp0 + k];
+      if (pg >= 0 && pg < p.num_pages) tma_prefetch_4d(tm_kv, 0, 0, 0, pg * tp.groups_per_page);
+    }
+    ahead.step();
+  };
+  for (int i = 0; i < kPrefetchAhead; ++i) prefetch();
+
+  TileCursor cur(p, r);
+  while (cur.live) {
+    if (cur.first()) {
+      checked_len(p, cur.w.b, err);
+      if (!mbar_wait(bar_addr(m.q_empty), (q_it & 1) ^ 1, abort, kTimeoutNs)) { ok = false; break; }
+      mbar_arrive_expect_tx(bar_addr(m.q_full), uint32_t(kKb * tp.q_rows * 128));
+      for (int kb = 0; kb < kKb; ++kb)
+        tma_load_2d(sQ + kb * (64 * 128), tm_q, bar_addr(m.q_full), kb * 64,
+                    cur.w.b * p.heads + cur.w.g * kHeads);
+      last_q = q_it & 1;
+      ++q_it;
+    }
+    const int s = kv_it & 1;
+    if (!mbar_wait(bar_addr(m.kv_empty[s]), ((kv_it >> 1) & 1) ^ 1, abort, kTimeoutNs)) {
+      ok = false;
+      break;
+    }
+    int lp0, lp1;
+    tile_pages(p, cur.t, cur.w.n, &lp0, &lp1);
+    int pages[8];
+    uint32_t bytes = 0;
+    for (int k = 0; k <= lp1 - lp0; ++k) {
+      int pg = p.block_table[size_t(cur.w.b) * p.max_pages + lp0 + k];
+      if (pg < 0 || pg >= p.num_pages) {
+        atomicOr(err, kErrBadPage);
+        pg = -1;
+      } else {
+        bytes += page_bytes;
+      }
+      pages[k] = pg;
+    }
+    mbar_arrive_expect_tx(bar_addr(m.kv_full[s]), bytes);
+    for (int k = 0; k <= lp1 - lp0; ++k)
+      if (pages[k] >= 0)
+        tma_load_4d(sKv + s * kStageBytes + k * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0, 0, 0,
+                    pages[k] * tp.groups_per_page);
+    last_kv[s] = (kv_it >> 1) & 1;
+    ++kv_it;
+    prefetch();
+    cur.step();
+  }
+  if (!ok) atomicOr(err, kErrTimeout);
+  // never leave the CTA with a copy still in flight into its shared memory
+  if (last_q >= 0) mbar_wait_drain(bar_addr(m.q_full), last_q, kDrainNs);
+  for (int s = 0; s < 2; ++s)
+    if (last_kv[s] >= 0) mbar_wait_drain(bar_addr(m.kv_full[s]), last_kv[s], kDrainNs);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+//
+// One thread, two cursors over the same tile sequence: S(k) needs tile k in
+// its stage, Q of its request and S buffer k mod 2 free; PV(k) needs P(k)
+// (and, for a request's first tile, O^T free).  Whichever is ready is issued,
+// PV first because it frees a stage for the next load.
+
+__device__ void tc_mma(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
+                       uint32_t sKv, uint32_t sP, uint32_t tmem, int *err) {
+  using namespace tc;
+  const DecodeParams &p = tp.p;
+  volatile int *abort = &m.abort;
+  const uint32_t idesc_s = idesc_bf16_f32(64, 64, false, false);
+  const uint32_t idesc_o = idesc_bf16_f32(128, tp.npv, true, false);
+  uint32_t s_it = 0, pv_it = 0, q_it = 0, o_it = 0;
+  TileCursor sc(p, r), pc(p, r);
+  bool ok = true;
+  uint64_t idle_since = globaltimer();
+
+  while (pc.live) {
+    bool progress = false;
+    // ---- PV(pv_it): O^T(chunk c) (+)= V^T P^T over ceil(nv/16) steps of 16 tokens
+    if (pv_it < s_it && mbar_test_wait(bar_addr(m.p_full), pv_it & 1) &&
+        (!pc.first() || mbar_test_wait(bar_addr(m.o_free), (o_it & 1) ^ 1))) {
+      tc_fence_after();
+      const int st = pv_it & 1;
+      const uint32_t stage = sKv + st * kStageBytes;
+      const int ksteps = (pc.nv() + 15) >> 4;
+      const bool fresh = pc.first();
+      for (int ks = 0; ks < ksteps; ++ks) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint64_t a = smem_desc_sw128(stage + 2 * ks * kAtomBytes + 2 * c * 1024, 1024,
+                                             kAtomBytes);
+          const uint64_t bdesc = smem_desc_sw128(sP + ks * 32, 16, 1024);
+          mma_bf16_ss(tmem + kColO + 64 * c, a, bdesc, idesc_o, !(fresh && ks == 0));
+        }
+      }
+      mma_commit(bar_addr(m.kv_empty[st]));
+      mma_commit(bar_addr(m.p_free));
+      if (pc.last()) {
+        mma_commit(bar_addr(m.o_full));
+        ++o_it;
+      }
+      ++pv_it;
+      pc.step();
+      progress = true;
+    }
+    // ---- S(s_it) = Q K^T, 36 K-steps alternating between two accumulators
+    if (sc.live) {
+      const int st = s_it & 1;
+      const uint32_t ph = (s_it >> 1) & 1;
+      if (mbar_test_wait(bar_addr(m.kv_full[st]), ph) &&
+          (!sc.first() || mbar_test_wait(bar_addr(m.q_full), q_it & 1)) &&
+          mbar_test_wait(bar_addr(m.s_free[st]), ph ^ 1)) {
+        tc_fence_after();
+        if (sc.first()) ++q_it;
+        const uint32_t stage = sKv + st * kStageBytes;
+#pragma unroll 4
+        for (int ks = 0; ks < kKb * 4; ++ks) {
+          const int kb = ks >> 2, sub = ks & 3;
+          const uint64_t a = smem_desc_sw128(sQ + kb * (64 * 128) + sub * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc_sw128(stage + kb * 1024 + sub * 32, 16, kAtomBytes);
+          mma_bf16_ss(tmem + kColS + 64 * (2 * st + (ks & 1)), a, bdesc, idesc_s, ks >= 2);
+        }
+        mma_commit(bar_addr(m.s_full[st]));
+        if (sc.last()) mma_commit(bar_addr(m.q_empty));
+        ++s_it;
+        sc.step();
+        progress = true;
+      }
+    }
+    if (progress) {
+      idle_since = globaltimer();
+    } else if (*abort || globaltimer() - idle_since > kTimeoutNs) {
+      *abort = 1;
+      ok = false;
+      break;
+    }
+  }
+  if (!ok) atomicOr(err, kErrTimeout);
+  // every MMA of this thread completes before the TMEM is freed
+  mma_commit(bar_addr(m.drain));
+  mbar_wait_drain(bar_addr(m.drain), 0, kDrainNs);
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+
+__device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
+                           unsigned char *smem, uint32_t tmem, int *err) {
+  using namespace tc;
+  const DecodeParams &p = tp.p;
+  volatile int *abort = &m.abort;
+  const int gt = int(threadIdx.x) - 128;  // rank in the warpgroup
+  const int q = gt >> 5, lane = gt & 31;
+  const bool srow = lane < 16;            // this lane holds a head's S row
+  const int hrow = 16 * q + (lane & 15);
+  const uint32_t tq = tmem + (uint32_t(32 * q) << 16);
+  const float cs = p.score_scale_log2 * p.kv_scale;
+  uint32_t kv_it = 0, p_it = 0, o_it = 0;
+  bool ok = true;
+
+  Walk w(p, r);
+  for (; ok && w.next(); w.advance()) {
+    const int hn = min(kHeads, p.heads - w.g * kHeads);
+    float mrun = -INFINITY, ell = 0.f;
+    for (long long t = w.t0; t < w.t1; ++t, ++kv_it, ++p_it) {
+      const int s = kv_it & 1;
+      const uint32_t ph = (kv_it >> 1) & 1;
+      const int nv = min(kTile, w.n - int(t) * kTile);
+      // Every wait of the warpgroup is followed by a group vote, so that a
+      // wait that gave up in one warp never strands the others at a barrier.
+      bool got = __all_sync(0xffffffffu, mbar_wait(bar_addr(m.s_full[s]), ph, abort, kTimeoutNs));
+      float x[64];
+      if (got) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t a[16], bb[16];
+          tmem_ld16(tq + kColS + 64 * (2 * s) + 16 * c, a);
+          tmem_ld16(tq + kColS + 64 * (2 * s + 1) + 16 * c, bb);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            x[16 * c + i] = (__uint_as_float(a[i]) + __uint_as_float(bb[i])) * cs;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(m.s_free[s]));
+      }
+
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        x[k] = k < nv ? x[k] : -INFINITY;
+        tmax = fmaxf(tmax, x[k]);
+      }
+      float mnew = mrun, alpha = 1.f;
+      bool resc = false;
+      if (t == w.t0) {
+        mnew = tmax;
+      } else if (tmax > mrun + kRescaleThreshold) {
+        mnew = tmax;
+        alpha = exp2f(mrun - mnew);
+        resc = srow;
+      }
+      // PV of the previous tile has finished: O^T is stable and P is free
+      if (got) got = mbar_wait(bar_addr(m.p_free), (p_it & 1) ^ 1, abort, kTimeoutNs);
+      if (!named_sync_and(1, 128, got)) { ok = false; break; }
+      tc_fence_after();
+      if (srow) m.alpha[p_it & 1][hrow] = alpha;
+      if (named_sync_or(1, 128, resc)) {
+        const float *al = m.alpha[p_it & 1];
+        for (int c = 0; c < 4; ++c)
+          for (int hb = 0; hb < tp.npv / 16; ++hb) {
+            uint32_t o[16];
+            tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * al[16 * hb + i]);
+            tmem_st16(tq + kColO + 64 * c + 16 * hb, o);
+          }
+        tmem_wait_st();
+      }
+      if (srow) {
+        unsigned char *prow = smem + kOffP + (hrow >> 3) * 1024 + (hrow & 7) * 128;
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(x[8 * c + 2 * e] - mnew),
+                                                      exp2f(x[8 * c + 2 * e + 1] - mnew));
+            const float2 back = __bfloat1622float2(b2);
+            lsum += back.x + back.y;
+            pk[e] = *reinterpret_cast<uint32_t *>(&b2);
+          }
+          *reinterpret_cast<uint4 *>(prow + ((c ^ (hrow & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        ell = ell * alpha + lsum;
+        mrun = mnew;
+      }
+      // rows [nv, roundup16(nv)) of V are read by the last PV step but hold no
+      // owned token (stale or unowned data): zero their 512 value dims
+      if (nv & 15) {
+        unsigned char *stage = smem + kOffKv + s * kStageBytes;
+        const int r0 = nv, nrow = ((nv + 15) & ~15) - nv;
+        for (int i = gt; i < nrow * 64; i += 128) {
+          const int row = r0 + (i >> 6), kb = (i >> 3) & 7, ch = i & 7;
+          *reinterpret_cast<uint4 *>(stage + (row >> 3) * kAtomBytes + kb * 1024 + (row & 7) * 128 +
+                                     ch * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(m.p_full));
+    }
+    if (!ok) break;
+
+    // ---- epilogue of this CTA's share of request v
+    if (srow) m.ell[hrow] = ell;
+    const bool got_o = mbar_wait(bar_addr(m.o_full), o_it & 1, abort, kTimeoutNs);
+    if (!named_sync_and(2, 128, got_o)) { ok = false; break; }
+    tc_fence_after();
+    const SplitInfo si = split_info(r, w.v, w.pv, w.tiles);
+    const bool split = si.nsplits > 1;
+    const size_t out_row0 = size_t(w.b) * p.heads + size_t(w.g) * kHeads;
+    for (int c = 0; c < 4; ++c) {
+      const int dv = 128 * c + 32 * q + lane;
+      for (int hb = 0; hb < tp.npv / 16; ++hb) {
+        uint32_t o[16];
+        tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int h = 16 * hb + i;
+          if (h < hn) {
+            const float val = __uint_as_float(o[i]) * (p.kv_scale / m.ell[h]);
+            if (!split)
+              p.out[(out_row0 + h) * kDv + dv] = __float2bfloat16_rn(val);
+            else
+              slot_out_ptr(p)[(size_t(si.slot) * kSlotHeads + h) * kDv + dv] = val;
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_addr(m.o_free));
+    ++o_it;
+    if (srow && hrow < hn) {
+      const float lse2 = mrun + log2f(ell);
+      if (!split)
+        p.lse[out_row0 + hrow] = lse_out(p, lse2);
+      else
+        slot_lse_ptr(p)[si.slot * kSlotHeads + hrow] = lse2;
+    }
+    if (split && split_ticket(p, w.v, si.nsplits, &m.flag, gt, GroupSync{3, 128}))
+      merge_splits(p, r, w.v, w.pv, si, m.merge_m, m.merge_inv, gt, 128, GroupSync{3, 128});
+  }
+  if (!ok) atomicOr(err, kErrTimeout);
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(tc::kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_kv) {
+  using namespace tc;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  unsigned char *smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
+  TcMisc &m = *reinterpret_cast<TcMisc *>(smem + kOffMisc);
+  const DecodeParams &p = tp.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int *err = error_word(p);
+
+  // Q rows past the request's heads and P rows past them are read by the
+  // MMAs but never loaded: they must hold finite values.
+  for (int i = tid; i < kQBytes / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < kPBytes / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(smem + kOffP)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_addr(m.kv_full[s]), 1);
+      mbar_init(bar_addr(m.kv_empty[s]), 1);
+      mbar_init(bar_addr(m.s_full[s]), 1);
+      mbar_init(bar_addr(m.s_free[s]), 4);
+    }
+    mbar_init(bar_addr(m.q_full), 1);
+    mbar_init(bar_addr(m.q_empty), 1);
+    mbar_init(bar_addr(m.p_full), 4);
+    mbar_init(bar_addr(m.p_free), 1);
+    mbar_init(bar_addr(m.o_full), 1);
+    mbar_init(bar_addr(m.o_free), 4);
+    mbar_init(bar_addr(m.drain), 1);
+    m.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+  }
+  fence_proxy_async_smem();
+  write_empty_requests(p);
+  cta_schedule(p, &m.range, m.scratch);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+  const CtaRange r = m.range;
+
+  if (r.start < r.end) {
+    if (warp == 0) {
+      if (lane == 0)
+        tc_producer(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
+    } else if (warp == 1) {
+      if (lane == 0) tc_mma(tp, r, m, sbase + kOffQ, sbase + kOffKv, sbase + kOffP, tmem, err);
+    } else if (warp >= 4) {
+      tc_softmax(tp, r, m, smem, tmem, err);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int tc_smem_bytes() { return tc::kSmemBytes; }
+
+cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
+                             const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
+                             cudaStream_t stream) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tc::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  TcParams tp;
+  tp.p = p;
+  tp.npv = npv;
+  tp.q_rows = q_rows;
+  tp.groups_per_page = groups_per_page;
+  decode_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

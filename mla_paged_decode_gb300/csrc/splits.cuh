@@ -62,31 +62,51 @@ __device__ inline void write_empty_requests(const DecodeParams &p) {
   }
 }
 
-// Called by all threads after this CTA's slot for request v is written.
-// Returns true in the CTA that completes the request (it must merge).
-__device__ inline bool split_ticket(const DecodeParams &p, int v, int nsplits, int *s_flag) {
+// Barrier of every thread of the CTA.
+struct CtaSync {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// Named barrier of `count` threads (a warpgroup that runs the epilogue while
+// other warps of the CTA do something else).
+struct GroupSync {
+  uint32_t id, count;
+  __device__ __forceinline__ void operator()() const {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+  }
+};
+
+// Called by the `sync` group after this CTA's slot for request v is written
+// (`rank` = the caller's index in the group).  Returns true in the CTA that
+// completes the request: it must merge.
+template <class Sync>
+__device__ inline bool split_ticket(const DecodeParams &p, int v, int nsplits, int *s_flag,
+                                    int rank, Sync sync) {
   __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  sync();
+  if (rank == 0) {
     int prev = atomicAdd(counters_ptr(p) + v, 1);
     *s_flag = (prev == nsplits - 1);
   }
-  __syncthreads();
+  sync();
   bool last = *s_flag != 0;
   if (last) __threadfence();
   return last;
 }
 
-// Merge the nsplits slots of request v into out/lse.  Block-wide; uses
-// s_m / s_inv (kSlotHeads floats each) of shared memory.  Resets the ticket.
+// Merge the nsplits slots of request v into out/lse, by the `sync` group of
+// `nthreads` threads (`rank` = the caller's index); uses s_m / s_inv
+// (kSlotHeads floats each) of shared memory.  Resets the ticket.
+template <class Sync>
 __device__ inline void merge_splits(const DecodeParams &p, const CtaRange &r, int v, long long pv,
-                             const SplitInfo &si, float *s_m, float *s_inv) {
+                                    const SplitInfo &si, float *s_m, float *s_inv, int rank,
+                                    int nthreads, Sync sync) {
   const int b = v / p.head_groups, g = v % p.head_groups;
   const int h0 = g * p.heads_per_group;
   const int hn = min(p.heads_per_group, p.heads - h0);
   const float *sl = slot_lse_ptr(p);
   const float *so = slot_out_ptr(p);
-  for (int h = threadIdx.x; h < hn; h += blockDim.x) {
+  for (int h = rank; h < hn; h += nthreads) {
     float mx = -INFINITY;
     for (int k = 0; k < si.nsplits; ++k) {
       int slot = slot_of(r, si.c_first + k, si.c_first, pv);
@@ -101,8 +121,8 @@ __device__ inline void merge_splits(const DecodeParams &p, const CtaRange &r, in
     s_inv[h] = 1.f / sum;
     p.lse[size_t(b) * p.heads + h0 + h] = lse_out(p, mx + log2f(sum));
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < hn * (kDv / 4); i += blockDim.x) {
+  sync();
+  for (int i = rank; i < hn * (kDv / 4); i += nthreads) {
     int h = i / (kDv / 4), d4 = i % (kDv / 4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < si.nsplits; ++k) {
@@ -119,8 +139,8 @@ __device__ inline void merge_splits(const DecodeParams &p, const CtaRange &r, in
     pk.y = *reinterpret_cast<uint32_t *>(&hi);
     reinterpret_cast<uint2 *>(p.out + (size_t(b) * p.heads + h0 + h) * kDv)[d4] = pk;
   }
-  if (threadIdx.x == 0) counters_ptr(p)[v] = 0;
-  __syncthreads();
+  if (rank == 0) counters_ptr(p)[v] = 0;
+  sync();
 }
 
 }  // namespace mla

@@ -127,7 +127,7 @@ def test_combine_rejects_bad_arguments(lib):
 
 
 def test_status_strings(lib):
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         assert lib.mla_status_string(code)
     assert lib.mla_version() >= 100
 
