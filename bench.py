@@ -221,9 +221,10 @@ def run_ours(args, world, rank, local):
     barrier(world)
     mla.load_library()
 
-    case = workloads.config_long32k(device=dev, seed=args.seed, batch=args.batch)
-    if args.batch != 64:
-        case.name += f"_b{args.batch}"
+    case = workloads.config_long32k(device=dev, seed=args.seed, batch=args.batch,
+                                    pool_pages=args.pool_pages)
+    if args.batch != 64 or args.pool_pages != 40000:
+        case.name += f"_b{args.batch}_pool{args.pool_pages}"
     B, H = case.batch, case.heads
     kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
     out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
@@ -390,6 +391,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=64,
                     help="requests per step (64 = the headline workload; smaller only for profiling)")
+    ap.add_argument("--pool-pages", type=int, default=40000,
+                    help="cache pool size in pages (40000 = the headline workload)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

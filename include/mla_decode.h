@@ -86,10 +86,10 @@ typedef struct mla_decode_desc {
 /*
  * Bytes of scratch workspace mla_decode_partial needs for `d` on a GPU with
  * `num_sms` SMs (num_sms <= 0: ask the current device).  Returns 0 if `d` is
- * NULL or invalid.  The workspace holds per-request split counters, a device
- * error word and the fp32 partial results of requests split across CTAs.
- * It must be zero-filled once before its first use; every call leaves the
- * counters at zero again.
+ * NULL or invalid.  The workspace holds a device error word, per-request
+ * split records and the fp32 partial results of requests split across CTAs.
+ * Its first 256 bytes (the error word) must be zero before the first call;
+ * everything else is rewritten by each call before it is read.
  */
 size_t mla_decode_workspace_size(const mla_decode_desc *d, int num_sms);
 
@@ -117,7 +117,10 @@ size_t mla_decode_workspace_size(const mla_decode_desc *d, int num_sms);
  *              A request for which the partition owns no token gets out = 0 and
  *              lse = -inf (the neutral pair of the LSE merge).
  *  workspace   scratch of >= mla_decode_workspace_size(d, 0) bytes, 256-byte
- *              aligned, zero-filled before first use (see above).
+ *              aligned, its first 256 bytes zero before first use (see above).
+ *
+ * Enqueues two kernels on `stream`: the decode kernel and the merge of the
+ * requests its schedule split across SMs.
  *
  * Single-token decode only: q_len != 1 is rejected with MLA_ERR_SHAPE, the
  * analogue of the DCP kernel gate that refuses multi-token (causal) requests.
@@ -149,7 +152,7 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
  * larger batches return MLA_ERR_WORKSPACE without launching.  All calls share
  * the one array: calls that may overlap on the GPU (different streams, or
  * different host threads) race and must be serialised by the caller.  Each
- * call clears the array's counters before its kernel; kernel-side bounds
+ * call clears the array's error word before its kernels; kernel-side bounds
  * errors are not reported by this variant (use mla_decode_partial with
  * mla_decode_check_workspace to diagnose them).
  */

@@ -22,22 +22,23 @@ constexpr int kErrTimeout = 4;   // a bounded wait inside the kernel gave up
 
 // Workspace layout (all offsets multiples of 256 bytes):
 //   [0, 256)                 header: int32 error word
-//   counters                 int32[num_virtual_requests] split tickets
+//   info                     int4[num_virtual_requests]: {first CTA, splits, its slot}
 //   slot lse                 fp32[2 * grid][kSlotHeads]   (base-2 lse of a split)
 //   slot out                 fp32[2 * grid][kSlotHeads][512] (normalised split output)
 struct WorkspaceLayout {
-  size_t counters, slot_lse, slot_out, total;
+  size_t info, slot_lse, slot_out, total;
 };
 
-__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+__host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-__host__ __device__ inline WorkspaceLayout workspace_layout(int num_virtual, int grid) {
-  WorkspaceLayout w;
-  w.counters = 256;
-  w.slot_lse = align256(w.counters + sizeof(int) * size_t(num_virtual));
-  w.slot_out = align256(w.slot_lse + sizeof(float) * size_t(2 * grid) * kSlotHeads);
-  w.total = align256(w.slot_out + sizeof(float) * size_t(2 * grid) * kSlotHeads * kDv);
-  return w;
+__host__ __device__ constexpr WorkspaceLayout workspace_layout(int num_virtual, int grid) {
+  return WorkspaceLayout{
+      256, align256(256 + 16 * size_t(num_virtual)),
+      align256(align256(256 + 16 * size_t(num_virtual)) +
+               sizeof(float) * size_t(2 * grid) * kSlotHeads),
+      align256(align256(align256(256 + 16 * size_t(num_virtual)) +
+                        sizeof(float) * size_t(2 * grid) * kSlotHeads) +
+               sizeof(float) * size_t(2 * grid) * kSlotHeads * kDv)};
 }
 
 struct DecodeParams {
@@ -89,8 +90,9 @@ __device__ __forceinline__ int request_tiles(const DecodeParams &p, int v) {
 // v = b * head_groups + g (tiles_v = ceil(local_len / 64)) over G_eff =
 // min(gridDim.x, T) CTAs: CTA c owns tiles [c*T/G_eff, (c+1)*T/G_eff).  A
 // request crossing a boundary is split; each split writes a normalised fp32
-// partial into slot 2c (the CTA's first request) or 2c+1 (its last), and the
-// CTA that completes a request's ticket merges the splits.
+// partial into slot 2c (the CTA's first request) or 2c+1 (its last); the
+// request's first CTA records {itself, split count, its slot} and a second
+// kernel merges the splits.
 
 struct CtaRange {
   long long start, end;   // global tile range of this CTA

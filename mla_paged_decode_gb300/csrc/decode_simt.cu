@@ -16,10 +16,8 @@ struct SimtSmem {
   float q[kSimtHeads][kDqk];
   __nv_bfloat16 kv[kTile][kKvStride];
   float prob[kSimtHeads][kTile];
-  float m[kSlotHeads], inv[kSlotHeads];
   CtaRange range;
   long long scratch[kSimtThreads / 32 + 1];
-  int flag;
 };
 
 __device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
@@ -194,14 +192,13 @@ __global__ void __launch_bounds__(kSimtThreads, 1) decode_simt_kernel(DecodePara
         if (lane == 0) slot_lse_ptr(p)[si.slot * kSlotHeads + hl] = lse2;
       }
     }
-    if (split && split_ticket(p, v, si.nsplits, &s.flag, tid, CtaSync{}))
-      merge_splits(p, r, v, pv, si, s.m, s.inv, tid, kSimtThreads, CtaSync{});
+    if (tid == 0) record_split(p, v, si);
     pv += tiles;
     ++v;
   }
 }
 
-size_t simt_smem_bytes() { return sizeof(SimtSmem); }
+cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream);
 
 cudaError_t launch_decode_simt(const DecodeParams &p, int grid, cudaStream_t stream) {
   static int configured_device = -1;
@@ -215,7 +212,8 @@ cudaError_t launch_decode_simt(const DecodeParams &p, int grid, cudaStream_t str
     configured_device = dev;
   }
   decode_simt_kernel<<<grid, kSimtThreads, sizeof(SimtSmem), stream>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? launch_split_merge(p, grid, stream) : e;
 }
 
 }  // namespace mla

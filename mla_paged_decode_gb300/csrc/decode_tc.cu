@@ -64,10 +64,8 @@ struct TcMisc {
   uint64_t p_full, p_free, o_full, o_free, drain;
   uint32_t tmem_base;
   int abort;
-  int flag;
   float alpha[2][64];
   float ell[64];
-  float merge_m[kSlotHeads], merge_inv[kSlotHeads];
   CtaRange range;
   long long scratch[tc::kThreads / 32 + 1];
 };
@@ -447,8 +445,7 @@ __device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
       else
         slot_lse_ptr(p)[si.slot * kSlotHeads + hrow] = lse2;
     }
-    if (split && split_ticket(p, w.v, si.nsplits, &m.flag, gt, GroupSync{3, 128}))
-      merge_splits(p, r, w.v, w.pv, si, m.merge_m, m.merge_inv, gt, 128, GroupSync{3, 128});
+    if (gt == 0) record_split(p, w.v, si);
   }
   if (!ok) atomicOr(err, kErrTimeout);
 }
@@ -529,6 +526,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
 int tc_smem_bytes() { return tc::kSmemBytes; }
 
+cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream);
+
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
                              const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
                              cudaStream_t stream) {
@@ -548,7 +547,8 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int gro
   tp.q_rows = q_rows;
   tp.groups_per_page = groups_per_page;
   decode_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? launch_split_merge(p, grid, stream) : e;
 }
 
 }  // namespace mla

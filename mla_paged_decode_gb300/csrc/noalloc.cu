@@ -7,7 +7,7 @@
 // device synchronisation cudaMalloc / cudaFree may cause, and plain-C hosts
 // without an allocator of their own.  They pass inputs and outputs only.
 //
-// The scratch (split tickets, the device error word and the split partials)
+// The scratch (split records, the device error word and the split partials)
 // is g_noalloc_scratch below: ~40 MB that every GPU which loads this library
 // keeps until the process exits.  Host code must not use the array's name as
 // a device address -- on the host it is only a stand-in -- so each device's
@@ -30,12 +30,8 @@ constexpr int kNoAllocHeadsPerGroup = 32;   // the CUDA-core decode kernel's hea
 constexpr int kNoAllocMaxVirtual = 16384;   // batch * ceil(heads / 32)
 constexpr int kNoAllocMaxGrid = 152;        // CTAs (GPUs with more SMs use 152)
 
-constexpr size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
-// Same layout as mla::workspace_layout(kNoAllocMaxVirtual, kNoAllocMaxGrid).
 constexpr size_t kNoAllocBytes =
-    up256(up256(up256(256 + sizeof(int) * size_t(kNoAllocMaxVirtual)) +
-                sizeof(float) * size_t(2 * kNoAllocMaxGrid) * mla::kSlotHeads) +
-          sizeof(float) * size_t(2 * kNoAllocMaxGrid) * mla::kSlotHeads * mla::kDv);
+    mla::workspace_layout(kNoAllocMaxVirtual, kNoAllocMaxGrid).total;
 
 }  // namespace
 
@@ -114,9 +110,9 @@ extern "C" int mla_decode_partial_noalloc(const void *q, const void *kv_pages,
   if (wl.total > kNoAllocBytes) return MLA_ERR_WORKSPACE;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The scratch keeps the previous call's contents: the error word and the
-  // split tickets must start at zero.
-  if (cudaMemsetAsync(dev.scratch, 0, wl.slot_lse, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // The scratch keeps the previous call's contents: the error word must start
+  // at zero (every other part is rewritten before it is read).
+  if (cudaMemsetAsync(dev.scratch, 0, 256, s) != cudaSuccess) return MLA_ERR_CUDA;
 
   mla::DecodeParams p;
   p.q = static_cast<const __nv_bfloat16 *>(q);

@@ -1,0 +1,105 @@
+// Merge of the requests that the stream-K schedule cut across CTAs (the
+// split-KV reduce inside one partition).  Each split left a normalised fp32
+// output and its base-2 LSE in a workspace slot, and the request's first CTA
+// recorded {first CTA, number of splits, its slot}; split k > 0 lives in slot
+// 2 (first + k).  The merge is the LSE-weighted combine of those splits.
+//
+// One CTA per (virtual request, 8 heads): a warp per head reduces the split
+// LSEs (max, then the weights 2^(lse_k - max) kept in shared memory), then
+// each thread owns 4 of the 512 value dims and streams the splits' float4s
+// with independent loads.
+#include "common.cuh"
+#include "splits.cuh"
+
+namespace mla {
+
+constexpr int kMergeThreads = 128;  // x 4 dims = 512
+constexpr int kMergeHeads = 8;
+
+__global__ void __launch_bounds__(kMergeThreads)
+    split_merge_kernel(DecodeParams p, int max_splits) {
+  extern __shared__ float s_w[];  // [max_splits][kMergeHeads] weights, then [kMergeHeads] 1/sum
+  const int v = blockIdx.x;
+  const int b = v / p.head_groups, g = v % p.head_groups;
+  const int h_first = blockIdx.y * kMergeHeads;  // within the head group
+  const int group_heads = min(p.heads_per_group, p.heads - g * p.heads_per_group);
+  if (h_first >= group_heads) return;
+  const int hn = min(kMergeHeads, group_heads - h_first);
+  if (request_tiles(p, v) == 0) return;
+  const int4 info = info_ptr(p)[v];
+  const int ns = info.y;
+  if (ns <= 1 || ns > max_splits) return;
+  const float *sl = slot_lse_ptr(p);
+  const float *so = slot_out_ptr(p);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *inv = s_w + max_splits * kMergeHeads;
+  const size_t row0 = size_t(b) * p.heads + size_t(g) * p.heads_per_group + h_first;
+
+  for (int hh = warp; hh < hn; hh += kMergeThreads / 32) {
+    float mx = -INFINITY;
+    for (int k = lane; k < ns; k += 32) {
+      const int slot = k == 0 ? info.z : 2 * (info.x + k);
+      mx = fmaxf(mx, sl[slot * kSlotHeads + h_first + hh]);
+    }
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.f;
+    for (int k = lane; k < ns; k += 32) {
+      const int slot = k == 0 ? info.z : 2 * (info.x + k);
+      const float w = exp2f(sl[slot * kSlotHeads + h_first + hh] - mx);
+      s_w[k * kMergeHeads + hh] = w;
+      sum += w;
+    }
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+      inv[hh] = 1.f / sum;
+      p.lse[row0 + hh] = lse_out(p, mx + log2f(sum));
+    }
+  }
+  __syncthreads();
+
+  const int d4 = threadIdx.x;  // value dims 4 d4 .. 4 d4 + 3
+  for (int hh = 0; hh < hn; ++hh) {
+    const size_t col = size_t(h_first + hh) * kDv / 4 + d4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int k = 0;
+    for (; k + 4 <= ns; k += 4) {
+      float4 x[4];
+      float w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int slot = (k + u) == 0 ? info.z : 2 * (info.x + k + u);
+        x[u] = reinterpret_cast<const float4 *>(so + size_t(slot) * kSlotHeads * kDv)[col];
+        w[u] = s_w[(k + u) * kMergeHeads + hh];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x += w[u] * x[u].x; acc.y += w[u] * x[u].y;
+        acc.z += w[u] * x[u].z; acc.w += w[u] * x[u].w;
+      }
+    }
+    for (; k < ns; ++k) {
+      const int slot = k == 0 ? info.z : 2 * (info.x + k);
+      const float4 x = reinterpret_cast<const float4 *>(so + size_t(slot) * kSlotHeads * kDv)[col];
+      const float w = s_w[k * kMergeHeads + hh];
+      acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
+    }
+    const float s = inv[hh];
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * s, acc.y * s);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * s, acc.w * s);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+    reinterpret_cast<uint2 *>(p.out + (row0 + hh) * kDv)[d4] = pk;
+  }
+}
+
+cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream) {
+  const int V = p.batch * p.head_groups;
+  if (V == 0) return cudaSuccess;
+  dim3 blocks(V, (p.heads_per_group + kMergeHeads - 1) / kMergeHeads);
+  const size_t smem = sizeof(float) * (size_t(grid) * kMergeHeads + kMergeHeads);
+  split_merge_kernel<<<blocks, kMergeThreads, smem, stream>>>(p, grid);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

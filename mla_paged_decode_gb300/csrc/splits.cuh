@@ -33,8 +33,8 @@ __device__ __forceinline__ float *slot_lse_ptr(const DecodeParams &p) {
 __device__ __forceinline__ float *slot_out_ptr(const DecodeParams &p) {
   return reinterpret_cast<float *>(p.ws + p.wl.slot_out);
 }
-__device__ __forceinline__ int *counters_ptr(const DecodeParams &p) {
-  return reinterpret_cast<int *>(p.ws + p.wl.counters);
+__device__ __forceinline__ int4 *info_ptr(const DecodeParams &p) {
+  return reinterpret_cast<int4 *>(p.ws + p.wl.info);
 }
 __device__ __forceinline__ int *error_word(const DecodeParams &p) {
   return reinterpret_cast<int *>(p.ws);
@@ -62,85 +62,11 @@ __device__ inline void write_empty_requests(const DecodeParams &p) {
   }
 }
 
-// Barrier of every thread of the CTA.
-struct CtaSync {
-  __device__ __forceinline__ void operator()() const { __syncthreads(); }
-};
-
-// Named barrier of `count` threads (a warpgroup that runs the epilogue while
-// other warps of the CTA do something else).
-struct GroupSync {
-  uint32_t id, count;
-  __device__ __forceinline__ void operator()() const {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-  }
-};
-
-// Called by the `sync` group after this CTA's slot for request v is written
-// (`rank` = the caller's index in the group).  Returns true in the CTA that
-// completes the request: it must merge.
-template <class Sync>
-__device__ inline bool split_ticket(const DecodeParams &p, int v, int nsplits, int *s_flag,
-                                    int rank, Sync sync) {
-  __threadfence();
-  sync();
-  if (rank == 0) {
-    int prev = atomicAdd(counters_ptr(p) + v, 1);
-    *s_flag = (prev == nsplits - 1);
-  }
-  sync();
-  bool last = *s_flag != 0;
-  if (last) __threadfence();
-  return last;
-}
-
-// Merge the nsplits slots of request v into out/lse, by the `sync` group of
-// `nthreads` threads (`rank` = the caller's index); uses s_m / s_inv
-// (kSlotHeads floats each) of shared memory.  Resets the ticket.
-template <class Sync>
-__device__ inline void merge_splits(const DecodeParams &p, const CtaRange &r, int v, long long pv,
-                                    const SplitInfo &si, float *s_m, float *s_inv, int rank,
-                                    int nthreads, Sync sync) {
-  const int b = v / p.head_groups, g = v % p.head_groups;
-  const int h0 = g * p.heads_per_group;
-  const int hn = min(p.heads_per_group, p.heads - h0);
-  const float *sl = slot_lse_ptr(p);
-  const float *so = slot_out_ptr(p);
-  for (int h = rank; h < hn; h += nthreads) {
-    float mx = -INFINITY;
-    for (int k = 0; k < si.nsplits; ++k) {
-      int slot = slot_of(r, si.c_first + k, si.c_first, pv);
-      mx = fmaxf(mx, __ldcg(sl + slot * kSlotHeads + h));
-    }
-    float sum = 0.f;
-    for (int k = 0; k < si.nsplits; ++k) {
-      int slot = slot_of(r, si.c_first + k, si.c_first, pv);
-      sum += exp2f(__ldcg(sl + slot * kSlotHeads + h) - mx);
-    }
-    s_m[h] = mx;
-    s_inv[h] = 1.f / sum;
-    p.lse[size_t(b) * p.heads + h0 + h] = lse_out(p, mx + log2f(sum));
-  }
-  sync();
-  for (int i = rank; i < hn * (kDv / 4); i += nthreads) {
-    int h = i / (kDv / 4), d4 = i % (kDv / 4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < si.nsplits; ++k) {
-      int slot = slot_of(r, si.c_first + k, si.c_first, pv);
-      float w = exp2f(__ldcg(sl + slot * kSlotHeads + h) - s_m[h]);
-      float4 x = __ldcg(reinterpret_cast<const float4 *>(so + (size_t(slot) * kSlotHeads + h) * kDv) + d4);
-      acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
-    }
-    float inv = s_inv[h];
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t *>(&lo);
-    pk.y = *reinterpret_cast<uint32_t *>(&hi);
-    reinterpret_cast<uint2 *>(p.out + (size_t(b) * p.heads + h0 + h) * kDv)[d4] = pk;
-  }
-  if (rank == 0) counters_ptr(p)[v] = 0;
-  sync();
+// Called (by one thread) in each CTA that worked on request v: the CTA that
+// holds the request's first tile records where its splits are, for the merge
+// kernel.  Every request with owned tokens gets a fresh record each call.
+__device__ __forceinline__ void record_split(const DecodeParams &p, int v, const SplitInfo &si) {
+  if (int(blockIdx.x) == si.c_first) info_ptr(p)[v] = make_int4(si.c_first, si.nsplits, si.slot, 0);
 }
 
 }  // namespace mla

@@ -175,10 +175,11 @@ def config_small(device="cpu", seed: int = 0, **kw) -> DecodeCase:
                             num_parts=2, seed=seed, device=device, **kw)
 
 
-def config_long32k(device="cpu", seed: int = 0, batch: int = 64, **kw) -> DecodeCase:
+def config_long32k(device="cpu", seed: int = 0, batch: int = 64, pool_pages: int = 40000,
+                   **kw) -> DecodeCase:
     """B=64, H=64, L ~ U{4096..32768}, 40k-page pool, P=1."""
     lens = uniform_lens(batch, 4096, 32768, seed)
-    return make_decode_case("long32k_b64_h64_bf16", 64, lens, pool_pages=40000,
+    return make_decode_case("long32k_b64_h64_bf16", 64, lens, pool_pages=pool_pages,
                             num_parts=1, seed=seed, device=device, **kw)
 
 
