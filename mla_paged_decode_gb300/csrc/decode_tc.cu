@@ -4,23 +4,26 @@
 // 128, heads as N) with fp32 accumulators in TMEM, and a warpgroup runs the
 // online softmax between them.
 //
-// Roles (256 threads):
+// Roles (288 threads):
 //   warp 0, lane 0  TMA producer: Q of each request (9 boxes of 64 dims) and,
 //                   per tile, one 4-D box per page holding the 64/P rows the
 //                   partition owns, into a [atom][dim block][8 rows][128 B]
 //                   swizzled layout that serves both MMAs.
-//   warp 1          TMEM owner (alloc/free); lane 0 issues the MMAs.
+//   warp 1          TMEM owner (alloc/free).
+//   warps 1, 2      lane 0 issues half of the score MMAs (one accumulator each).
+//   warps 3, 8      lane 0 issues the PV MMAs of two of the four value chunks.
 //   warps 4..7      softmax and epilogue.  The S accumulator (M = 64) puts
-//                   head 16q + i in TMEM lane 32q + i, so warp q's lanes 0..15
-//                   each own one head's row of 64 token scores.  Every thread
-//                   owns TMEM lane 32q + lane of O^T: one value dimension.
+//                   head 16q + i in TMEM lane 32q + i (i < 16); read with the
+//                   16x256b shape, each lane of warp q gets 2 heads x 16 of the
+//                   64 tokens.  For the epilogue every thread owns TMEM lane
+//                   32q + lane of O^T: one value dimension.
 //
 // Pipeline per tile i (stage / S buffer i mod 2): producer -> kv_full ->
 // MMA S_i (36 MMAs, two interleaved accumulators so consecutive MMAs are
 // independent) -> s_full -> softmax reads S_i, frees it (s_free), waits for
 // PV_{i-1} (p_free), rescales O^T only when some head's running max grew by
 // more than 2^8, writes P_i (bf16) -> p_full -> MMA PV_i (4 independent
-// value-dim chunks) -> kv_empty + p_free.  The MMA thread issues S_{i+1} as
+// value-dim chunks) -> kv_empty + p_free.  The score issuers start S_{i+1} as
 // soon as tile i+1 lands, so the score MMAs of the next tile overlap this
 // tile's softmax, and the producer keeps the pages of the tile two ahead
 // streaming into L2.
@@ -32,17 +35,18 @@ namespace mla {
 using namespace sm100;
 
 namespace tc {
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;
 constexpr int kHeads = 64;                   // heads per virtual request (M of S)
 constexpr int kKb = kDqk / 64;               // 9 blocks of 64 bf16 = 128 B
 constexpr int kQBytes = kKb * 64 * 128;      // [kb][64 rows][128 B]
 constexpr int kAtomBytes = kKb * 1024;       // 8 tokens x 576 dims: [kb][8][128 B]
 constexpr int kStageBytes = 8 * kAtomBytes;  // 64 tokens
-constexpr int kPBytes = 64 * 128;            // P [64 heads][64 tokens] bf16
+// P [64 heads][64 tokens] bf16 reuses the rope block (dims 512..575) of the
+// tile's own stage, dead once S is computed: atom a at a * kAtomBytes + kPOff.
+constexpr int kPOff = 8 * 1024;
 constexpr int kOffQ = 0;
 constexpr int kOffKv = kOffQ + kQBytes;
-constexpr int kOffP = kOffKv + 2 * kStageBytes;
-constexpr int kOffMisc = kOffP + kPBytes;
+constexpr int kOffMisc = kOffKv + 2 * kStageBytes;
 constexpr int kSmemBytes = 232448;           // per-block maximum on sm_100 parts
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                // O^T chunk c: columns [64c, 64c + npv)
@@ -61,7 +65,7 @@ struct TcParams {
 
 struct TcMisc {
   uint64_t kv_full[2], kv_empty[2], q_full, q_empty, s_full[2], s_free[2];
-  uint64_t p_full, p_free, o_full, o_free, drain;
+  uint64_t p_full[2], p_free, o_full, o_free, drain;
   uint32_t tmem_base;
   int abort;
   float alpha[2][64];
@@ -168,11 +172,8 @@ __device__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, ui
       last_q = q_it & 1;
       ++q_it;
     }
+    // page indices are read before waiting for the stage, hiding their latency
     const int s = kv_it & 1;
-    if (!mbar_wait(bar_addr(m.kv_empty[s]), ((kv_it >> 1) & 1) ^ 1, abort, kTimeoutNs)) {
-      ok = false;
-      break;
-    }
     int lp0, lp1;
     tile_pages(p, cur.t, cur.w.n, &lp0, &lp1);
     int pages[8];
@@ -186,6 +187,10 @@ __device__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, ui
         bytes += page_bytes;
       }
       pages[k] = pg;
+    }
+    if (!mbar_wait(bar_addr(m.kv_empty[s]), ((kv_it >> 1) & 1) ^ 1, abort, kTimeoutNs)) {
+      ok = false;
+      break;
     }
     mbar_arrive_expect_tx(bar_addr(m.kv_full[s]), bytes);
     for (int k = 0; k <= lp1 - lp0; ++k)
@@ -204,88 +209,99 @@ __device__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, ui
     if (last_kv[s] >= 0) mbar_wait_drain(bar_addr(m.kv_full[s]), last_kv[s], kDrainNs);
 }
 
-// ------------------------------------------------------------------ MMA issuer
+// ------------------------------------------------------------------ MMA issuers
 //
-// One thread, two cursors over the same tile sequence: S(k) needs tile k in
-// its stage, Q of its request and S buffer k mod 2 free; PV(k) needs P(k)
-// (and, for a request's first tile, O^T free).  Whichever is ready is issued,
-// PV first because it frees a stage for the next load.
+// A tcgen05.mma costs its issuing thread ~55 cycles whatever its size up to
+// N = 128 (measured on this GB300), so one thread cannot keep the tensor core
+// fed with M = 64 / N = 64 score MMAs.  Three warps issue: two split the 36
+// K-steps of S (one accumulator each), one issues PV.
 
-__device__ void tc_mma(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
-                       uint32_t sKv, uint32_t sP, uint32_t tmem, int *err) {
+// Descriptors: an offset is added to the encoded start address (bits 0..13,
+// address >> 4), which never carries because shared addresses stay below 256 KB.
+__device__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
+                         uint32_t sKv, uint32_t tmem, int chain, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const uint32_t idesc_s = idesc_bf16_f32(64, 64, false, false);
-  const uint32_t idesc_o = idesc_bf16_f32(128, tp.npv, true, false);
-  uint32_t s_it = 0, pv_it = 0, q_it = 0, o_it = 0;
-  TileCursor sc(p, r), pc(p, r);
+  const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);            // Q, K-major
+  const uint64_t dk0 = smem_desc_sw128(sKv, 16, kAtomBytes);    // K tile, K-major
+  constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
+  uint32_t s_it = 0, q_it = 0;
   bool ok = true;
-  uint64_t idle_since = globaltimer();
-
-  while (pc.live) {
-    bool progress = false;
-    // ---- PV(pv_it): O^T(chunk c) (+)= V^T P^T over ceil(nv/16) steps of 16 tokens
-    if (pv_it < s_it && mbar_test_wait(bar_addr(m.p_full), pv_it & 1) &&
-        (!pc.first() || mbar_test_wait(bar_addr(m.o_free), (o_it & 1) ^ 1))) {
-      tc_fence_after();
-      const int st = pv_it & 1;
-      const uint32_t stage = sKv + st * kStageBytes;
-      const int ksteps = (pc.nv() + 15) >> 4;
-      const bool fresh = pc.first();
-      for (int ks = 0; ks < ksteps; ++ks) {
+  for (TileCursor sc(p, r); sc.live; sc.step(), ++s_it) {
+    const int st = s_it & 1;
+    const uint32_t ph = (s_it >> 1) & 1;
+    if (!mbar_wait(bar_addr(m.kv_full[st]), ph, abort, kTimeoutNs)) { ok = false; break; }
+    if (sc.first()) {
+      if (!mbar_wait(bar_addr(m.q_full), q_it & 1, abort, kTimeoutNs)) { ok = false; break; }
+      ++q_it;
+    }
+    if (!mbar_wait(bar_addr(m.s_free[st]), ph ^ 1, abort, kTimeoutNs)) { ok = false; break; }
+    tc_fence_after();
+    const uint64_t dk = dk0 + st * kStageEnc;
+    const uint32_t d = tmem + kColS + 64 * (2 * st + chain);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint64_t a = smem_desc_sw128(stage + 2 * ks * kAtomBytes + 2 * c * 1024, 1024,
-                                             kAtomBytes);
-          const uint64_t bdesc = smem_desc_sw128(sP + ks * 32, 16, 1024);
-          mma_bf16_ss(tmem + kColO + 64 * c, a, bdesc, idesc_o, !(fresh && ks == 0));
-        }
-      }
-      mma_commit(bar_addr(m.kv_empty[st]));
-      mma_commit(bar_addr(m.p_free));
-      if (pc.last()) {
-        mma_commit(bar_addr(m.o_full));
-        ++o_it;
-      }
-      ++pv_it;
-      pc.step();
-      progress = true;
+    for (int i = 0; i < kKb * 2; ++i) {
+      const int ks = 2 * i + chain;
+      const int kb = ks >> 2, sub = ks & 3;
+      mma_bf16_ss(d, dq + ((kb * (64 * 128) + sub * 32) >> 4), dk + ((kb * 1024 + sub * 32) >> 4),
+                  idesc_s, i > 0);
     }
-    // ---- S(s_it) = Q K^T, 36 K-steps alternating between two accumulators
-    if (sc.live) {
-      const int st = s_it & 1;
-      const uint32_t ph = (s_it >> 1) & 1;
-      if (mbar_test_wait(bar_addr(m.kv_full[st]), ph) &&
-          (!sc.first() || mbar_test_wait(bar_addr(m.q_full), q_it & 1)) &&
-          mbar_test_wait(bar_addr(m.s_free[st]), ph ^ 1)) {
-        tc_fence_after();
-        if (sc.first()) ++q_it;
-        const uint32_t stage = sKv + st * kStageBytes;
-#pragma unroll 4
-        for (int ks = 0; ks < kKb * 4; ++ks) {
-          const int kb = ks >> 2, sub = ks & 3;
-          const uint64_t a = smem_desc_sw128(sQ + kb * (64 * 128) + sub * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(stage + kb * 1024 + sub * 32, 16, kAtomBytes);
-          mma_bf16_ss(tmem + kColS + 64 * (2 * st + (ks & 1)), a, bdesc, idesc_s, ks >= 2);
-        }
-        mma_commit(bar_addr(m.s_full[st]));
-        if (sc.last()) mma_commit(bar_addr(m.q_empty));
-        ++s_it;
-        sc.step();
-        progress = true;
-      }
-    }
-    if (progress) {
-      idle_since = globaltimer();
-    } else if (*abort || globaltimer() - idle_since > kTimeoutNs) {
-      *abort = 1;
+    mma_commit(bar_addr(m.s_full[st]));
+    if (sc.last()) mma_commit(bar_addr(m.q_empty));
+  }
+  if (!ok) atomicOr(err, kErrTimeout);
+  mma_commit(bar_addr(m.drain));
+  mbar_wait_drain(bar_addr(m.drain), 0, kDrainNs);
+}
+
+// O^T(chunk c) (+)= V^T(tile) P^T over ceil(nv/16) steps of 16 tokens; issuer
+// `half` takes value chunks 2 half and 2 half + 1.
+__device__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
+                          uint32_t tmem, int half, int *err) {
+  using namespace tc;
+  const DecodeParams &p = tp.p;
+  volatile int *abort = &m.abort;
+  const uint32_t idesc_o = idesc_bf16_f32(128, tp.npv, true, false);
+  const uint64_t dv0 = smem_desc_sw128(sKv, 1024, kAtomBytes);           // V^T, MN-major
+  const uint64_t dp0 = smem_desc_sw128(sKv + kPOff, 16, kAtomBytes);     // P, K-major
+  constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
+  uint32_t pv_it = 0, o_it = 0;
+  bool ok = true;
+  for (TileCursor pc(p, r); pc.live; pc.step(), ++pv_it) {
+    if (!mbar_wait(bar_addr(m.p_full[pv_it & 1]), (pv_it >> 1) & 1, abort, kTimeoutNs)) {
       ok = false;
       break;
     }
+    const bool fresh = pc.first();
+    if (fresh && !mbar_wait(bar_addr(m.o_free), (o_it & 1) ^ 1, abort, kTimeoutNs)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const int st = pv_it & 1;
+    const uint64_t dv = dv0 + st * kStageEnc, dp = dp0 + st * kStageEnc;
+    const int ksteps = (pc.nv() + 15) >> 4;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      if (ks < ksteps) {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * half + cc;
+          mma_bf16_ss(tmem + kColO + 64 * c, dv + ((2 * ks * kAtomBytes + 2 * c * 1024) >> 4),
+                      dp + ((ks * 32) >> 4), idesc_o, !(fresh && ks == 0));
+        }
+      }
+    }
+    mma_commit(bar_addr(m.kv_empty[st]));
+    mma_commit(bar_addr(m.p_free));
+    if (pc.last()) {
+      mma_commit(bar_addr(m.o_full));
+      ++o_it;
+    }
   }
   if (!ok) atomicOr(err, kErrTimeout);
-  // every MMA of this thread completes before the TMEM is freed
   mma_commit(bar_addr(m.drain));
   mbar_wait_drain(bar_addr(m.drain), 0, kDrainNs);
 }
@@ -299,8 +315,11 @@ __device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
   volatile int *abort = &m.abort;
   const int gt = int(threadIdx.x) - 128;  // rank in the warpgroup
   const int q = gt >> 5, lane = gt & 31;
-  const bool srow = lane < 16;            // this lane holds a head's S row
-  const int hrow = 16 * q + (lane & 15);
+  // 16x256b view of the M = 64 score accumulator: this lane holds heads
+  // row[0] = 16q + lane/4 and row[1] = row[0] + 8, and of every 8 tokens the
+  // pair 2 (lane % 4) + {0, 1}; four lanes share a head.
+  const int row[2] = {16 * q + (lane >> 2), 16 * q + (lane >> 2) + 8};
+  const int pair = 2 * (lane & 3);
   const uint32_t tq = tmem + (uint32_t(32 * q) << 16);
   const float cs = p.score_scale_log2 * p.kv_scale;
   uint32_t kv_it = 0, p_it = 0, o_it = 0;
@@ -309,7 +328,8 @@ __device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
   Walk w(p, r);
   for (; ok && w.next(); w.advance()) {
     const int hn = min(kHeads, p.heads - w.g * kHeads);
-    float mrun = -INFINITY, ell = 0.f;
+    float mrun[2] = {-INFINITY, -INFINITY};  // running max (base-2 units) of each head
+    float ellp[2] = {0.f, 0.f};              // this lane's share of each head's sum
     for (long long t = w.t0; t < w.t1; ++t, ++kv_it, ++p_it) {
       const int s = kv_it & 1;
       const uint32_t ph = (kv_it >> 1) & 1;
@@ -317,45 +337,57 @@ __device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
       // Every wait of the warpgroup is followed by a group vote, so that a
       // wait that gave up in one warp never strands the others at a barrier.
       bool got = __all_sync(0xffffffffu, mbar_wait(bar_addr(m.s_full[s]), ph, abort, kTimeoutNs));
-      float x[64];
+      float x[32];  // unscaled scores: x[4j + 2h + e] = head row[h], token 8j + pair + e
       if (got) {
         tc_fence_after();
+        uint32_t ra[32], rb[32];
+        tmem_ld16x256b_x8(tq + kColS + 64 * (2 * s), ra);
+        tmem_ld16x256b_x8(tq + kColS + 64 * (2 * s + 1), rb);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t a[16], bb[16];
-          tmem_ld16(tq + kColS + 64 * (2 * s) + 16 * c, a);
-          tmem_ld16(tq + kColS + 64 * (2 * s + 1) + 16 * c, bb);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            x[16 * c + i] = (__uint_as_float(a[i]) + __uint_as_float(bb[i])) * cs;
-        }
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(ra[i]) + __uint_as_float(rb[i]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_addr(m.s_free[s]));
       }
-
-      float tmax = -INFINITY;
+      float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        x[k] = k < nv ? x[k] : -INFINITY;
-        tmax = fmaxf(tmax, x[k]);
-      }
-      float mnew = mrun, alpha = 1.f;
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float &v = x[4 * j + 2 * h + e];
+            v = (8 * j + pair + e) < nv ? v : -INFINITY;
+            tmax[h] = fmaxf(tmax[h], v);
+          }
+      float mnew[2], alpha[2];
       bool resc = false;
-      if (t == w.t0) {
-        mnew = tmax;
-      } else if (tmax > mrun + kRescaleThreshold) {
-        mnew = tmax;
-        alpha = exp2f(mrun - mnew);
-        resc = srow;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 1));
+        tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 2));
+        const float sm = tmax[h] * cs;  // cs > 0: the scaled maximum
+        mnew[h] = mrun[h];
+        alpha[h] = 1.f;
+        if (t == w.t0) {
+          mnew[h] = sm;
+        } else if (sm > mrun[h] + kRescaleThreshold) {
+          mnew[h] = sm;
+          alpha[h] = exp2f(mrun[h] - sm);
+          resc = true;
+        }
       }
-      // PV of the previous tile has finished: O^T is stable and P is free
-      if (got) got = mbar_wait(bar_addr(m.p_free), (p_it & 1) ^ 1, abort, kTimeoutNs);
       if (!named_sync_and(1, 128, got)) { ok = false; break; }
-      tc_fence_after();
-      if (srow) m.alpha[p_it & 1][hrow] = alpha;
+      if ((lane & 3) == 0) {
+        m.alpha[p_it & 1][row[0]] = alpha[0];
+        m.alpha[p_it & 1][row[1]] = alpha[1];
+      }
       if (named_sync_or(1, 128, resc)) {
+        // rescaling O^T needs the previous tile's PV to have finished
+        got = mbar_wait(bar_addr(m.p_free), (p_it - 1) & 1, abort, kTimeoutNs);
+        if (!named_sync_and(1, 128, got)) { ok = false; break; }
+        tc_fence_after();
         const float *al = m.alpha[p_it & 1];
         for (int c = 0; c < 4; ++c)
           for (int hb = 0; hb < tp.npv / 16; ++hb) {
@@ -369,25 +401,24 @@ __device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
           }
         tmem_wait_st();
       }
-      if (srow) {
-        unsigned char *prow = smem + kOffP + (hrow >> 3) * 1024 + (hrow & 7) * 128;
+      // P = 2^(s cs - m) in bf16, row-major [head][token] in the swizzled
+      // K-major layout: each lane writes 4-byte token pairs
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        unsigned char *prow = smem + kOffKv + s * kStageBytes + (row[h] >> 3) * kAtomBytes + kPOff +
+                              (row[h] & 7) * 128 + (lane & 3) * 4;
         float lsum = 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(x[8 * c + 2 * e] - mnew),
-                                                      exp2f(x[8 * c + 2 * e + 1] - mnew));
-            const float2 back = __bfloat1622float2(b2);
-            lsum += back.x + back.y;
-            pk[e] = *reinterpret_cast<uint32_t *>(&b2);
-          }
-          *reinterpret_cast<uint4 *>(prow + ((c ^ (hrow & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int j = 0; j < 8; ++j) {
+          __nv_bfloat162 b2 =
+              __floats2bfloat162_rn(exp2f(fmaf(x[4 * j + 2 * h], cs, -mnew[h])),
+                                    exp2f(fmaf(x[4 * j + 2 * h + 1], cs, -mnew[h])));
+          const float2 back = __bfloat1622float2(b2);
+          lsum += back.x + back.y;
+          *reinterpret_cast<__nv_bfloat162 *>(prow + ((j ^ (row[h] & 7)) << 4)) = b2;
         }
-        ell = ell * alpha + lsum;
-        mrun = mnew;
+        ellp[h] = ellp[h] * alpha[h] + lsum;
+        mrun[h] = mnew[h];
       }
       // rows [nv, roundup16(nv)) of V are read by the last PV step but hold no
       // owned token (stale or unowned data): zero their 512 value dims
@@ -395,20 +426,30 @@ __device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
         unsigned char *stage = smem + kOffKv + s * kStageBytes;
         const int r0 = nv, nrow = ((nv + 15) & ~15) - nv;
         for (int i = gt; i < nrow * 64; i += 128) {
-          const int row = r0 + (i >> 6), kb = (i >> 3) & 7, ch = i & 7;
-          *reinterpret_cast<uint4 *>(stage + (row >> 3) * kAtomBytes + kb * 1024 + (row & 7) * 128 +
+          const int rr = r0 + (i >> 6), kb = (i >> 3) & 7, ch = i & 7;
+          *reinterpret_cast<uint4 *>(stage + (rr >> 3) * kAtomBytes + kb * 1024 + (rr & 7) * 128 +
                                      ch * 16) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(m.p_full));
+      if (lane == 0) mbar_arrive(bar_addr(m.p_full[s]));
     }
     if (!ok) break;
 
+    // the four lanes of a head hold parts of its sum
+    float ell[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      ell[h] = ellp[h] + __shfl_xor_sync(0xffffffffu, ellp[h], 1);
+      ell[h] += __shfl_xor_sync(0xffffffffu, ell[h], 2);
+    }
     // ---- epilogue of this CTA's share of request v
-    if (srow) m.ell[hrow] = ell;
+    if ((lane & 3) == 0) {  // per-head output scale: kv_scale / sum
+      m.ell[row[0]] = p.kv_scale / ell[0];
+      m.ell[row[1]] = p.kv_scale / ell[1];
+    }
     const bool got_o = mbar_wait(bar_addr(m.o_full), o_it & 1, abort, kTimeoutNs);
     if (!named_sync_and(2, 128, got_o)) { ok = false; break; }
     tc_fence_after();
@@ -416,35 +457,40 @@ __device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
     const bool split = si.nsplits > 1;
     const size_t out_row0 = size_t(w.b) * p.heads + size_t(w.g) * kHeads;
     for (int c = 0; c < 4; ++c) {
+      // one value dimension (this thread's TMEM lane) x 64 heads of chunk c:
+      // four loads in flight, one wait
       const int dv = 128 * c + 32 * q + lane;
-      for (int hb = 0; hb < tp.npv / 16; ++hb) {
-        uint32_t o[16];
-        tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
-        tmem_wait_ld();
+      uint32_t o[4][16];
+#pragma unroll
+      for (int hb = 0; hb < 4; ++hb) tmem_ld16(tq + kColO + 64 * c + 16 * hb, o[hb]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int hb = 0; hb < 4; ++hb)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int h = 16 * hb + i;
           if (h < hn) {
-            const float val = __uint_as_float(o[i]) * (p.kv_scale / m.ell[h]);
+            const float val = __uint_as_float(o[hb][i]) * m.ell[h];
             if (!split)
               p.out[(out_row0 + h) * kDv + dv] = __float2bfloat16_rn(val);
             else
               slot_out_ptr(p)[(size_t(si.slot) * kSlotHeads + h) * kDv + dv] = val;
           }
         }
-      }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_addr(m.o_free));
     ++o_it;
-    if (srow && hrow < hn) {
-      const float lse2 = mrun + log2f(ell);
-      if (!split)
-        p.lse[out_row0 + hrow] = lse_out(p, lse2);
-      else
-        slot_lse_ptr(p)[si.slot * kSlotHeads + hrow] = lse2;
-    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if ((lane & 3) == 0 && row[h] < hn) {
+        const float lse2 = mrun[h] + log2f(ell[h]);
+        if (!split)
+          p.lse[out_row0 + row[h]] = lse_out(p, lse2);
+        else
+          slot_lse_ptr(p)[si.slot * kSlotHeads + row[h]] = lse2;
+      }
     if (gt == 0) record_split(p, w.v, si);
   }
   if (!ok) atomicOr(err, kErrTimeout);
@@ -466,26 +512,27 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int *err = error_word(p);
 
-  // Q rows past the request's heads and P rows past them are read by the
-  // MMAs but never loaded: they must hold finite values.
+  // Q rows past the request's heads are read by the MMAs but never loaded:
+  // they must hold finite values.  (P rows past them are written each tile.)
   for (int i = tid; i < kQBytes / 16; i += kThreads)
     reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < kPBytes / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(smem + kOffP)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_addr(m.kv_full[s]), 1);
-      mbar_init(bar_addr(m.kv_empty[s]), 1);
-      mbar_init(bar_addr(m.s_full[s]), 1);
+      mbar_init(bar_addr(m.kv_empty[s]), 2);  // both PV issuers commit
+      mbar_init(bar_addr(m.s_full[s]), 2);   // both score issuers commit
       mbar_init(bar_addr(m.s_free[s]), 4);
     }
     mbar_init(bar_addr(m.q_full), 1);
-    mbar_init(bar_addr(m.q_empty), 1);
-    mbar_init(bar_addr(m.p_full), 4);
-    mbar_init(bar_addr(m.p_free), 1);
-    mbar_init(bar_addr(m.o_full), 1);
+    mbar_init(bar_addr(m.q_empty), 2);
+    // one per stage: the softmax runs ahead of the PV issuers, and tile k + 2
+    // (same stage) cannot reach the softmax before PV k has been issued
+    mbar_init(bar_addr(m.p_full[0]), 4);
+    mbar_init(bar_addr(m.p_full[1]), 4);
+    mbar_init(bar_addr(m.p_free), 2);
+    mbar_init(bar_addr(m.o_full), 2);
     mbar_init(bar_addr(m.o_free), 4);
-    mbar_init(bar_addr(m.drain), 1);
+    mbar_init(bar_addr(m.drain), 4);       // all four MMA issuers
     m.abort = 0;
     fence_barrier_init();
   }
@@ -510,9 +557,11 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     if (warp == 0) {
       if (lane == 0)
         tc_producer(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
-    } else if (warp == 1) {
-      if (lane == 0) tc_mma(tp, r, m, sbase + kOffQ, sbase + kOffKv, sbase + kOffP, tmem, err);
-    } else if (warp >= 4) {
+    } else if (warp == 1 || warp == 2) {
+      if (lane == 0) tc_mma_s(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
+    } else if (warp == 3 || warp == 8) {
+      if (lane == 0) tc_mma_pv(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
+    } else {
       tc_softmax(tp, r, m, smem, tmem, err);
     }
   }

@@ -4,17 +4,18 @@
 // recorded {first CTA, number of splits, its slot}; split k > 0 lives in slot
 // 2 (first + k).  The merge is the LSE-weighted combine of those splits.
 //
-// One CTA per (virtual request, 8 heads): a warp per head reduces the split
+// One CTA per (virtual request, 2 heads): a warp per head reduces the split
 // LSEs (max, then the weights 2^(lse_k - max) kept in shared memory), then
-// each thread owns 4 of the 512 value dims and streams the splits' float4s
-// with independent loads.
+// each thread owns 4 of the 512 value dims and keeps the loads of 4 splits x 2
+// heads in flight before accumulating.
 #include "common.cuh"
 #include "splits.cuh"
 
 namespace mla {
 
 constexpr int kMergeThreads = 128;  // x 4 dims = 512
-constexpr int kMergeHeads = 8;
+constexpr int kMergeHeads = 2;      // heads per CTA
+constexpr int kMergeBatch = 4;      // splits whose loads are in flight together
 
 __global__ void __launch_bounds__(kMergeThreads)
     split_merge_kernel(DecodeParams p, int max_splits) {
@@ -34,18 +35,16 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float *inv = s_w + max_splits * kMergeHeads;
   const size_t row0 = size_t(b) * p.heads + size_t(g) * p.heads_per_group + h_first;
+  auto slot_of_split = [&](int k) { return k == 0 ? info.z : 2 * (info.x + k); };
 
-  for (int hh = warp; hh < hn; hh += kMergeThreads / 32) {
+  if (warp < hn) {  // warp hh: weights of head hh over the splits
+    const int hh = warp;
     float mx = -INFINITY;
-    for (int k = lane; k < ns; k += 32) {
-      const int slot = k == 0 ? info.z : 2 * (info.x + k);
-      mx = fmaxf(mx, sl[slot * kSlotHeads + h_first + hh]);
-    }
+    for (int k = lane; k < ns; k += 32) mx = fmaxf(mx, sl[slot_of_split(k) * kSlotHeads + h_first + hh]);
     for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float sum = 0.f;
     for (int k = lane; k < ns; k += 32) {
-      const int slot = k == 0 ? info.z : 2 * (info.x + k);
-      const float w = exp2f(sl[slot * kSlotHeads + h_first + hh] - mx);
+      const float w = exp2f(sl[slot_of_split(k) * kSlotHeads + h_first + hh] - mx);
       s_w[k * kMergeHeads + hh] = w;
       sum += w;
     }
@@ -58,34 +57,36 @@ __global__ void __launch_bounds__(kMergeThreads)
   __syncthreads();
 
   const int d4 = threadIdx.x;  // value dims 4 d4 .. 4 d4 + 3
-  for (int hh = 0; hh < hn; ++hh) {
-    const size_t col = size_t(h_first + hh) * kDv / 4 + d4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int k = 0;
-    for (; k + 4 <= ns; k += 4) {
-      float4 x[4];
-      float w[4];
+  float4 acc[kMergeHeads];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int slot = (k + u) == 0 ? info.z : 2 * (info.x + k + u);
-        x[u] = reinterpret_cast<const float4 *>(so + size_t(slot) * kSlotHeads * kDv)[col];
-        w[u] = s_w[(k + u) * kMergeHeads + hh];
-      }
+  for (int hh = 0; hh < kMergeHeads; ++hh) acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < ns; k0 += kMergeBatch) {
+    float4 x[kMergeBatch][kMergeHeads];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        acc.x += w[u] * x[u].x; acc.y += w[u] * x[u].y;
-        acc.z += w[u] * x[u].z; acc.w += w[u] * x[u].w;
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int k = k0 + u;
+      const float4 *src = reinterpret_cast<const float4 *>(
+          so + size_t(k < ns ? slot_of_split(k) : 0) * kSlotHeads * kDv);
+#pragma unroll
+      for (int hh = 0; hh < kMergeHeads; ++hh)
+        x[u][hh] = (k < ns && hh < hn) ? src[size_t(h_first + hh) * (kDv / 4) + d4]
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u)
+#pragma unroll
+      for (int hh = 0; hh < kMergeHeads; ++hh) {
+        const float w = (k0 + u < ns) ? s_w[(k0 + u) * kMergeHeads + hh] : 0.f;
+        acc[hh].x += w * x[u][hh].x; acc[hh].y += w * x[u][hh].y;
+        acc[hh].z += w * x[u][hh].z; acc[hh].w += w * x[u][hh].w;
       }
-    }
-    for (; k < ns; ++k) {
-      const int slot = k == 0 ? info.z : 2 * (info.x + k);
-      const float4 x = reinterpret_cast<const float4 *>(so + size_t(slot) * kSlotHeads * kDv)[col];
-      const float w = s_w[k * kMergeHeads + hh];
-      acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
-    }
-    const float s = inv[hh];
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * s, acc.y * s);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * s, acc.w * s);
+  }
+#pragma unroll
+  for (int hh = 0; hh < kMergeHeads; ++hh) {
+    if (hh >= hn) break;
+    const float sc = inv[hh];
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[hh].x * sc, acc[hh].y * sc);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[hh].z * sc, acc[hh].w * sc);
     uint2 pk;
     pk.x = *reinterpret_cast<uint32_t *>(&lo);
     pk.y = *reinterpret_cast<uint32_t *>(&hi);

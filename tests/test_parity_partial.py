@@ -189,3 +189,19 @@ def test_multi_token_query_is_rejected():
                            case.sm_scale, 0, out, lse, workspace=torch.zeros(
                                1 << 20, dtype=torch.uint8, device="cuda"))
     assert e.value.status == -2
+
+
+def test_many_back_to_back_calls_never_time_out_and_stay_identical():
+    """Pipeline races (a lost or aliased barrier phase) would show up as a
+    timeout reported in the workspace or as differing outputs."""
+    case = workloads.config_long32k(device="cuda", batch=32, pool_pages=17000, seed=3)
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table)
+    ref_out, ref_lse = run_partial(case, 0, 0, workspace=ws)
+    out = torch.empty_like(ref_out)
+    lse = torch.empty_like(ref_lse)
+    for _ in range(300):
+        mla.decode_partial(case.q, case.kv_pages, case.block_table, case.seq_lens, 0, 1,
+                           case.sm_scale, 0, out, lse, workspace=ws)
+    assert mla.check_workspace(ws) == 0
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(lse, ref_lse)
