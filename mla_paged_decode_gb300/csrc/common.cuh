@@ -86,29 +86,39 @@ __device__ __forceinline__ int request_tiles(const DecodeParams &p, int v) {
 
 // ---------------------------------------------------------------- split schedule
 //
-// Stream-K split of the concatenated tile sequence of all virtual requests
-// v = b * head_groups + g (tiles_v = ceil(local_len / 64)) over G_eff =
-// min(gridDim.x, T) CTAs: CTA c owns tiles [c*T/G_eff, (c+1)*T/G_eff).  A
-// request crossing a boundary is split; each split writes a normalised fp32
-// partial into slot 2c (the CTA's first request) or 2c+1 (its last); the
-// request's first CTA records {itself, split count, its slot} and a second
-// kernel merges the splits.
+// Cost-weighted stream-K split of the concatenated tile sequence of all
+// virtual requests v = b * head_groups + g (tiles_v = ceil(local_len / 64)).
+// Every request with tiles costs tiles_v + kPieceCost: the extra units stand
+// for the per-piece work (Q load, pipeline refill, epilogue), so a CTA whose
+// range crosses a request boundary gets fewer tiles.  Request v occupies cost
+// units [P_v, P_v + tiles_v) followed by a gap of kPieceCost; C = total cost.
+// G_eff = min(gridDim.x, C) CTAs; CTA c owns the tiles whose cost lies in
+// [c*C/G_eff, (c+1)*C/G_eff).  A request crossing a boundary is split; each
+// split writes a normalised fp32 partial into slot 2c (the CTA's first
+// request) or 2c+1 (its last); the request's first CTA records {itself,
+// split count, its slot} and a second kernel merges the splits.
+
+constexpr int kPieceCost = 4;
 
 struct CtaRange {
-  long long start, end;   // global tile range of this CTA
-  long long total;        // T
-  int g_eff;              // CTAs that own tiles
+  long long start, end;   // cost range of this CTA
+  long long total;        // C
+  int g_eff;              // CTAs that own cost units
   int v_begin;            // first virtual request with tiles in range
-  long long p_begin;      // tile prefix of v_begin
+  long long p_begin;      // cost start of v_begin
 };
 
-__device__ __forceinline__ long long sched_start(long long c, long long T, int g_eff) {
-  return c * T / g_eff;
+__device__ __forceinline__ long long sched_start(long long c, long long C, int g_eff) {
+  return c * C / g_eff;
 }
 
 // Largest c with sched_start(c) <= x.
-__device__ __forceinline__ int sched_owner(long long x, long long T, int g_eff) {
-  return int(((x + 1) * g_eff - 1) / T);
+__device__ __forceinline__ int sched_owner(long long x, long long C, int g_eff) {
+  return int(((x + 1) * g_eff - 1) / C);
+}
+
+__device__ __forceinline__ long long request_cost(int tiles) {
+  return tiles > 0 ? tiles + kPieceCost : 0;
 }
 
 // Block-wide: computes this CTA's range.  All threads must call it.
@@ -116,22 +126,22 @@ __device__ __forceinline__ int sched_owner(long long x, long long T, int g_eff) 
 __device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long long *scratch) {
   const int V = p.batch * p.head_groups;
   const int tid = threadIdx.x, nw = blockDim.x / 32, lane = tid & 31, warp = tid >> 5;
-  // pass 1: total tiles
+  // pass 1: total cost
   long long mine = 0;
-  for (int v = tid; v < V; v += blockDim.x) mine += request_tiles(p, v);
+  for (int v = tid; v < V; v += blockDim.x) mine += request_cost(request_tiles(p, v));
   for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
   if (lane == 0) scratch[warp] = mine;
   __syncthreads();
   if (tid == 0) {
-    long long T = 0;
-    for (int w = 0; w < nw; ++w) T += scratch[w];
-    r->total = T;
-    r->g_eff = int(T < (long long)gridDim.x ? T : (long long)gridDim.x);
+    long long C = 0;
+    for (int w = 0; w < nw; ++w) C += scratch[w];
+    r->total = C;
+    r->g_eff = int(C < (long long)gridDim.x ? C : (long long)gridDim.x);
     r->v_begin = V;
     r->p_begin = 0;
     if (r->g_eff > 0 && (int)blockIdx.x < r->g_eff) {
-      r->start = sched_start(blockIdx.x, T, r->g_eff);
-      r->end = sched_start(blockIdx.x + 1, T, r->g_eff);
+      r->start = sched_start(blockIdx.x, C, r->g_eff);
+      r->end = sched_start(blockIdx.x + 1, C, r->g_eff);
     } else {
       r->start = r->end = 0;
     }
@@ -139,12 +149,14 @@ __device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long lon
   __syncthreads();
   const long long start = r->start, end = r->end;
   if (start >= end) return;
-  // pass 2: locate the request holding tile `start` (chunked block scan)
+  // pass 2: the first request whose tiles end after `start` (chunked block
+  // scan of the costs); its predecessor ends at P_v - kPieceCost
   long long base = 0;
   for (int v0 = 0; v0 < V; v0 += blockDim.x) {
     int v = v0 + tid;
-    long long t = v < V ? request_tiles(p, v) : 0;
-    long long incl = t;
+    const int tiles = v < V ? request_tiles(p, v) : 0;
+    const long long cst = request_cost(tiles);
+    long long incl = cst;
     for (int o = 1; o < 32; o <<= 1) {
       long long y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
@@ -157,8 +169,8 @@ __device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long lon
       if (w < warp) wbase += scratch[w];
       chunk += scratch[w];
     }
-    long long excl = base + wbase + incl - t;
-    if (t > 0 && excl <= start && start < excl + t) {
+    const long long excl = base + wbase + incl - cst;
+    if (tiles > 0 && excl + tiles > start && excl - kPieceCost <= start) {
       r->v_begin = v;
       r->p_begin = excl;
     }

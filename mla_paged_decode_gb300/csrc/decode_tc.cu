@@ -96,7 +96,7 @@ struct Walk {
     }
     return false;
   }
-  __device__ void advance() { pv += tiles; ++v; }
+  __device__ void advance() { pv += request_cost(tiles); ++v; }
 };
 
 // One position in the walk: request + tile.
@@ -134,7 +134,7 @@ __device__ __forceinline__ void tile_pages(const DecodeParams &p, long long t, i
 
 constexpr int kPrefetchAhead = 2;  // tiles whose pages are pulled into L2 ahead of the stage
 
-__device__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
+__device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                             uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
                             int *err) {
   using namespace tc;
@@ -218,7 +218,7 @@ __device__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, ui
 
 // Descriptors: an offset is added to the encoded start address (bits 0..13,
 // address >> 4), which never carries because shared addresses stay below 256 KB.
-__device__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
+__device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                          uint32_t sKv, uint32_t tmem, int chain, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
@@ -258,7 +258,7 @@ __device__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint3
 
 // O^T(chunk c) (+)= V^T(tile) P^T over ceil(nv/16) steps of 16 tokens; issuer
 // `half` takes value chunks 2 half and 2 half + 1.
-__device__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
+__device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
                           uint32_t tmem, int half, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
@@ -308,7 +308,7 @@ __device__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint
 
 // ------------------------------------------------------------------ softmax + epilogue
 
-__device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
+__device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
                            unsigned char *smem, uint32_t tmem, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
@@ -465,18 +465,23 @@ __device__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
       for (int hb = 0; hb < 4; ++hb) tmem_ld16(tq + kColO + 64 * c + 16 * hb, o[hb]);
       tmem_wait_ld();
 #pragma unroll
-      for (int hb = 0; hb < 4; ++hb)
+      for (int hb = 0; hb < 4; ++hb) {
+        // the block's 16 output scales, read before its stores
+        float sc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sc[i] = m.ell[16 * hb + i];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int h = 16 * hb + i;
           if (h < hn) {
-            const float val = __uint_as_float(o[hb][i]) * m.ell[h];
+            const float val = __uint_as_float(o[hb][i]) * sc[i];
             if (!split)
               p.out[(out_row0 + h) * kDv + dv] = __float2bfloat16_rn(val);
             else
               slot_out_ptr(p)[(size_t(si.slot) * kSlotHeads + h) * kDv + dv] = val;
           }
         }
+      }
     }
     tc_fence_before();
     __syncwarp();

@@ -20,6 +20,9 @@ constexpr int kMergeBatch = 4;      // splits whose loads are in flight together
 __global__ void __launch_bounds__(kMergeThreads)
     split_merge_kernel(DecodeParams p, int max_splits) {
   extern __shared__ float s_w[];  // [max_splits][kMergeHeads] weights, then [kMergeHeads] 1/sum
+  // launched as a programmatic dependent of the decode kernel: wait until its
+  // grid has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int v = blockIdx.x;
   const int b = v / p.head_groups, g = v % p.head_groups;
   const int h_first = blockIdx.y * kMergeHeads;  // within the head group
@@ -99,8 +102,17 @@ cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t str
   if (V == 0) return cudaSuccess;
   dim3 blocks(V, (p.heads_per_group + kMergeHeads - 1) / kMergeHeads);
   const size_t smem = sizeof(float) * (size_t(grid) * kMergeHeads + kMergeHeads);
-  split_merge_kernel<<<blocks, kMergeThreads, smem, stream>>>(p, grid);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = blocks;
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_merge_kernel, p, grid);
 }
 
 }  // namespace mla
