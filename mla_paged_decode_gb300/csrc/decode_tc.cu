@@ -350,17 +350,19 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_addr(m.s_free[s]));
       }
+      if (nv < kTile) {  // the tile's tail: tokens past the request's end
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            x[4 * j + i] = (8 * j + pair + (i & 1)) < nv ? x[4 * j + i] : -INFINITY;
+      }
       float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int j = 0; j < 8; ++j)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float &v = x[4 * j + 2 * h + e];
-            v = (8 * j + pair + e) < nv ? v : -INFINITY;
-            tmax[h] = fmaxf(tmax[h], v);
-          }
+          tmax[h] = fmaxf(tmax[h], fmaxf(x[4 * j + 2 * h], x[4 * j + 2 * h + 1]));
       float mnew[2], alpha[2];
       bool resc = false;
 #pragma unroll
@@ -378,28 +380,33 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
           resc = true;
         }
       }
-      if (!named_sync_and(1, 128, got)) { ok = false; break; }
       if ((lane & 3) == 0) {
         m.alpha[p_it & 1][row[0]] = alpha[0];
         m.alpha[p_it & 1][row[1]] = alpha[1];
       }
-      if (named_sync_or(1, 128, resc)) {
-        // rescaling O^T needs the previous tile's PV to have finished
-        got = mbar_wait(bar_addr(m.p_free), (p_it - 1) & 1, abort, kTimeoutNs);
+      // one group barrier in the common case; more only when some lane needs
+      // an O rescale or a wait gave up.  Every branch below follows a group
+      // result, so all 128 lanes take it together.
+      if (named_sync_or(1, 128, resc || !got)) {
         if (!named_sync_and(1, 128, got)) { ok = false; break; }
-        tc_fence_after();
-        const float *al = m.alpha[p_it & 1];
-        for (int c = 0; c < 4; ++c)
-          for (int hb = 0; hb < tp.npv / 16; ++hb) {
-            uint32_t o[16];
-            tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
-            tmem_wait_ld();
+        if (named_sync_or(1, 128, resc)) {
+          // rescaling O^T needs the previous tile's PV to have finished
+          const bool pv_done = mbar_wait(bar_addr(m.p_free), (p_it - 1) & 1, abort, kTimeoutNs);
+          if (!named_sync_and(1, 128, pv_done)) { ok = false; break; }
+          tc_fence_after();
+          const float *al = m.alpha[p_it & 1];
+          for (int c = 0; c < 4; ++c)
+            for (int hb = 0; hb < tp.npv / 16; ++hb) {
+              uint32_t o[16];
+              tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
+              tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              o[i] = __float_as_uint(__uint_as_float(o[i]) * al[16 * hb + i]);
-            tmem_st16(tq + kColO + 64 * c + 16 * hb, o);
-          }
-        tmem_wait_st();
+              for (int i = 0; i < 16; ++i)
+                o[i] = __float_as_uint(__uint_as_float(o[i]) * al[16 * hb + i]);
+              tmem_st16(tq + kColO + 64 * c + 16 * hb, o);
+            }
+          tmem_wait_st();
+        }
       }
       // P = 2^(s cs - m) in bf16, row-major [head][token] in the swizzled
       // K-major layout: each lane writes 4-byte token pairs

@@ -205,3 +205,19 @@ def test_many_back_to_back_calls_never_time_out_and_stay_identical():
     assert mla.check_workspace(ws) == 0
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     assert torch.equal(lse, ref_lse)
+
+
+@pytest.mark.parametrize("num_parts", [1, 2])
+def test_growing_scores_take_the_rescale_path(num_parts):
+    """The rope dims of the keys grow along the sequence, so a later tile's
+    maximum exceeds the running maximum by far more than 2^8 and O must be
+    rescaled; the values (latent dims) keep their N(0, 1) scale."""
+    case = workloads.make_decode_case("growing", 64, [2000, 700, 129], seed=12, device="cuda",
+                                      num_parts=num_parts)
+    bt = case.block_table.cpu()
+    kv = case.kv_pages.float()
+    for b, L in enumerate(case.seq_lens.cpu().tolist()):
+        for i in range((L + 63) // 64):
+            kv[int(bt[b, i]), :, 512:] *= 1.0 + 1.5 * i
+    case.kv_pages = kv.to(torch.bfloat16)
+    _check_all(case)
