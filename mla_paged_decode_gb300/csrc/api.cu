@@ -104,16 +104,17 @@ int tensor_map_fail(const char *what, CUresult r) {
 
 constexpr int kTcHeadsPerGroup = 64;
 
-// The tensor-core kernel takes bf16 caches and partitions whose owned rows of
-// a page form whole 8-row groups (P | 8).
-bool tensor_core_path(const mla_decode_desc *d, int num_parts) {
-  return d->kv_dtype == MLA_KV_BF16 &&
-         (num_parts == 1 || num_parts == 2 || num_parts == 4 || num_parts == 8);
+// The tensor-core kernel takes partitions whose owned rows of a page form
+// whole 8-row groups (P | 8), for bf16 and e4m3 caches alike.
+bool tensor_core_path(const mla_decode_desc *, int num_parts) {
+  return num_parts == 1 || num_parts == 2 || num_parts == 4 || num_parts == 8;
 }
 
 // Q as [B*H rows, 576] bf16, one 64-column swizzled box of min(64, H) rows;
-// partition r's rows of the cache as a 4-D view (64 dims, 8 rows of stride P,
-// 9 blocks of 64 dims, groups of 8 rows), one box = one page's owned rows.
+// partition r's rows of a bf16 cache as a 4-D view (64 dims, 8 rows of stride
+// P, 9 blocks of 64 dims, groups of 8 rows), one box = one page's owned rows;
+// of an e4m3 cache as a 2-D view (144 words of 4 fp8 values, rows of stride
+// P), one unswizzled box = one page's 64/P owned rows of 576 B.
 int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, int part_id,
                      int num_parts, CUtensorMap *tm_q, CUtensorMap *tm_kv) {
   EncodeTiled enc = encode_tiled();
@@ -132,7 +133,20 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("q", r);
   }
-  {
+  if (d->kv_dtype == MLA_KV_E4M3) {
+    const cuuint64_t P = cuuint64_t(num_parts);
+    const cuuint32_t R = cuuint32_t(mla::kPage / num_parts);
+    const cuuint64_t row8 = cuuint64_t(mla::kDqk);
+    const char *base = static_cast<const char *>(kv) + size_t(part_id) * row8;
+    cuuint64_t dims[2] = {row8 / 4, cuuint64_t(d->num_pages) * R};
+    cuuint64_t strides[1] = {P * row8};
+    cuuint32_t box[2] = {cuuint32_t(row8 / 4), R};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<char *>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3", r);
+  } else {
     const cuuint64_t P = cuuint64_t(num_parts);
     const cuuint32_t G = cuuint32_t(8 / num_parts);
     const char *base = static_cast<const char *>(kv) + size_t(part_id) * row;

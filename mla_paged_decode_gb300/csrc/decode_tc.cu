@@ -18,6 +18,14 @@
 //                   64 tokens.  For the epilogue every thread owns TMEM lane
 //                   32q + lane of O^T: one value dimension.
 //
+// e4m3 caches (the same kernel with F8 = true, 384 threads): the producer
+// lands each owned fp8 row (576 B) in the upper half of its stage, and
+// warps 9..11 expand them in place into the same swizzled layout as f16 (an
+// exact conversion), converting the request's Q to f16 as well with one
+// power-of-two scale that keeps its largest element in [2^14, 2^15); the
+// MMAs then run with f16 operands, P is written as f16, and the scores carry
+// sm_scale * kv_scale / (that power of two).
+//
 // Pipeline per tile i (stage / S buffer i mod 2): producer -> kv_full ->
 // MMA S_i (36 MMAs, two interleaved accumulators so consecutive MMAs are
 // independent) -> s_full -> softmax reads S_i, frees it (s_free), waits for
@@ -35,7 +43,10 @@ namespace mla {
 using namespace sm100;
 
 namespace tc {
-constexpr int kThreads = 288;
+constexpr int kThreads = 288;                // bf16 cache
+constexpr int kThreadsF8 = 384;              // e4m3 cache: + 3 converter warps
+constexpr int kConvWarp0 = 9;
+constexpr int kConvThreads = 96;
 constexpr int kHeads = 64;                   // heads per virtual request (M of S)
 constexpr int kKb = kDqk / 64;               // 9 blocks of 64 bf16 = 128 B
 constexpr int kQBytes = kKb * 64 * 128;      // [kb][64 rows][128 B]
@@ -54,6 +65,9 @@ constexpr uint32_t kColS = 256;              // S(buffer s, chain k): 256 + 64 (
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr float kRescaleThreshold = 8.f;     // base-2 units
+constexpr int kRawOff = kStageBytes / 2;     // e4m3: raw [64 rows][576 B] in the stage's upper half
+constexpr int kRawRow = kDqk;                // bytes of one fp8 row
+constexpr int kRawChunks = kRawRow / 16;     // 36 chunks of 16 values
 }  // namespace tc
 
 struct TcParams {
@@ -63,15 +77,21 @@ struct TcParams {
   int groups_per_page;  // 8-row atoms one page holds for this partition: 8 / P
 };
 
+template <bool F8>
+constexpr int tc_threads() { return F8 ? tc::kThreadsF8 : tc::kThreads; }
+
 struct TcMisc {
   uint64_t kv_full[2], kv_empty[2], q_full, q_empty, s_full[2], s_free[2];
   uint64_t p_full[2], p_free, o_full, o_free, drain;
+  uint64_t kv_conv[2], q_ready;  // e4m3 only: stage / Q expanded to f16
   uint32_t tmem_base;
   int abort;
   float alpha[2][64];
   float ell[64];
+  float tscale[2];               // e4m3 only: score scale (base 2) of the tile in each stage
+  uint32_t conv_max[4];
   CtaRange range;
-  long long scratch[tc::kThreads / 32 + 1];
+  long long scratch[tc::kThreadsF8 / 32 + 1];
 };
 static_assert(sizeof(TcMisc) + 1024 <= tc::kSmemBytes - tc::kOffMisc, "shared memory budget");
 
@@ -134,6 +154,7 @@ __device__ __forceinline__ void tile_pages(const DecodeParams &p, long long t, i
 
 constexpr int kPrefetchAhead = 2;  // tiles whose pages are pulled into L2 ahead of the stage
 
+template <bool F8>
 __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                             uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
                             int *err) {
@@ -142,7 +163,12 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   volatile int *abort = &m.abort;
   uint32_t kv_it = 0, q_it = 0;
   int last_q = -1, last_kv[2] = {-1, -1};
-  const uint32_t page_bytes = uint32_t(tp.groups_per_page) * kAtomBytes;
+  // bf16: one 4-D box of groups_per_page swizzled atoms per page; e4m3: one
+  // 2-D box of the page's 8 * groups_per_page owned rows, 576 B each
+  const int rows_per_page = 8 * tp.groups_per_page;
+  const uint32_t page_bytes =
+      F8 ? uint32_t(rows_per_page * kRawRow) : uint32_t(tp.groups_per_page) * kAtomBytes;
+  const uint32_t dst0 = F8 ? sKv + kRawOff : sKv;
   bool ok = true;
 
   // L2 prefetch of the pages of the tile kPrefetchAhead positions ahead: the
@@ -154,7 +180,12 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
     tile_pages(p, ahead.t, ahead.w.n, &lp0, &lp1);
     for (int k = 0; k <= lp1 - lp0; ++k) {
       const int pg = p.block_table[size_t(ahead.w.b) * p.max_pages + lp0 + k];
-      if (pg >= 0 && pg < p.num_pages) tma_prefetch_4d(tm_kv, 0, 0, 0, pg * tp.groups_per_page);
+      if (pg >= 0 && pg < p.num_pages) {
+        if (F8)
+          tma_prefetch_2d(tm_kv, 0, pg * rows_per_page);
+        else
+          tma_prefetch_4d(tm_kv, 0, 0, 0, pg * tp.groups_per_page);
+      }
     }
     ahead.step();
   };
@@ -194,9 +225,14 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
     }
     mbar_arrive_expect_tx(bar_addr(m.kv_full[s]), bytes);
     for (int k = 0; k <= lp1 - lp0; ++k)
-      if (pages[k] >= 0)
-        tma_load_4d(sKv + s * kStageBytes + k * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0, 0, 0,
-                    pages[k] * tp.groups_per_page);
+      if (pages[k] >= 0) {
+        if (F8)
+          tma_load_2d(dst0 + s * kStageBytes + k * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0,
+                      pages[k] * rows_per_page);
+        else
+          tma_load_4d(dst0 + s * kStageBytes + k * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0,
+                      0, 0, pages[k] * tp.groups_per_page);
+      }
     last_kv[s] = (kv_it >> 1) & 1;
     ++kv_it;
     prefetch();
@@ -218,12 +254,16 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 
 // Descriptors: an offset is added to the encoded start address (bits 0..13,
 // address >> 4), which never carries because shared addresses stay below 256 KB.
+template <bool F8>
 __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                          uint32_t sKv, uint32_t tmem, int chain, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
-  const uint32_t idesc_s = idesc_bf16_f32(64, 64, false, false);
+  const uint32_t idesc_s = idesc_f32acc(64, 64, false, false, !F8);
+  // e4m3: the stage and Q are ready once the converter has expanded them
+  uint64_t *kv_ready = F8 ? m.kv_conv : m.kv_full;
+  uint64_t &q_ready = F8 ? m.q_ready : m.q_full;
   const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);            // Q, K-major
   const uint64_t dk0 = smem_desc_sw128(sKv, 16, kAtomBytes);    // K tile, K-major
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
@@ -232,9 +272,9 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
   for (TileCursor sc(p, r); sc.live; sc.step(), ++s_it) {
     const int st = s_it & 1;
     const uint32_t ph = (s_it >> 1) & 1;
-    if (!mbar_wait(bar_addr(m.kv_full[st]), ph, abort, kTimeoutNs)) { ok = false; break; }
+    if (!mbar_wait(bar_addr(kv_ready[st]), ph, abort, kTimeoutNs)) { ok = false; break; }
     if (sc.first()) {
-      if (!mbar_wait(bar_addr(m.q_full), q_it & 1, abort, kTimeoutNs)) { ok = false; break; }
+      if (!mbar_wait(bar_addr(q_ready), q_it & 1, abort, kTimeoutNs)) { ok = false; break; }
       ++q_it;
     }
     if (!mbar_wait(bar_addr(m.s_free[st]), ph ^ 1, abort, kTimeoutNs)) { ok = false; break; }
@@ -258,12 +298,13 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
 
 // O^T(chunk c) (+)= V^T(tile) P^T over ceil(nv/16) steps of 16 tokens; issuer
 // `half` takes value chunks 2 half and 2 half + 1.
+template <bool F8>
 __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
                           uint32_t tmem, int half, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
-  const uint32_t idesc_o = idesc_bf16_f32(128, tp.npv, true, false);
+  const uint32_t idesc_o = idesc_f32acc(128, tp.npv, true, false, !F8);
   const uint64_t dv0 = smem_desc_sw128(sKv, 1024, kAtomBytes);           // V^T, MN-major
   const uint64_t dp0 = smem_desc_sw128(sKv + kPOff, 16, kAtomBytes);     // P, K-major
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
@@ -308,6 +349,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
 
 // ------------------------------------------------------------------ softmax + epilogue
 
+template <bool F8>
 __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
                            unsigned char *smem, uint32_t tmem, int *err) {
   using namespace tc;
@@ -321,7 +363,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
   const int row[2] = {16 * q + (lane >> 2), 16 * q + (lane >> 2) + 8};
   const int pair = 2 * (lane & 3);
   const uint32_t tq = tmem + (uint32_t(32 * q) << 16);
-  const float cs = p.score_scale_log2 * p.kv_scale;
+  float cs = p.score_scale_log2 * p.kv_scale;
   uint32_t kv_it = 0, p_it = 0, o_it = 0;
   bool ok = true;
 
@@ -337,6 +379,11 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
       // Every wait of the warpgroup is followed by a group vote, so that a
       // wait that gave up in one warp never strands the others at a barrier.
       bool got = __all_sync(0xffffffffu, mbar_wait(bar_addr(m.s_full[s]), ph, abort, kTimeoutNs));
+      if (F8 && got) {
+        // the converter's scale of this tile (Q's power of two folded in)
+        got = __all_sync(0xffffffffu, mbar_wait(bar_addr(m.kv_conv[s]), ph, abort, kTimeoutNs));
+        cs = m.tscale[s];
+      }
       float x[32];  // unscaled scores: x[4j + 2h + e] = head row[h], token 8j + pair + e
       if (got) {
         tc_fence_after();
@@ -408,8 +455,9 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
           tmem_wait_st();
         }
       }
-      // P = 2^(s cs - m) in bf16, row-major [head][token] in the swizzled
-      // K-major layout: each lane writes 4-byte token pairs
+      // P = 2^(s cs - m) in bf16 (f16 for e4m3 caches), row-major
+      // [head][token] in the swizzled K-major layout: each lane writes 4-byte
+      // token pairs; the sum takes the rounded values the MMA will read
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         unsigned char *prow = smem + kOffKv + s * kStageBytes + (row[h] >> 3) * kAtomBytes + kPOff +
@@ -417,12 +465,21 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
         float lsum = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          __nv_bfloat162 b2 =
-              __floats2bfloat162_rn(exp2f(fmaf(x[4 * j + 2 * h], cs, -mnew[h])),
-                                    exp2f(fmaf(x[4 * j + 2 * h + 1], cs, -mnew[h])));
-          const float2 back = __bfloat1622float2(b2);
+          const float e0 = exp2f(fmaf(x[4 * j + 2 * h], cs, -mnew[h]));
+          const float e1 = exp2f(fmaf(x[4 * j + 2 * h + 1], cs, -mnew[h]));
+          float2 back;
+          uint32_t bits;
+          if (F8) {
+            __half2 v = __floats2half2_rn(e0, e1);
+            back = __half22float2(v);
+            bits = *reinterpret_cast<uint32_t *>(&v);
+          } else {
+            __nv_bfloat162 v = __floats2bfloat162_rn(e0, e1);
+            back = __bfloat1622float2(v);
+            bits = *reinterpret_cast<uint32_t *>(&v);
+          }
           lsum += back.x + back.y;
-          *reinterpret_cast<__nv_bfloat162 *>(prow + ((j ^ (row[h] & 7)) << 4)) = b2;
+          *reinterpret_cast<uint32_t *>(prow + ((j ^ (row[h] & 7)) << 4)) = bits;
         }
         ellp[h] = ellp[h] * alpha[h] + lsum;
         mrun[h] = mnew[h];
@@ -508,9 +565,138 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
   if (!ok) atomicOr(err, kErrTimeout);
 }
 
+// ------------------------------------------------------------------ e4m3 converter
+//
+// Warps 9..11.  Q (bf16, as landed by TMA) becomes f16 scaled by 2^k, k chosen
+// from the largest |q| of the request so that it lies in [2^14, 2^15): every
+// bf16 value down to 2^-31 of that maximum is exact in f16 and nothing
+// overflows; the scores then carry 2^-k.  Each 16-byte chunk of fp8 values
+// (one row, 16 consecutive dims) becomes two 16-byte f16 chunks of the
+// swizzled [atom][dim block][8 rows][128 B] layout.
+
+// bf16 pair -> f16 pair, both scaled by the power of two `sc` (exact unless
+// the scaled value leaves f16's range, which the choice of k rules out).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc) {
+  const float lo = __uint_as_float(w << 16) * sc;
+  const float hi = __uint_as_float(w & 0xffff0000u) * sc;
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Dims 16 ch .. 16 ch + 15 of `row`: 16 e4m3 values -> two f16 chunks.
+__device__ __forceinline__ void expand_fp8_chunk(unsigned char *stage, int row, int ch, uint4 w) {
+  using namespace tc;
+  uint4 lo, hi;
+  lo.x = e4m3x2_to_f16x2(uint16_t(w.x));
+  lo.y = e4m3x2_to_f16x2(uint16_t(w.x >> 16));
+  lo.z = e4m3x2_to_f16x2(uint16_t(w.y));
+  lo.w = e4m3x2_to_f16x2(uint16_t(w.y >> 16));
+  hi.x = e4m3x2_to_f16x2(uint16_t(w.z));
+  hi.y = e4m3x2_to_f16x2(uint16_t(w.z >> 16));
+  hi.z = e4m3x2_to_f16x2(uint16_t(w.w));
+  hi.w = e4m3x2_to_f16x2(uint16_t(w.w >> 16));
+  const int kb = ch >> 2, j = (ch & 3) * 2, sw = row & 7;
+  unsigned char *line = stage + (row >> 3) * kAtomBytes + kb * 1024 + sw * 128;
+  *reinterpret_cast<uint4 *>(line + ((j ^ sw) << 4)) = lo;
+  *reinterpret_cast<uint4 *>(line + (((j + 1) ^ sw) << 4)) = hi;
+}
+
+__device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r, TcMisc &m,
+                                           unsigned char *smem, int *err) {
+  using namespace tc;
+  const DecodeParams &p = tp.p;
+  volatile int *abort = &m.abort;
+  const int ct = int(threadIdx.x) - kConvWarp0 * 32;  // 0 .. 95
+  const int cw = ct >> 5, lane = ct & 31;
+  constexpr int kPerPhase = 32 * kRawChunks / kConvThreads;  // 12 chunks per thread per 32 rows
+  static_assert(32 * kRawChunks % kConvThreads == 0, "converter split");
+  uint32_t kv_it = 0, q_it = 0;
+  float qinv = 1.f;
+  bool ok = true;
+  for (TileCursor c(p, r); c.live; c.step(), ++kv_it) {
+    if (c.first()) {
+      const bool got = mbar_wait(bar_addr(m.q_full), q_it & 1, abort, kTimeoutNs);
+      if (!named_sync_and(3, kConvThreads, got)) { ok = false; break; }
+      uint4 *qv = reinterpret_cast<uint4 *>(smem + kOffQ);  // [kb][64 rows][8 chunks]
+      uint32_t mx = 0;
+      for (int i = ct; i < kQBytes / 16; i += kConvThreads) {
+        if (((i >> 3) & 63) >= tp.q_rows) continue;
+        const uint4 w = qv[i];
+        mx = __vmaxu2(mx, w.x & 0x7fff7fffu);
+        mx = __vmaxu2(mx, w.y & 0x7fff7fffu);
+        mx = __vmaxu2(mx, w.z & 0x7fff7fffu);
+        mx = __vmaxu2(mx, w.w & 0x7fff7fffu);
+      }
+      mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
+      if (lane == 0) m.conv_max[cw] = mx;
+      named_sync(3, kConvThreads);
+      mx = max(m.conv_max[0], max(m.conv_max[1], m.conv_max[2]));
+      // |q| bits are ordered like magnitudes; an Inf or NaN keeps k = 0
+      int k = 0;
+      if (mx < 0x7f80u) k = min(126, max(-126, 14 - (int(mx >> 7) - 127)));
+      const float sc = __int_as_float((127 + k) << 23);
+      qinv = __int_as_float((127 - k) << 23);
+      for (int i = ct; i < kQBytes / 16; i += kConvThreads) {
+        if (((i >> 3) & 63) >= tp.q_rows) continue;
+        uint4 w = qv[i];
+        w.x = bf16x2_to_f16x2_scaled(w.x, sc);
+        w.y = bf16x2_to_f16x2_scaled(w.y, sc);
+        w.z = bf16x2_to_f16x2_scaled(w.z, sc);
+        w.w = bf16x2_to_f16x2_scaled(w.w, sc);
+        qv[i] = w;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(m.q_ready));
+      ++q_it;
+    }
+    const int s = kv_it & 1;
+    const bool got = mbar_wait(bar_addr(m.kv_full[s]), (kv_it >> 1) & 1, abort, kTimeoutNs);
+    if (!named_sync_and(3, kConvThreads, got)) { ok = false; break; }
+    unsigned char *stage = smem + kOffKv + s * kStageBytes;
+    const unsigned char *raw = stage + kRawOff;
+    // Rows past the request's end stay unconverted: their scores are masked
+    // and the softmax zeroes the value rows the last PV step reads.
+    const int nv = c.nv();
+    // rows 0..31 land in atoms 0..3, below the raw rows
+#pragma unroll 4
+    for (int u = 0; u < kPerPhase; ++u) {
+      const int i = ct + u * kConvThreads, row = i / kRawChunks, ch = i - row * kRawChunks;
+      if (row < nv)
+        expand_fp8_chunk(stage, row, ch,
+                         *reinterpret_cast<const uint4 *>(raw + row * kRawRow + ch * 16));
+    }
+    if (nv > 32) {
+      // atoms 4, 5 overwrite raw rows 0..31 (consumed above); atoms 6, 7 the
+      // raw rows 32..63 themselves: read them all, then write
+      named_sync(3, kConvThreads);
+      uint4 w[kPerPhase];
+#pragma unroll
+      for (int u = 0; u < kPerPhase; ++u) {
+        const int i = ct + u * kConvThreads, row = 32 + i / kRawChunks;
+        const int ch = i - (row - 32) * kRawChunks;
+        if (row < nv) w[u] = *reinterpret_cast<const uint4 *>(raw + row * kRawRow + ch * 16);
+      }
+      named_sync(3, kConvThreads);
+#pragma unroll
+      for (int u = 0; u < kPerPhase; ++u) {
+        const int i = ct + u * kConvThreads, row = 32 + i / kRawChunks;
+        const int ch = i - (row - 32) * kRawChunks;
+        if (row < nv) expand_fp8_chunk(stage, row, ch, w[u]);
+      }
+    }
+    if (ct == 0) m.tscale[s] = p.score_scale_log2 * p.kv_scale * qinv;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_addr(m.kv_conv[s]));
+  }
+  if (!ok) atomicOr(err, kErrTimeout);
+}
+
 // ------------------------------------------------------------------ kernel
 
-__global__ void __launch_bounds__(tc::kThreads, 1)
+template <bool F8>
+__global__ void __launch_bounds__(tc_threads<F8>(), 1)
     decode_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_kv) {
   using namespace tc;
@@ -526,7 +712,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
   // Q rows past the request's heads are read by the MMAs but never loaded:
   // they must hold finite values.  (P rows past them are written each tile.)
-  for (int i = tid; i < kQBytes / 16; i += kThreads)
+  for (int i = tid; i < kQBytes / 16; i += tc_threads<F8>())
     reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -545,6 +731,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     mbar_init(bar_addr(m.o_full), 2);
     mbar_init(bar_addr(m.o_free), 4);
     mbar_init(bar_addr(m.drain), 4);       // all four MMA issuers
+    mbar_init(bar_addr(m.kv_conv[0]), 3);  // one arrival per converter warp
+    mbar_init(bar_addr(m.kv_conv[1]), 3);
+    mbar_init(bar_addr(m.q_ready), 3);
     m.abort = 0;
     fence_barrier_init();
   }
@@ -568,13 +757,15 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   if (r.start < r.end) {
     if (warp == 0) {
       if (lane == 0)
-        tc_producer(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
+        tc_producer<F8>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
     } else if (warp == 1 || warp == 2) {
-      if (lane == 0) tc_mma_s(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
+      if (lane == 0) tc_mma_s<F8>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
     } else if (warp == 3 || warp == 8) {
-      if (lane == 0) tc_mma_pv(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
-    } else {
-      tc_softmax(tp, r, m, smem, tmem, err);
+      if (lane == 0) tc_mma_pv<F8>(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
+    } else if (warp < 8) {
+      tc_softmax<F8>(tp, r, m, smem, tmem, err);
+    } else if (F8) {
+      tc_convert(tp, r, m, smem, err);
     }
   }
   tc_fence_before();
@@ -592,22 +783,26 @@ cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t str
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
                              const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
                              cudaStream_t stream) {
-  static int configured[64] = {0};
+  static int configured[64][2] = {};
+  const bool f8 = p.kv_e4m3 != 0;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
+  if (dev >= 0 && dev < 64 && !configured[dev][f8]) {
+    cudaError_t e = cudaFuncSetAttribute(f8 ? decode_tc_kernel<true> : decode_tc_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          tc::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev] = 1;
+    configured[dev][f8] = 1;
   }
   TcParams tp;
   tp.p = p;
   tp.npv = npv;
   tp.q_rows = q_rows;
   tp.groups_per_page = groups_per_page;
-  decode_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
+  if (f8)
+    decode_tc_kernel<true><<<grid, tc::kThreadsF8, tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
+  else
+    decode_tc_kernel<false><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? launch_split_merge(p, grid, stream) : e;
 }

@@ -113,6 +113,13 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint
 }
 
 // Bring a 4-D box of a tensor into L2 without shared memory (a hint).
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_4d(const void *tmap, int c0, int c1, int c2, int c3) {
   asm volatile(
       "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
@@ -137,11 +144,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: operand stored MN-major (else K-major).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4)                      // D = f32
-         | (1u << 7) | (1u << 10)       // A = B = bf16
+// kind::f16 instruction descriptor with an f32 accumulator; A and B are both
+// bf16 (format 1) or both f16 (format 0).
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn, bool b_mn, bool bf16) {
+  return (1u << 4)                                          // D = f32
+         | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10)  // A, B format
          | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_f32acc(M, N, a_mn, b_mn, true);
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

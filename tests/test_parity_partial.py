@@ -71,6 +71,9 @@ SHAPES = [
     (64, [1500, 33, 0, 640], 4, "e4m3"),
     (128, [900, 1, 65], 1, "e4m3"),
     (16, [300, 17], 5, "e4m3"),
+    (16, [1, 3, 5, 7, 511, 1025], 8, "e4m3"),
+    (128, [2000, 97, 40, 0], 2, "e4m3"),
+    (48, [64, 96, 31, 2049], 1, "e4m3"),
 ]
 
 
@@ -221,3 +224,17 @@ def test_growing_scores_take_the_rescale_path(num_parts):
             kv[int(bt[b, i]), :, 512:] *= 1.0 + 1.5 * i
     case.kv_pages = kv.to(torch.bfloat16)
     _check_all(case)
+
+
+@pytest.mark.parametrize("num_parts", [1, 4])
+@pytest.mark.parametrize("q_shift", [16, -24])
+def test_fp8_query_far_outside_f16_range(q_shift, num_parts):
+    """An e4m3 cache runs its MMAs on f16 operands: Q is rescaled by a power of
+    two first, so a query of magnitude 2^16 (past f16's maximum) or 2^-24 (in
+    its subnormals) gives the same attention as the unscaled one; sm_scale
+    carries the opposite power so that the scores are ordinary."""
+    case = workloads.make_decode_case("fp8_qshift", 64, [700, 65, 1300], seed=30 + q_shift,
+                                      device="cuda", kv_dtype="e4m3", num_parts=num_parts)
+    case.q = (case.q.float() * 2.0 ** q_shift).to(torch.bfloat16)
+    case.sm_scale = case.sm_scale * 2.0 ** -q_shift
+    _check_all(case, bases=(0,), atol=FP8_ATOL)
