@@ -570,8 +570,8 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
 // Warps 9..11.  Q (bf16, as landed by TMA) becomes f16 scaled by 2^k, k chosen
 // from the largest |q| of the request so that it lies in [2^14, 2^15): every
 // bf16 value down to 2^-31 of that maximum is exact in f16 and nothing
-// overflows; the scores then carry 2^-k.  Each 16-byte chunk of fp8 values
-// (one row, 16 consecutive dims) becomes two 16-byte f16 chunks of the
+// overflows; the scores then carry 2^-k.  Each 8-byte chunk of fp8 values
+// (one row, 8 consecutive dims) becomes one 16-byte f16 chunk of the
 // swizzled [atom][dim block][8 rows][128 B] layout.
 
 // bf16 pair -> f16 pair, both scaled by the power of two `sc` (exact unless
@@ -583,22 +583,14 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc)
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Dims 16 ch .. 16 ch + 15 of `row`: 16 e4m3 values -> two f16 chunks.
-__device__ __forceinline__ void expand_fp8_chunk(unsigned char *stage, int row, int ch, uint4 w) {
-  using namespace tc;
-  uint4 lo, hi;
-  lo.x = e4m3x2_to_f16x2(uint16_t(w.x));
-  lo.y = e4m3x2_to_f16x2(uint16_t(w.x >> 16));
-  lo.z = e4m3x2_to_f16x2(uint16_t(w.y));
-  lo.w = e4m3x2_to_f16x2(uint16_t(w.y >> 16));
-  hi.x = e4m3x2_to_f16x2(uint16_t(w.z));
-  hi.y = e4m3x2_to_f16x2(uint16_t(w.z >> 16));
-  hi.z = e4m3x2_to_f16x2(uint16_t(w.w));
-  hi.w = e4m3x2_to_f16x2(uint16_t(w.w >> 16));
-  const int kb = ch >> 2, j = (ch & 3) * 2, sw = row & 7;
-  unsigned char *line = stage + (row >> 3) * kAtomBytes + kb * 1024 + sw * 128;
-  *reinterpret_cast<uint4 *>(line + ((j ^ sw) << 4)) = lo;
-  *reinterpret_cast<uint4 *>(line + (((j + 1) ^ sw) << 4)) = hi;
+// 8 e4m3 values -> one 16-byte f16 chunk at `dst`.
+__device__ __forceinline__ void expand_fp8_store(unsigned char *dst, uint2 w) {
+  uint4 o;
+  o.x = e4m3x2_to_f16x2(uint16_t(w.x));
+  o.y = e4m3x2_to_f16x2(uint16_t(w.x >> 16));
+  o.z = e4m3x2_to_f16x2(uint16_t(w.y));
+  o.w = e4m3x2_to_f16x2(uint16_t(w.y >> 16));
+  *reinterpret_cast<uint4 *>(dst) = o;
 }
 
 __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r, TcMisc &m,
@@ -608,8 +600,17 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
   volatile int *abort = &m.abort;
   const int ct = int(threadIdx.x) - kConvWarp0 * 32;  // 0 .. 95
   const int cw = ct >> 5, lane = ct & 31;
-  constexpr int kPerPhase = 32 * kRawChunks / kConvThreads;  // 12 chunks per thread per 32 rows
-  static_assert(32 * kRawChunks % kConvThreads == 0, "converter split");
+  // Thread (tr, tc) = (ct / 24, ct % 24) converts, of rows 4k + tr, the 8-value
+  // chunks tc, tc + 24 and tc + 48: chunk c lands in dim block c / 8 at
+  // swizzled position (c % 8) ^ (row % 8), so the three chunks sit 3 blocks
+  // (3072 B) apart, and row 4k + tr has row % 8 = tr + 4 (k % 2), atom k / 2.
+  const int tr = ct / 24, tc = ct - 24 * (ct / 24);
+  const int src0 = tr * kRawRow + tc * 8;
+  const int dst0 = (tc >> 3) * 1024 + tr * 128 + (((tc & 7) ^ tr) << 4);
+  const int dst1 = (tc >> 3) * 1024 + (tr + 4) * 128 + (((tc & 7) ^ (tr + 4)) << 4);
+  constexpr int kQPer = kQBytes / 16 / kConvThreads;         // 48 uint4 of Q per thread
+  static_assert(kConvThreads == 4 * 24 && kRawRow == 72 * 8, "converter split");
+  static_assert(kQBytes / 16 % kConvThreads == 0 && kQPer % 8 == 0, "Q split");
   uint32_t kv_it = 0, q_it = 0;
   float qinv = 1.f;
   bool ok = true;
@@ -618,9 +619,15 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
       const bool got = mbar_wait(bar_addr(m.q_full), q_it & 1, abort, kTimeoutNs);
       if (!named_sync_and(3, kConvThreads, got)) { ok = false; break; }
       uint4 *qv = reinterpret_cast<uint4 *>(smem + kOffQ);  // [kb][64 rows][8 chunks]
+      // the maximum over this request's heads; rows past them (zeros, or the
+      // next request's heads that the box also covers) only feed score rows
+      // the epilogue drops
+      const int hn = min(kHeads, p.heads - c.w.g * kHeads);
       uint32_t mx = 0;
-      for (int i = ct; i < kQBytes / 16; i += kConvThreads) {
-        if (((i >> 3) & 63) >= tp.q_rows) continue;
+#pragma unroll 8
+      for (int u = 0; u < kQPer; ++u) {
+        const int i = ct + u * kConvThreads;
+        if (((i >> 3) & 63) >= hn) continue;
         const uint4 w = qv[i];
         mx = __vmaxu2(mx, w.x & 0x7fff7fffu);
         mx = __vmaxu2(mx, w.y & 0x7fff7fffu);
@@ -636,14 +643,14 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
       if (mx < 0x7f80u) k = min(126, max(-126, 14 - (int(mx >> 7) - 127)));
       const float sc = __int_as_float((127 + k) << 23);
       qinv = __int_as_float((127 - k) << 23);
-      for (int i = ct; i < kQBytes / 16; i += kConvThreads) {
-        if (((i >> 3) & 63) >= tp.q_rows) continue;
-        uint4 w = qv[i];
+#pragma unroll 8
+      for (int u = 0; u < kQPer; ++u) {
+        uint4 w = qv[ct + u * kConvThreads];
         w.x = bf16x2_to_f16x2_scaled(w.x, sc);
         w.y = bf16x2_to_f16x2_scaled(w.y, sc);
         w.z = bf16x2_to_f16x2_scaled(w.z, sc);
         w.w = bf16x2_to_f16x2_scaled(w.w, sc);
-        qv[i] = w;
+        qv[ct + u * kConvThreads] = w;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -657,32 +664,47 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
     const unsigned char *raw = stage + kRawOff;
     // Rows past the request's end stay unconverted: their scores are masked
     // and the softmax zeroes the value rows the last PV step reads.
+    //
+    // Destination atom a (rows 8a .. 8a + 7) covers raw rows 16 (a - 4) ..
+    // 16 (a - 4) + 15 for a >= 4, so the rows go in four groups: 0..31 (below
+    // the raw rows), 32..47 (over raw rows 0..31), 48..55 (over 32..47), and
+    // 56..63, which overlaps its own raw rows: read first, written last.
     const int nv = c.nv();
-    // rows 0..31 land in atoms 0..3, below the raw rows
-#pragma unroll 4
-    for (int u = 0; u < kPerPhase; ++u) {
-      const int i = ct + u * kConvThreads, row = i / kRawChunks, ch = i - row * kRawChunks;
-      if (row < nv)
-        expand_fp8_chunk(stage, row, ch,
-                         *reinterpret_cast<const uint4 *>(raw + row * kRawRow + ch * 16));
-    }
+    uint2 w[4][3];
+    // steps k0 .. k0 + n - 1: loads, then conversions and stores
+    auto load = [&](int k0, int n) {
+#pragma unroll
+      for (int k = 0; k < n; ++k)
+        if (4 * (k0 + k) + tr < nv)
+#pragma unroll
+          for (int e = 0; e < 3; ++e)
+            w[k][e] = *reinterpret_cast<const uint2 *>(raw + src0 + (k0 + k) * 4 * kRawRow + e * 192);
+    };
+    auto store = [&](int k0, int n) {
+#pragma unroll
+      for (int k = 0; k < n; ++k)
+        if (4 * (k0 + k) + tr < nv)
+#pragma unroll
+          for (int e = 0; e < 3; ++e)
+            expand_fp8_store(stage + ((k0 + k) >> 1) * kAtomBytes + (((k0 + k) & 1) ? dst1 : dst0) +
+                                 e * 3072,
+                             w[k][e]);
+    };
+    load(0, 4); store(0, 4);
+    load(4, 4); store(4, 4);
     if (nv > 32) {
-      // atoms 4, 5 overwrite raw rows 0..31 (consumed above); atoms 6, 7 the
-      // raw rows 32..63 themselves: read them all, then write
       named_sync(3, kConvThreads);
-      uint4 w[kPerPhase];
+      load(8, 4); store(8, 4);
+      if (nv > 48) {
+        named_sync(3, kConvThreads);
+        load(12, 4);            // rows 48..63
+        store(12, 2);           // rows 48..55 over raw rows 32..47
+        if (nv > 56) {
+          named_sync(3, kConvThreads);
 #pragma unroll
-      for (int u = 0; u < kPerPhase; ++u) {
-        const int i = ct + u * kConvThreads, row = 32 + i / kRawChunks;
-        const int ch = i - (row - 32) * kRawChunks;
-        if (row < nv) w[u] = *reinterpret_cast<const uint4 *>(raw + row * kRawRow + ch * 16);
-      }
-      named_sync(3, kConvThreads);
-#pragma unroll
-      for (int u = 0; u < kPerPhase; ++u) {
-        const int i = ct + u * kConvThreads, row = 32 + i / kRawChunks;
-        const int ch = i - (row - 32) * kRawChunks;
-        if (row < nv) expand_fp8_chunk(stage, row, ch, w[u]);
+          for (int k = 0; k < 2; ++k) w[k][0] = w[k + 2][0], w[k][1] = w[k + 2][1], w[k][2] = w[k + 2][2];
+          store(14, 2);
+        }
       }
     }
     if (ct == 0) m.tscale[s] = p.score_scale_log2 * p.kv_scale * qinv;

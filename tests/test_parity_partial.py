@@ -74,6 +74,8 @@ SHAPES = [
     (16, [1, 3, 5, 7, 511, 1025], 8, "e4m3"),
     (128, [2000, 97, 40, 0], 2, "e4m3"),
     (48, [64, 96, 31, 2049], 1, "e4m3"),
+    (80, [300, 900, 1], 2, "e4m3"),
+    (80, [700, 5], 1, "bf16"),
 ]
 
 
