@@ -89,6 +89,7 @@ struct TcMisc {
   float alpha[2][64];
   float ell[64];
   float tscale[2];               // e4m3 only: score scale (base 2) of the tile in each stage
+  uint32_t vote[2][4];           // softmax: per-warp flags of the tile, by tile parity
   uint32_t conv_max[4];
   CtaRange range;
   long long scratch[tc::kThreadsF8 / 32 + 1];
@@ -349,6 +350,36 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
 
 // ------------------------------------------------------------------ softmax + epilogue
 
+// Packed fp32 pair arithmetic (one instruction per pair on sm_100 parts).
+__device__ __forceinline__ unsigned long long f2_bits(float2 a) {
+  return *reinterpret_cast<unsigned long long *>(&a);
+}
+__device__ __forceinline__ float2 bits_f2(unsigned long long b) {
+  return *reinterpret_cast<float2 *>(&b);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// 2^x by the hardware approximation (relative error far below the bf16 / f16
+// rounding that follows); results below 2^-126 flush to zero.
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 template <bool F8>
 __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
                            unsigned char *smem, uint32_t tmem, int *err) {
@@ -384,7 +415,9 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
         got = __all_sync(0xffffffffu, mbar_wait(bar_addr(m.kv_conv[s]), ph, abort, kTimeoutNs));
         cs = m.tscale[s];
       }
-      float x[32];  // unscaled scores: x[4j + 2h + e] = head row[h], token 8j + pair + e
+      // unscaled scores in token pairs: xp[2j + h] = head row[h], tokens
+      // 8j + pair + {0, 1}
+      float2 xp[16];
       if (got) {
         tc_fence_after();
         uint32_t ra[32], rb[32];
@@ -392,24 +425,33 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
         tmem_ld16x256b_x8(tq + kColS + 64 * (2 * s + 1), rb);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(ra[i]) + __uint_as_float(rb[i]);
+        for (int k = 0; k < 16; ++k)
+          xp[k] = add2(make_float2(__uint_as_float(ra[2 * k]), __uint_as_float(ra[2 * k + 1])),
+                       make_float2(__uint_as_float(rb[2 * k]), __uint_as_float(rb[2 * k + 1])));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_addr(m.s_free[s]));
       }
       if (nv < kTile) {  // the tile's tail: tokens past the request's end
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            x[4 * j + i] = (8 * j + pair + (i & 1)) < nv ? x[4 * j + i] : -INFINITY;
+        for (int k = 0; k < 16; ++k) {
+          const int tok = 8 * (k >> 1) + pair;
+          xp[k].x = tok < nv ? xp[k].x : -INFINITY;
+          xp[k].y = tok + 1 < nv ? xp[k].y : -INFINITY;
+        }
       }
-      float tmax[2] = {-INFINITY, -INFINITY};
+      float tmax[2];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          tmax[h] = fmaxf(tmax[h], fmaxf(x[4 * j + 2 * h], x[4 * j + 2 * h + 1]));
+      for (int h = 0; h < 2; ++h) {
+        float mx = max3(xp[h].x, xp[h].y, xp[2 + h].x);
+        mx = max3(mx, xp[2 + h].y, xp[4 + h].x);
+        mx = max3(mx, xp[4 + h].y, xp[6 + h].x);
+        mx = max3(mx, xp[6 + h].y, xp[8 + h].x);
+        mx = max3(mx, xp[8 + h].y, xp[10 + h].x);
+        mx = max3(mx, xp[10 + h].y, xp[12 + h].x);
+        mx = max3(mx, xp[12 + h].y, xp[14 + h].x);
+        tmax[h] = fmaxf(mx, xp[14 + h].y);
+      }
       float mnew[2], alpha[2];
       bool resc = false;
 #pragma unroll
@@ -431,29 +473,36 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
         m.alpha[p_it & 1][row[0]] = alpha[0];
         m.alpha[p_it & 1][row[1]] = alpha[1];
       }
-      // one group barrier in the common case; more only when some lane needs
-      // an O rescale or a wait gave up.  Every branch below follows a group
-      // result, so all 128 lanes take it together.
-      if (named_sync_or(1, 128, resc || !got)) {
-        if (!named_sync_and(1, 128, got)) { ok = false; break; }
-        if (named_sync_or(1, 128, resc)) {
-          // rescaling O^T needs the previous tile's PV to have finished
-          const bool pv_done = mbar_wait(bar_addr(m.p_free), (p_it - 1) & 1, abort, kTimeoutNs);
-          if (!named_sync_and(1, 128, pv_done)) { ok = false; break; }
-          tc_fence_after();
-          const float *al = m.alpha[p_it & 1];
-          for (int c = 0; c < 4; ++c)
-            for (int hb = 0; hb < tp.npv / 16; ++hb) {
-              uint32_t o[16];
-              tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
-              tmem_wait_ld();
+      // One plain group barrier per tile: each warp posts whether one of its
+      // heads needs an O rescale (bit 0) or a wait gave up (bit 1), and every
+      // branch below follows the OR of the four, so all 128 lanes take it
+      // together.  (Flags are double-buffered by tile parity: a warp cannot
+      // rewrite a buffer before every warp has passed the next barrier.)
+      {
+        const uint32_t flag = (__any_sync(0xffffffffu, resc) ? 1u : 0u) | (got ? 0u : 2u);
+        if (lane == 0) m.vote[p_it & 1][q] = flag;
+      }
+      named_sync(1, 128);
+      const uint32_t vote = m.vote[p_it & 1][0] | m.vote[p_it & 1][1] | m.vote[p_it & 1][2] |
+                            m.vote[p_it & 1][3];
+      if (vote & 2u) { ok = false; break; }
+      if (vote & 1u) {
+        // rescaling O^T needs the previous tile's PV to have finished
+        const bool pv_done = mbar_wait(bar_addr(m.p_free), (p_it - 1) & 1, abort, kTimeoutNs);
+        if (!named_sync_and(1, 128, pv_done)) { ok = false; break; }
+        tc_fence_after();
+        const float *al = m.alpha[p_it & 1];
+        for (int c = 0; c < 4; ++c)
+          for (int hb = 0; hb < tp.npv / 16; ++hb) {
+            uint32_t o[16];
+            tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                o[i] = __float_as_uint(__uint_as_float(o[i]) * al[16 * hb + i]);
-              tmem_st16(tq + kColO + 64 * c + 16 * hb, o);
-            }
-          tmem_wait_st();
-        }
+            for (int i = 0; i < 16; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * al[16 * hb + i]);
+            tmem_st16(tq + kColO + 64 * c + 16 * hb, o);
+          }
+        tmem_wait_st();
       }
       // P = 2^(s cs - m) in bf16 (f16 for e4m3 caches), row-major
       // [head][token] in the swizzled K-major layout: each lane writes 4-byte
@@ -462,11 +511,12 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
       for (int h = 0; h < 2; ++h) {
         unsigned char *prow = smem + kOffKv + s * kStageBytes + (row[h] >> 3) * kAtomBytes + kPOff +
                               (row[h] & 7) * 128 + (lane & 3) * 4;
-        float lsum = 0.f;
+        const float2 c2 = make_float2(cs, cs), m2 = make_float2(-mnew[h], -mnew[h]);
+        float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float e0 = exp2f(fmaf(x[4 * j + 2 * h], cs, -mnew[h]));
-          const float e1 = exp2f(fmaf(x[4 * j + 2 * h + 1], cs, -mnew[h]));
+          const float2 arg = fma2(xp[2 * j + h], c2, m2);
+          const float e0 = ex2(arg.x), e1 = ex2(arg.y);
           float2 back;
           uint32_t bits;
           if (F8) {
@@ -475,13 +525,13 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
             bits = *reinterpret_cast<uint32_t *>(&v);
           } else {
             __nv_bfloat162 v = __floats2bfloat162_rn(e0, e1);
-            back = __bfloat1622float2(v);
             bits = *reinterpret_cast<uint32_t *>(&v);
+            back = make_float2(__uint_as_float(bits << 16), __uint_as_float(bits & 0xffff0000u));
           }
-          lsum += back.x + back.y;
+          lsum = add2(lsum, back);
           *reinterpret_cast<uint32_t *>(prow + ((j ^ (row[h] & 7)) << 4)) = bits;
         }
-        ellp[h] = ellp[h] * alpha[h] + lsum;
+        ellp[h] = ellp[h] * alpha[h] + (lsum.x + lsum.y);
         mrun[h] = mnew[h];
       }
       // rows [nv, roundup16(nv)) of V are read by the last PV step but hold no
