@@ -350,6 +350,23 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
 
 // ------------------------------------------------------------------ softmax + epilogue
 
+// O^T *= alpha per head (column), for this warp's 32 TMEM lanes.  Rare (a
+// head's running maximum grew by more than 2^8): kept out of line so that
+// the softmax loop's instruction stream stays short.
+__device__ __noinline__ void rescale_o(uint32_t tq, const float *al, int npv) {
+  using namespace tc;
+  for (int c = 0; c < 4; ++c)
+    for (int hb = 0; hb < npv / 16; ++hb) {
+      uint32_t o[16];
+      tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[16 * hb + i]);
+      tmem_st16(tq + kColO + 64 * c + 16 * hb, o);
+    }
+  tmem_wait_st();
+}
+
 // Packed fp32 pair arithmetic (one instruction per pair on sm_100 parts).
 __device__ __forceinline__ unsigned long long f2_bits(float2 a) {
   return *reinterpret_cast<unsigned long long *>(&a);
@@ -491,18 +508,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
         const bool pv_done = mbar_wait(bar_addr(m.p_free), (p_it - 1) & 1, abort, kTimeoutNs);
         if (!named_sync_and(1, 128, pv_done)) { ok = false; break; }
         tc_fence_after();
-        const float *al = m.alpha[p_it & 1];
-        for (int c = 0; c < 4; ++c)
-          for (int hb = 0; hb < tp.npv / 16; ++hb) {
-            uint32_t o[16];
-            tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              o[i] = __float_as_uint(__uint_as_float(o[i]) * al[16 * hb + i]);
-            tmem_st16(tq + kColO + 64 * c + 16 * hb, o);
-          }
-        tmem_wait_st();
+        rescale_o(tq, m.alpha[p_it & 1], tp.npv);
       }
       // P = 2^(s cs - m) in bf16 (f16 for e4m3 caches), row-major
       // [head][token] in the swizzled K-major layout: each lane writes 4-byte
