@@ -397,6 +397,18 @@ __device__ __forceinline__ float ex2(float x) {
   return r;
 }
 
+// Value rows [nv, roundup16(nv)) of a stage (the last tile of a request),
+// zeroed by the softmax warpgroup (rank gt): out of line, once per request.
+__device__ __noinline__ void zero_value_tail(unsigned char *stage, int nv, int gt) {
+  using namespace tc;
+  const int r0 = nv, nrow = ((nv + 15) & ~15) - nv;
+  for (int i = gt; i < nrow * 64; i += 128) {
+    const int rr = r0 + (i >> 6), kb = (i >> 3) & 7, ch = i & 7;
+    *reinterpret_cast<uint4 *>(stage + (rr >> 3) * kAtomBytes + kb * 1024 + (rr & 7) * 128 + ch * 16) =
+        make_uint4(0, 0, 0, 0);
+  }
+}
+
 template <bool F8>
 __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
                            unsigned char *smem, uint32_t tmem, int *err) {
@@ -542,15 +554,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
       }
       // rows [nv, roundup16(nv)) of V are read by the last PV step but hold no
       // owned token (stale or unowned data): zero their 512 value dims
-      if (nv & 15) {
-        unsigned char *stage = smem + kOffKv + s * kStageBytes;
-        const int r0 = nv, nrow = ((nv + 15) & ~15) - nv;
-        for (int i = gt; i < nrow * 64; i += 128) {
-          const int rr = r0 + (i >> 6), kb = (i >> 3) & 7, ch = i & 7;
-          *reinterpret_cast<uint4 *>(stage + (rr >> 3) * kAtomBytes + kb * 1024 + (rr & 7) * 128 +
-                                     ch * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
+      if (nv & 15) zero_value_tail(smem + kOffKv + s * kStageBytes, nv, gt);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -649,6 +653,59 @@ __device__ __forceinline__ void expand_fp8_store(unsigned char *dst, uint2 w) {
   *reinterpret_cast<uint4 *>(dst) = o;
 }
 
+// The request's Q (bf16, as landed) to f16 in place, scaled by 2^k; *qinv =
+// 2^-k.  Once per request piece: out of line.
+__device__ __noinline__ bool convert_q(const TcParams &tp, TcMisc &m, unsigned char *smem, int g,
+                                       uint32_t q_it, float *qinv) {
+  using namespace tc;
+  const DecodeParams &p = tp.p;
+  volatile int *abort = &m.abort;
+  const int ct = int(threadIdx.x) - kConvWarp0 * 32;
+  const int cw = ct >> 5, lane = ct & 31;
+  constexpr int kQPer = kQBytes / 16 / kConvThreads;  // 48 uint4 of Q per thread
+  static_assert(kQBytes / 16 % kConvThreads == 0 && kQPer % 8 == 0, "Q split");
+  const bool got = mbar_wait(bar_addr(m.q_full), q_it & 1, abort, kTimeoutNs);
+  if (!named_sync_and(3, kConvThreads, got)) return false;
+  uint4 *qv = reinterpret_cast<uint4 *>(smem + kOffQ);  // [kb][64 rows][8 chunks]
+  // the maximum over this request's heads; rows past them (zeros, or the
+  // next request's heads that the box also covers) only feed score rows
+  // the epilogue drops
+  const int hn = min(kHeads, p.heads - g * kHeads);
+  uint32_t mx = 0;
+#pragma unroll 8
+  for (int u = 0; u < kQPer; ++u) {
+    const int i = ct + u * kConvThreads;
+    if (((i >> 3) & 63) >= hn) continue;
+    const uint4 w = qv[i];
+    mx = __vmaxu2(mx, w.x & 0x7fff7fffu);
+    mx = __vmaxu2(mx, w.y & 0x7fff7fffu);
+    mx = __vmaxu2(mx, w.z & 0x7fff7fffu);
+    mx = __vmaxu2(mx, w.w & 0x7fff7fffu);
+  }
+  mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
+  if (lane == 0) m.conv_max[cw] = mx;
+  named_sync(3, kConvThreads);
+  mx = max(m.conv_max[0], max(m.conv_max[1], m.conv_max[2]));
+  // |q| bits are ordered like magnitudes; an Inf or NaN keeps k = 0
+  int k = 0;
+  if (mx < 0x7f80u) k = min(126, max(-126, 14 - (int(mx >> 7) - 127)));
+  const float sc = __int_as_float((127 + k) << 23);
+  *qinv = __int_as_float((127 - k) << 23);
+#pragma unroll 8
+  for (int u = 0; u < kQPer; ++u) {
+    uint4 w = qv[ct + u * kConvThreads];
+    w.x = bf16x2_to_f16x2_scaled(w.x, sc);
+    w.y = bf16x2_to_f16x2_scaled(w.y, sc);
+    w.z = bf16x2_to_f16x2_scaled(w.z, sc);
+    w.w = bf16x2_to_f16x2_scaled(w.w, sc);
+    qv[ct + u * kConvThreads] = w;
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_addr(m.q_ready));
+  return true;
+}
+
 __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r, TcMisc &m,
                                            unsigned char *smem, int *err) {
   using namespace tc;
@@ -664,53 +721,13 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
   const int src0 = tr * kRawRow + tc * 8;
   const int dst0 = (tc >> 3) * 1024 + tr * 128 + (((tc & 7) ^ tr) << 4);
   const int dst1 = (tc >> 3) * 1024 + (tr + 4) * 128 + (((tc & 7) ^ (tr + 4)) << 4);
-  constexpr int kQPer = kQBytes / 16 / kConvThreads;         // 48 uint4 of Q per thread
   static_assert(kConvThreads == 4 * 24 && kRawRow == 72 * 8, "converter split");
-  static_assert(kQBytes / 16 % kConvThreads == 0 && kQPer % 8 == 0, "Q split");
   uint32_t kv_it = 0, q_it = 0;
   float qinv = 1.f;
   bool ok = true;
   for (TileCursor c(p, r); c.live; c.step(), ++kv_it) {
     if (c.first()) {
-      const bool got = mbar_wait(bar_addr(m.q_full), q_it & 1, abort, kTimeoutNs);
-      if (!named_sync_and(3, kConvThreads, got)) { ok = false; break; }
-      uint4 *qv = reinterpret_cast<uint4 *>(smem + kOffQ);  // [kb][64 rows][8 chunks]
-      // the maximum over this request's heads; rows past them (zeros, or the
-      // next request's heads that the box also covers) only feed score rows
-      // the epilogue drops
-      const int hn = min(kHeads, p.heads - c.w.g * kHeads);
-      uint32_t mx = 0;
-#pragma unroll 8
-      for (int u = 0; u < kQPer; ++u) {
-        const int i = ct + u * kConvThreads;
-        if (((i >> 3) & 63) >= hn) continue;
-        const uint4 w = qv[i];
-        mx = __vmaxu2(mx, w.x & 0x7fff7fffu);
-        mx = __vmaxu2(mx, w.y & 0x7fff7fffu);
-        mx = __vmaxu2(mx, w.z & 0x7fff7fffu);
-        mx = __vmaxu2(mx, w.w & 0x7fff7fffu);
-      }
-      mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
-      if (lane == 0) m.conv_max[cw] = mx;
-      named_sync(3, kConvThreads);
-      mx = max(m.conv_max[0], max(m.conv_max[1], m.conv_max[2]));
-      // |q| bits are ordered like magnitudes; an Inf or NaN keeps k = 0
-      int k = 0;
-      if (mx < 0x7f80u) k = min(126, max(-126, 14 - (int(mx >> 7) - 127)));
-      const float sc = __int_as_float((127 + k) << 23);
-      qinv = __int_as_float((127 - k) << 23);
-#pragma unroll 8
-      for (int u = 0; u < kQPer; ++u) {
-        uint4 w = qv[ct + u * kConvThreads];
-        w.x = bf16x2_to_f16x2_scaled(w.x, sc);
-        w.y = bf16x2_to_f16x2_scaled(w.y, sc);
-        w.z = bf16x2_to_f16x2_scaled(w.z, sc);
-        w.w = bf16x2_to_f16x2_scaled(w.w, sc);
-        qv[ct + u * kConvThreads] = w;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(m.q_ready));
+      if (!convert_q(tp, m, smem, c.w.g, q_it, &qinv)) { ok = false; break; }
       ++q_it;
     }
     const int s = kv_it & 1;
