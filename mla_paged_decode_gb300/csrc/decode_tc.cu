@@ -90,6 +90,7 @@ struct TcMisc {
   float ell[64];
   float tscale[2];               // e4m3 only: score scale (base 2) of the tile in each stage
   uint32_t vote[2][4];           // softmax: per-warp flags of the tile, by tile parity
+  alignas(16) unsigned char stage_out[4][2048];  // epilogue: per-warp transpose buffer
   uint32_t conv_max[4];
   CtaRange range;
   long long scratch[tc::kThreadsF8 / 32 + 1];
@@ -580,30 +581,60 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
     const SplitInfo si = split_info(r, w.v, w.pv, w.tiles);
     const bool split = si.nsplits > 1;
     const size_t out_row0 = size_t(w.b) * p.heads + size_t(w.g) * kHeads;
+    // This warp owns value dims 128c + 32q .. + 31 of each chunk c (its TMEM
+    // lanes).  Values go through a 2 KB per-warp buffer, transposed to
+    // [head][dim], so that each lane stores 16-byte runs of dims: 8 (bf16)
+    // or 16 (fp32 slot) stores per chunk instead of 64.
+    unsigned char *stg = m.stage_out[q];
+#pragma unroll 1
     for (int c = 0; c < 4; ++c) {
-      // one value dimension (this thread's TMEM lane) x 64 heads of chunk c:
-      // four loads in flight, one wait
-      const int dv = 128 * c + 32 * q + lane;
       uint32_t o[4][16];
 #pragma unroll
       for (int hb = 0; hb < 4; ++hb) tmem_ld16(tq + kColO + 64 * c + 16 * hb, o[hb]);
       tmem_wait_ld();
+      const int d0 = 128 * c + 32 * q;
+      if (!split) {
 #pragma unroll
-      for (int hb = 0; hb < 4; ++hb) {
-        // the block's 16 output scales, read before its stores
-        float sc[16];
+        for (int half = 0; half < 2; ++half) {  // heads 32 half .. + 31
 #pragma unroll
-        for (int i = 0; i < 16; ++i) sc[i] = m.ell[16 * hb + i];
+          for (int hh = 0; hh < 2; ++hh) {
+            const int hb = 2 * half + hh;
+            float sc[16];  // the block's 16 output scales, read before its stores
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int h = 16 * hb + i;
-          if (h < hn) {
-            const float val = __uint_as_float(o[hb][i]) * sc[i];
-            if (!split)
-              p.out[(out_row0 + h) * kDv + dv] = __float2bfloat16_rn(val);
-            else
-              slot_out_ptr(p)[(size_t(si.slot) * kSlotHeads + h) * kDv + dv] = val;
+            for (int i = 0; i < 16; ++i) sc[i] = m.ell[16 * hb + i];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              reinterpret_cast<__nv_bfloat16 *>(stg)[(16 * hh + i) * 32 + lane] =
+                  __float2bfloat16_rn(__uint_as_float(o[hb][i]) * sc[i]);
           }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // 32 heads x 4 runs of 8 dims
+            const int k = lane + 32 * j, hl = k >> 2, part = k & 3, h = 32 * half + hl;
+            const uint4 v = *reinterpret_cast<const uint4 *>(stg + k * 16);
+            if (h < hn)
+              *reinterpret_cast<uint4 *>(p.out + (out_row0 + h) * kDv + d0 + part * 8) = v;
+          }
+          __syncwarp();
+        }
+      } else {
+        float *slot = slot_out_ptr(p) + size_t(si.slot) * kSlotHeads * kDv;
+#pragma unroll
+        for (int hb = 0; hb < 4; ++hb) {  // heads 16 hb .. + 15
+          float sc[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sc[i] = m.ell[16 * hb + i];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            reinterpret_cast<float *>(stg)[i * 32 + lane] = __uint_as_float(o[hb][i]) * sc[i];
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // 16 heads x 8 runs of 4 dims
+            const int k = lane + 32 * j, hl = k >> 3, part = k & 7, h = 16 * hb + hl;
+            const uint4 v = *reinterpret_cast<const uint4 *>(stg + k * 16);
+            if (h < hn) *reinterpret_cast<uint4 *>(slot + size_t(h) * kDv + d0 + part * 4) = v;
+          }
+          __syncwarp();
         }
       }
     }
