@@ -67,7 +67,6 @@ constexpr uint64_t kDrainNs = 200000000ull;
 constexpr float kRescaleThreshold = 8.f;     // base-2 units
 constexpr int kRawOff = kStageBytes / 2;     // e4m3: raw [64 rows][576 B] in the stage's upper half
 constexpr int kRawRow = kDqk;                // bytes of one fp8 row
-constexpr int kRawChunks = kRawRow / 16;     // 36 chunks of 16 values
 }  // namespace tc
 
 struct TcParams {
@@ -632,7 +631,8 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
           for (int j = 0; j < 4; ++j) {  // 16 heads x 8 runs of 4 dims
             const int k = lane + 32 * j, hl = k >> 3, part = k & 7, h = 16 * hb + hl;
             const uint4 v = *reinterpret_cast<const uint4 *>(stg + k * 16);
-            if (h < hn) *reinterpret_cast<uint4 *>(slot + size_t(h) * kDv + d0 + part * 4) = v;
+            // the merge reads it back after the rest of the KV stream
+            if (h < hn) st_global_keep_l2(slot + size_t(h) * kDv + d0 + part * 4, v);
           }
           __syncwarp();
         }
@@ -743,7 +743,7 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const int ct = int(threadIdx.x) - kConvWarp0 * 32;  // 0 .. 95
-  const int cw = ct >> 5, lane = ct & 31;
+  const int lane = ct & 31;
   // Thread (tr, tc) = (ct / 24, ct % 24) converts, of rows 4k + tr, the 8-value
   // chunks tc, tc + 24 and tc + 48: chunk c lands in dim block c / 8 at
   // swizzled position (c % 8) ^ (row % 8), so the three chunks sit 3 blocks

@@ -90,6 +90,19 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
   return true;
 }
 
+// ------------------------------------------------------------------ L2 policy
+
+// A 16-byte global store whose line L2 keeps ahead of normal-priority data
+// (evict_last): for small results that a later kernel reads back while a
+// large stream passes through L2 in between.
+__device__ __forceinline__ void st_global_keep_l2(void *dst, uint4 v) {
+  asm volatile(
+      "{ .reg .b64 pol; createpolicy.fractional.L2::evict_last.b64 pol, 1.0;\n"
+      "  st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, pol; }" ::"l"(dst),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
