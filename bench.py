@@ -311,12 +311,14 @@ def run_ours(args, world, rank, local):
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "frac_of_8tbs": achieved / 8000.0,
                      "traffic": traffic,
-                     "kernel": "mla_decode_partial (one launch per step)"},
+                     "kernel": "mla_decode_partial: decode kernel + split merge, timed "
+                               "together per call (CUDA events on the launching stream)"},
         "e2e": {"value": aggregate(e_ms_max, args.steps, B, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "q, block table and lengths copied from pinned host memory, out and "
                         "lse read back, every step; the KV cache stays resident in HBM"},
-        "gpu_launches": args.steps,
+        # each mla_decode_partial call launches the decode kernel and the split merge
+        "gpu_launches": 2 * args.steps,
         "clocks": clock_info,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
