@@ -5,10 +5,10 @@
 // online softmax between them.
 //
 // Roles (288 threads):
-//   warp 0, lane 0  TMA producer: Q of each request (9 boxes of 64 dims) and,
+//   warp 0          TMA producer: Q of each request (9 boxes of 64 dims) and,
 //                   per tile, one 4-D box per page holding the 64/P rows the
-//                   partition owns, into a [atom][dim block][8 rows][128 B]
-//                   swizzled layout that serves both MMAs.
+//                   partition owns (lane k: page k), into a [atom][dim block]
+//                   [8 rows][128 B] swizzled layout that serves both MMAs.
 //   warp 1          TMEM owner (alloc/free).
 //   warps 1, 2      lane 0 issues half of the score MMAs (one accumulator each).
 //   warps 3, 8      lane 0 issues the PV MMAs of two of the four value chunks.
@@ -162,6 +162,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
+  const int lane = threadIdx.x & 31;
   uint32_t kv_it = 0, q_it = 0;
   int last_q = -1, last_kv[2] = {-1, -1};
   // bf16: one 4-D box of groups_per_page swizzled atoms per page; e4m3: one
@@ -172,74 +173,85 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   const uint32_t dst0 = F8 ? sKv + kRawOff : sKv;
   bool ok = true;
 
-  // L2 prefetch of the pages of the tile kPrefetchAhead positions ahead: the
-  // 129 MB L2 gives the two shared-memory stages more HBM requests in flight.
+  // The whole warp produces: lane k handles page k of a tile (a tile spans P
+  // pages), so the page-index loads, L2 prefetches and TMA boxes of a tile go
+  // out together rather than one after another.  A lane's page index is read
+  // kPrefetchAhead tiles early, when the page is prefetched into L2 (the
+  // 129 MB L2 gives the two shared-memory stages more HBM requests in
+  // flight), and carried in `ring` until its tile is loaded.
   TileCursor ahead(p, r);
-  auto prefetch = [&]() {
-    if (!ahead.live) return;
-    int lp0, lp1;
-    tile_pages(p, ahead.t, ahead.w.n, &lp0, &lp1);
-    for (int k = 0; k <= lp1 - lp0; ++k) {
-      const int pg = p.block_table[size_t(ahead.w.b) * p.max_pages + lp0 + k];
-      if (pg >= 0 && pg < p.num_pages) {
-        if (F8)
-          tma_prefetch_2d(tm_kv, 0, pg * rows_per_page);
-        else
-          tma_prefetch_4d(tm_kv, 0, 0, 0, pg * tp.groups_per_page);
+  auto next_ahead = [&]() {
+    int pg = -1;
+    if (ahead.live) {
+      int lp0, lp1;
+      tile_pages(p, ahead.t, ahead.w.n, &lp0, &lp1);
+      if (lane <= lp1 - lp0) {
+        pg = p.block_table[size_t(ahead.w.b) * p.max_pages + lp0 + lane];
+        if (pg >= 0 && pg < p.num_pages) {
+          if (F8)
+            tma_prefetch_2d(tm_kv, 0, pg * rows_per_page);
+          else
+            tma_prefetch_4d(tm_kv, 0, 0, 0, pg * tp.groups_per_page);
+        }
       }
+      ahead.step();
     }
-    ahead.step();
+    return pg;
   };
-  for (int i = 0; i < kPrefetchAhead; ++i) prefetch();
+  int ring[kPrefetchAhead];
+#pragma unroll
+  for (int i = 0; i < kPrefetchAhead; ++i) ring[i] = next_ahead();
 
   TileCursor cur(p, r);
   while (cur.live) {
     if (cur.first()) {
       checked_len(p, cur.w.b, err);
-      if (!mbar_wait(bar_addr(m.q_empty), (q_it & 1) ^ 1, abort, kTimeoutNs)) { ok = false; break; }
-      mbar_arrive_expect_tx(bar_addr(m.q_full), uint32_t(kKb * tp.q_rows * 128));
-      for (int kb = 0; kb < kKb; ++kb)
-        tma_load_2d(sQ + kb * (64 * 128), tm_q, bar_addr(m.q_full), kb * 64,
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(m.q_empty), (q_it & 1) ^ 1, abort, kTimeoutNs))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(bar_addr(m.q_full), uint32_t(kKb * tp.q_rows * 128));
+      __syncwarp();
+      if (lane < kKb)
+        tma_load_2d(sQ + lane * (64 * 128), tm_q, bar_addr(m.q_full), lane * 64,
                     cur.w.b * p.heads + cur.w.g * kHeads);
       last_q = q_it & 1;
       ++q_it;
     }
-    // page indices are read before waiting for the stage, hiding their latency
     const int s = kv_it & 1;
     int lp0, lp1;
     tile_pages(p, cur.t, cur.w.n, &lp0, &lp1);
-    int pages[8];
-    uint32_t bytes = 0;
-    for (int k = 0; k <= lp1 - lp0; ++k) {
-      int pg = p.block_table[size_t(cur.w.b) * p.max_pages + lp0 + k];
-      if (pg < 0 || pg >= p.num_pages) {
-        atomicOr(err, kErrBadPage);
-        pg = -1;
-      } else {
-        bytes += page_bytes;
-      }
-      pages[k] = pg;
+    const bool mine = lane <= lp1 - lp0;
+    int pg = ring[0];
+    if (mine && (pg < 0 || pg >= p.num_pages)) {
+      atomicOr(err, kErrBadPage);
+      pg = -1;
     }
-    if (!mbar_wait(bar_addr(m.kv_empty[s]), ((kv_it >> 1) & 1) ^ 1, abort, kTimeoutNs)) {
+    const bool load = mine && pg >= 0;
+    const uint32_t bytes = uint32_t(__popc(__ballot_sync(0xffffffffu, load))) * page_bytes;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(m.kv_empty[s]), ((kv_it >> 1) & 1) ^ 1, abort,
+                                           kTimeoutNs))) {
       ok = false;
       break;
     }
-    mbar_arrive_expect_tx(bar_addr(m.kv_full[s]), bytes);
-    for (int k = 0; k <= lp1 - lp0; ++k)
-      if (pages[k] >= 0) {
-        if (F8)
-          tma_load_2d(dst0 + s * kStageBytes + k * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0,
-                      pages[k] * rows_per_page);
-        else
-          tma_load_4d(dst0 + s * kStageBytes + k * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0,
-                      0, 0, pages[k] * tp.groups_per_page);
-      }
+    if (lane == 0) mbar_arrive_expect_tx(bar_addr(m.kv_full[s]), bytes);
+    __syncwarp();
+    if (load) {
+      if (F8)
+        tma_load_2d(dst0 + s * kStageBytes + lane * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0,
+                    pg * rows_per_page);
+      else
+        tma_load_4d(dst0 + s * kStageBytes + lane * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0,
+                    0, 0, pg * tp.groups_per_page);
+    }
     last_kv[s] = (kv_it >> 1) & 1;
     ++kv_it;
-    prefetch();
+#pragma unroll
+    for (int i = 0; i + 1 < kPrefetchAhead; ++i) ring[i] = ring[i + 1];
+    ring[kPrefetchAhead - 1] = next_ahead();
     cur.step();
   }
-  if (!ok) atomicOr(err, kErrTimeout);
+  if (!ok && lane == 0) atomicOr(err, kErrTimeout);
   // never leave the CTA with a copy still in flight into its shared memory
   if (last_q >= 0) mbar_wait_drain(bar_addr(m.q_full), last_q, kDrainNs);
   for (int s = 0; s < 2; ++s)
@@ -882,8 +894,7 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
 
   if (r.start < r.end) {
     if (warp == 0) {
-      if (lane == 0)
-        tc_producer<F8>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
+      tc_producer<F8>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
     } else if (warp == 1 || warp == 2) {
       if (lane == 0) tc_mma_s<F8>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
     } else if (warp == 3 || warp == 8) {
