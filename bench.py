@@ -39,6 +39,7 @@ import workloads  # noqa: E402
 
 METRIC = "MLA decode tokens/s and KV-read HBM GB/s (fraction of roofline) on 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 ROW_BYTES = {"bf16": 576 * 2, "e4m3": 576}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_partial_long32k_traffic.txt")
 
@@ -87,6 +88,18 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense bf16 peak for the secondary (tensor) fraction: the burst figure
+    of the measured file, else the recipe's fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_digest() -> str:
@@ -293,6 +306,9 @@ def run_ours(args, world, rank, local):
     avg_launch_s = ms / 1e3 / args.steps
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / avg_launch_s / 1e9
+    flops = float(case.seq_lens.sum().item()) * H * (2 * 576 + 2 * 512)
+    tflops = flops / avg_launch_s / 1e12
+    tpeak, tpeak_kind = measured_bf16_tflops()
     traffic = recorded_traffic()
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -312,7 +328,12 @@ def run_ours(args, world, rank, local):
                      "frac_of_8tbs": achieved / 8000.0,
                      "traffic": traffic,
                      "kernel": "mla_decode_partial: decode kernel + split merge, timed "
-                               "together per call (CUDA events on the launching stream)"},
+                               "together per call (CUDA events on the launching stream)",
+                     # secondary: algorithmic flops of the real heads (QK^T over 576 dims,
+                     # PV over 512) against the dense bf16 peak; the padding of the
+                     # score MMA to 64 rows is not counted
+                     "tensor_tflops": tflops, "tensor_peak_tflops": tpeak,
+                     "tensor_frac": tflops / tpeak, "tensor_peak_source": tpeak_kind},
         "e2e": {"value": aggregate(e_ms_max, args.steps, B, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "q, block table and lengths copied from pinned host memory, out and "
