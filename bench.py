@@ -30,6 +30,7 @@ import sys
 import tempfile
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -403,12 +404,132 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def _append_subcache(case_bits_, B):
+    """The pages the append touches, copied into a compact cache (oracle sample)."""
+    kv, bt, pos = case_bits_
+    pages = [int(bt[b, int(pos[b]) // 64]) for b in range(B)]
+    uniq = sorted(set(pages))
+    remap = {p: i for i, p in enumerate(uniq)}
+    small = kv[uniq]
+    sbt = np.zeros((B, bt.shape[1]), dtype=np.int32)
+    for b in range(B):
+        sbt[b, int(pos[b]) // 64] = remap[pages[b]]
+    return small, sbt
+
+
+def run_append(args, world, rank, local):
+    """--op kv_append: one new cache row per request of the headline batch
+    (each request's last token rewritten, so its table needs no new page)."""
+    import mla_paged_decode_gb300 as mla
+    from mla_paged_decode_gb300 import build
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    if rank == 0 or not os.path.exists(mla.library_path()):
+        build.build()
+    barrier(world)
+    mla.load_library()
+    case = workloads.config_long32k(device=dev, seed=args.seed, batch=args.batch,
+                                    pool_pages=args.pool_pages)
+    B = case.batch
+    pos = (case.seq_lens - 1).contiguous()
+    g = torch.Generator().manual_seed(args.seed + 1)
+    new = torch.randn(B, 576, generator=g).to(torch.bfloat16).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mla.kv_append(new, case.kv_pages, case.block_table, pos, 0, 1, error_word=err,
+                      stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = ClockSampler(local)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    assert int(err.item()) == 0
+    # end to end: the new rows and positions from pinned host memory, the error word back
+    new_h, pos_h = new.cpu().pin_memory(), pos.cpu().pin_memory()
+    err_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    new_d, pos_d = torch.empty_like(new), torch.empty_like(pos)
+
+    def e2e_step():
+        new_d.copy_(new_h, non_blocking=True)
+        pos_d.copy_(pos_h, non_blocking=True)
+        mla.kv_append(new_d, case.kv_pages, case.block_table, pos_d, 0, 1, error_word=err,
+                      stream=stream)
+        err_h.copy_(err, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    per_s = ms / 1e3 / args.steps
+    byts = B * (1152 + 1152 + 8)   # new row read, cache row written, position + table entry
+    peak, peak_kind = measured_peaks()
+    line = {
+        "metric": "KV append: new cache rows per second (one per request), 1 GB300",
+        "value": aggregate(ms, args.steps, B, world), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "kv_append_" + case.name, "batch": B, "kv_dtype": "bf16",
+                   "positions": "each request's last token", "pool_pages": case.num_pages,
+                   "l2": "no flush: 147 KB per step, latency-bound"},
+        "roofline": {"bound": "hbm", "achieved": byts / per_s / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": byts / per_s / 1e9 / peak, "peak_source": peak_kind,
+                     "traffic": None,
+                     "kernel": "mla_kv_append (one launch per step); far below the HBM roof: "
+                               "a launch-latency-bound write of B rows"},
+        "e2e": {"value": aggregate(e_ms, args.steps, B, world), "unit": "rows/s",
+                "h2d_bytes_per_step": B * 1152 + B * 4, "d2h_bytes_per_step": 4},
+        "gpu_launches": args.steps,
+        "clocks": clock_info,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        kv_b = case.kv_pages.view(torch.int16).cpu().numpy().view(np.uint16)
+        bt = case.block_table.cpu().numpy()
+        small, sbt = _append_subcache((kv_b, bt, pos.cpu().numpy()), B)
+        new_b = new.view(torch.int16).cpu().numpy().view(np.uint16)
+        spent, calls = 0.0, 0
+        while spent < min(args.cpu_seconds, 5.0):
+            a = time.perf_counter()
+            oracle.kv_append(small, sbt, pos.cpu().numpy(), new_b, 0, 1)
+            spent += time.perf_counter() - a
+            calls += 1
+        line["cpu_baseline"] = {"value": calls * B / spent, "unit": "rows/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{calls} appends of the {B} rows into a compact copy "
+                                          f"of the {len(small)} touched pages, {spent:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["decode", "kv_append"], default="decode",
+                    help="decode (the headline) or the KV append of one row per request")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -420,7 +541,13 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
-    if args.impl == "reference":
+    if args.op == "kv_append":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the append's CPU oracle is reported as cpu_baseline of --op kv_append"}))
+            return
+        run_append(args, world, rank, local)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank, local)

@@ -1,7 +1,7 @@
 /*
  * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA absorbed paged-decode library.
  *
- * Two operations, both from the decode-context-parallel (DCP) pages:
+ * Three operations, all from the decode-context-parallel (DCP) pages:
  *
  *  mla_decode_partial  one partition's attention over a paged latent KV cache,
  *                      returning the partition-local pair (out, lse).
@@ -10,6 +10,12 @@
  *                      decode needs no causal bound), implementation step 3
  *                      (rank-local (out, lse); a rank owning nothing returns the
  *                      neutral (0, -inf)), step 4 (LSE in base 2 or base e).
+ *  mla_kv_append       the write side: each request's new token row into the
+ *                      paged cache (bf16, or quantised to e4m3 with the
+ *                      per-tensor scale), only on the partition that owns it.
+ *                      sglang pull 33926, implementation steps 3 (FP8 KV path)
+ *                      and 4 (under DCP the fused KV write is off and the
+ *                      pool's own write stores the rank's rows).
  *  mla_lse_combine     the LSE-weighted softmax merge of P partial results.
  *                      sglang pull 33364 ([Attention][DCP] Add symm_a2a ...),
  *                      "Modifications", kernel 4 (wait_lse_combine_kernel), here
@@ -167,6 +173,41 @@ int mla_decode_partial_noalloc(const void *q, const void *kv_pages, const int32_
  * synchronises; meant for tests and debugging.)
  */
 int mla_decode_check_workspace(void *workspace, mla_stream_t stream);
+
+/*
+ * Append: writes the new token's cache row of every request (sglang pull
+ * 33926, implementation steps 3 and 4; see the top of this file).
+ *
+ *  kv_new      bf16 [B, 576], contiguous: the new token's latent (dims 0..511)
+ *              and rope (512..575) per request, as the model produced them.
+ *  kv_pages    the GLOBAL paged cache, [num_pages, 64, 576] bf16 or e4m3 per
+ *              d->kv_dtype (written in place).
+ *  block_table int32 [B, max_pages_per_seq], as for mla_decode_partial.
+ *  positions   int32 [B]: global index t of each request's new token (its
+ *              length before the append).  Row t lands in physical page
+ *              block_table[b][t / 64], row t % 64.  t < 0 skips the request.
+ *  part_id, num_parts
+ *              only tokens the partition owns (t mod num_parts == part_id) are
+ *              written: each DCP rank stores its own rows.  num_parts = 1
+ *              writes every request's row.
+ *  d           the decode descriptor of the cache: batch, head_dim_qk (576),
+ *              page_size (64), num_pages, max_pages_per_seq, kv_dtype and, for
+ *              E4M3, kv_scale; num_heads, q_len and head_dim_v are not used.
+ *  error_word  optional device int32: a row whose logical page is past
+ *              max_pages_per_seq or whose block-table entry is outside
+ *              [0, num_pages) is skipped (never written) and bit 0 is OR-ed in.
+ *              NULL: such rows are skipped silently.
+ *
+ * A bf16 cache receives the row bits unchanged.  An e4m3 cache receives, per
+ * value, fp32(x) / kv_scale (an IEEE fp32 division) rounded to the nearest
+ * e4m3 value, ties to even, magnitudes past 448 saturated to +-448 (NaN
+ * inputs give an e4m3 NaN).  Rows of different requests must not alias (two
+ * requests writing the same page row race).  Enqueues one kernel on `stream`;
+ * batch 0 enqueues nothing.
+ */
+int mla_kv_append(const void *kv_new, void *kv_pages, const int32_t *block_table,
+                  const int32_t *positions, int part_id, int num_parts,
+                  const mla_decode_desc *d, int32_t *error_word, mla_stream_t stream);
 
 /* Sizes of an LSE combine. */
 typedef struct mla_combine_desc {

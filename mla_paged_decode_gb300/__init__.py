@@ -71,6 +71,8 @@ def load_library():
         lib.mla_decode_workspace_size.restype = sz
         lib.mla_decode_check_workspace.argtypes = [vp, vp]
         lib.mla_decode_check_workspace.restype = i32
+        lib.mla_kv_append.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(DecodeDesc), vp, vp]
+        lib.mla_kv_append.restype = i32
         lib.mla_lse_combine.argtypes = [vp, vp, i32, vp, ctypes.POINTER(CombineDesc), vp]
         lib.mla_lse_combine.restype = i32
         lib.mla_status_string.argtypes = [i32]
@@ -178,6 +180,45 @@ def decode_partial(q, kv_pages, block_table, seq_lens, part_id: int, num_parts: 
             _stream_ptr(stream, dev))
     _check(st)
     return out, lse
+
+
+def kv_append(kv_new, kv_pages, block_table, positions, part_id: int = 0, num_parts: int = 1, *,
+              kv_scale: float = 1.0, error_word=None, stream=None):
+    """mla_kv_append on torch tensors (see include/mla_decode.h).
+
+    kv_new bf16 [B, 576] (or [B, 1, 576]): each request's new token row;
+    positions int32 [B]: its global index (the length before the append;
+    negative skips the request).  Row positions[b] is written into kv_pages
+    (bf16, or uint8/float8_e4m3fn quantised with kv_scale) in place, if
+    partition part_id of num_parts owns it.  error_word: optional int32 [1]
+    device tensor that receives bit 0 for a row whose page entry is out of
+    range (that row is skipped).
+    """
+    dev = kv_pages.device
+    if dev.type != "cuda":
+        raise ValueError("kv_append runs on CUDA tensors only")
+    _need(kv_new, "kv_new", (torch.bfloat16,), dev)
+    _need(kv_pages, "kv_pages", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn), dev)
+    _need(block_table, "block_table", (torch.int32,), dev)
+    _need(positions, "positions", (torch.int32,), dev)
+    if kv_pages.dim() != 3 or block_table.dim() != 2:
+        raise ValueError("kv_pages must be [num_pages, 64, 576] and block_table [B, max_pages]")
+    B = positions.numel()
+    if kv_new.numel() != B * 576 or kv_new.shape[-1] != 576 or block_table.shape[0] != B:
+        raise ValueError("kv_new must be [B, 576] and block_table [B, max_pages] for B positions")
+    if error_word is not None:
+        _need(error_word, "error_word", (torch.int32,), dev)
+    d = DecodeDesc(batch=B, num_heads=1, q_len=1, head_dim_qk=576, head_dim_v=512,
+                   page_size=kv_pages.shape[1], num_pages=kv_pages.shape[0],
+                   max_pages_per_seq=block_table.shape[1], kv_dtype=_kv_dtype_code(kv_pages),
+                   kv_scale=float(kv_scale))
+    with torch.cuda.device(dev):
+        st = load_library().mla_kv_append(
+            kv_new.data_ptr(), kv_pages.data_ptr(), block_table.data_ptr(), positions.data_ptr(),
+            int(part_id), int(num_parts), ctypes.byref(d),
+            error_word.data_ptr() if error_word is not None else None, _stream_ptr(stream, dev))
+    _check(st)
+    return kv_pages
 
 
 def check_workspace(workspace: torch.Tensor, stream=None) -> int:

@@ -15,6 +15,10 @@
 
 namespace mla {
 cudaError_t launch_decode_simt(const DecodeParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_kv_append(const void *kv_new, void *kv_pages, const int32_t *block_table,
+                             const int32_t *positions, int batch, int part_id, int num_parts,
+                             int num_pages, int max_pages, int e4m3, float kv_scale,
+                             int32_t *error_word, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
                              const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
                              cudaStream_t stream);
@@ -177,6 +181,17 @@ int check_desc(const mla_decode_desc *d) {
   return MLA_OK;
 }
 
+// The fields of a decode descriptor that describe the cache itself.
+int check_cache_desc(const mla_decode_desc *d) {
+  if (!d) return MLA_ERR_NULL;
+  if (d->batch < 0 || d->num_pages < 1 || d->max_pages_per_seq < 1) return MLA_ERR_SHAPE;
+  if (d->head_dim_qk != mla::kDqk || d->page_size != mla::kPage) return MLA_ERR_SHAPE;
+  if (d->kv_dtype != MLA_KV_BF16 && d->kv_dtype != MLA_KV_E4M3) return MLA_ERR_ARG;
+  if (d->kv_dtype == MLA_KV_E4M3 && !(std::isfinite(d->kv_scale) && d->kv_scale > 0.f))
+    return MLA_ERR_ARG;
+  return MLA_OK;
+}
+
 int head_groups_of(const mla_decode_desc *d) {
   return (d->num_heads + kSimtHeadsPerGroup - 1) / kSimtHeadsPerGroup;
 }
@@ -277,6 +292,26 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
   } else {
     e = mla::launch_decode_simt(p, grid, s);
   }
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
+int mla_kv_append(const void *kv_new, void *kv_pages, const int32_t *block_table,
+                  const int32_t *positions, int part_id, int num_parts,
+                  const mla_decode_desc *d, int32_t *error_word, mla_stream_t stream) {
+  int st = check_cache_desc(d);
+  if (st != MLA_OK) return st;
+  if (num_parts < 1 || part_id < 0 || part_id >= num_parts) return MLA_ERR_PARTITION;
+  if (d->batch == 0) return MLA_OK;
+  if (!kv_new || !kv_pages || !block_table || !positions) return MLA_ERR_NULL;
+  if (!aligned(kv_new, 16) || !aligned(kv_pages, 16) || !aligned(block_table, 4) ||
+      !aligned(positions, 4) || !aligned(error_word, 4))
+    return MLA_ERR_ALIGN;
+  current_device(&st);
+  if (st != MLA_OK) return st;
+  cudaError_t e = mla::launch_kv_append(kv_new, kv_pages, block_table, positions, d->batch,
+                                        part_id, num_parts, d->num_pages, d->max_pages_per_seq,
+                                        d->kv_dtype == MLA_KV_E4M3, d->kv_scale, error_word,
+                                        reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 

@@ -38,6 +38,7 @@ import numpy as np
 
 D_QK = 576
 D_V = 512
+PAGE_SIZE = 64
 LOG2E = 1.4426950408889634   # log2(e)
 LN2 = 0.6931471805599453     # ln(2)
 LSE_NATURAL = 0
@@ -83,6 +84,71 @@ def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
     mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
     mag = np.where((e == 15) & ((b & 0x7) == 7), np.nan, mag)
     return sign * mag
+
+
+def _e4m3_finite_table():
+    """The 127 non-negative finite e4m3 values, ascending, with their codes."""
+    codes = np.arange(0x7F, dtype=np.uint8)          # 0x00 .. 0x7E (0x7F is NaN)
+    return e4m3_to_f64(codes), codes
+
+
+def f32_to_e4m3(x) -> np.ndarray:
+    """fp32 values -> OCP e4m3 codes (uint8): the nearest representable value,
+    ties to the even code (mantissa bit 0 clear), magnitudes beyond the
+    largest finite value 448 saturate to +-448, the sign is kept (so -0 and
+    negative values that round to zero give 0x80).  NaN inputs are not
+    defined here.  Exact: every fp32 input, e4m3 value and midpoint is exact
+    in fp64 (the write path of sglang pull 33926, implementation step 3:
+    the FP8 cache stores the quantised latent with one per-tensor scale)."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    vals, codes = _e4m3_finite_table()
+    a = np.abs(x)
+    hi = np.searchsorted(vals, a, side="left")       # first value >= a
+    hi = np.minimum(hi, len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    dlo = a - vals[lo]
+    dhi = vals[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & ((codes[hi] & 1) == 0))
+    c = np.where(a >= vals[-1], codes[-1], np.where(pick_hi, codes[hi], codes[lo]))
+    c = np.where(vals[hi] == a, codes[hi], c)
+    return (c | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+def kv_append(kv_bits: np.ndarray, block_table: np.ndarray, positions: np.ndarray,
+              new_bits: np.ndarray, part_id: int, num_parts: int, kv_dtype: str = "bf16",
+              kv_scale: float = 1.0, page_size: int = PAGE_SIZE):
+    """Writes each request's new latent row (bf16 bits [576]) into the paged
+    cache at global token positions[b] (the request's length before the
+    append), if positions[b] >= 0 and partition ``part_id`` owns that token
+    (positions[b] mod P == part_id: under DCP each rank writes only its own
+    tokens, sglang pull 33926, implementation step 4).  An e4m3 cache stores
+    f32_to_e4m3(fp32(x) / fp32(kv_scale)), the division in fp32 like the
+    kernel's.  A row whose page entry lies outside the table or the pool is
+    skipped and counted.  Returns (new cache, number of skipped rows); the
+    input cache is not modified."""
+    out = np.array(kv_bits, copy=True)
+    bt = np.asarray(block_table)
+    num_pages, max_pages = out.shape[0], bt.shape[1]
+    bad = 0
+    for b in range(len(positions)):
+        t = int(positions[b])
+        if t < 0 or t % num_parts != part_id:
+            continue
+        lp = t // page_size
+        if lp >= max_pages:
+            bad += 1
+            continue
+        pg = int(bt[b, lp])
+        if pg < 0 or pg >= num_pages:
+            bad += 1
+            continue
+        row = np.asarray(new_bits[b], dtype=np.uint16)
+        if kv_dtype == "bf16":
+            out[pg, t % page_size] = row
+        else:
+            x = (row.astype(np.uint32) << 16).view(np.float32)
+            out[pg, t % page_size] = f32_to_e4m3(x / np.float32(kv_scale))
+    return out, bad
 
 
 # ------------------------------------------------------------ paged gather

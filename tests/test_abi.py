@@ -137,3 +137,35 @@ def test_python_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 1, 16, 576, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         mla.decode_partial(q, q, q, q, 0, 1, 0.1, 0, q, q)
+
+
+def _append(lib, d, *, part_id=0, num_parts=1, kv_new=FAKE, kv=FAKE, err=None):
+    return lib.mla_kv_append(kv_new, kv, FAKE, FAKE, part_id, num_parts,
+                             ctypes.byref(d) if d is not None else None, err, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim_qk=512), -2), (dict(page_size=128), -2), (dict(num_pages=0), -2),
+    (dict(max_pages_per_seq=0), -2), (dict(batch=-3), -2), (dict(kv_dtype=2), -6),
+    (dict(kv_dtype=1, kv_scale=-1.0), -6), (dict(kv_dtype=1, kv_scale=float("inf")), -6),
+])
+def test_append_rejects_a_bad_cache_descriptor(lib, kw, code):
+    assert _append(lib, _desc(**kw)) == code
+
+
+def test_append_ignores_the_query_fields_of_the_descriptor(lib):
+    # q_len, num_heads and head_dim_v describe a query, not the cache: a
+    # descriptor with other values still gets as far as the pointer checks
+    assert _append(lib, _desc(q_len=3, num_heads=0, head_dim_v=1), kv_new=0) == -1
+
+
+def test_append_rejects_bad_partition_pointers_and_alignment(lib):
+    for part_id, num_parts in [(0, 0), (3, 3), (-1, 1)]:
+        assert _append(lib, _desc(), part_id=part_id, num_parts=num_parts) == -3
+    assert _append(lib, None) == -1
+    assert _append(lib, _desc(), kv_new=0) == -1
+    assert _append(lib, _desc(), kv=0) == -1
+    assert _append(lib, _desc(), kv_new=FAKE + 8) == -4
+    assert _append(lib, _desc(), kv=FAKE + 4) == -4
+    assert _append(lib, _desc(), err=FAKE + 2) == -4
+    assert _append(lib, _desc(batch=0), kv_new=0, kv=0) == 0

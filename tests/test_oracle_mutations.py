@@ -59,8 +59,22 @@ def _pin_formats():
     pins.test_fp8_partial_matches_brute_force()
 
 
+def _pin_append():
+    import test_oracle_append as ap
+    ap.test_e4m3_encode_round_trips_every_finite_code()
+    ap.test_e4m3_encode_ties_go_to_the_even_code()
+    ap.test_e4m3_encode_saturates_at_448()
+    ap.test_e4m3_encode_matches_torch_float8_in_range()
+    ap.test_append_writes_the_row_bits_and_nothing_else()
+    for n in (2, 3, 8):
+        ap.test_partition_appends_together_equal_one_unpartitioned_append(n)
+    ap.test_e4m3_append_stores_torchs_cast_of_x_over_scale()
+    ap.test_rows_with_a_bad_page_are_counted_and_not_written()
+    ap.test_decode_after_append_attends_to_the_new_row()
+
+
 PINS = [lambda: _pin_brute(0), lambda: _pin_brute(1), _pin_full_dims, _pin_closed_forms,
-        _pin_partitions, _pin_combine, _pin_formats]
+        _pin_partitions, _pin_combine, _pin_formats, _pin_append]
 
 
 def pin_failures() -> int:
@@ -157,7 +171,50 @@ def _e4m3_bias8(bits):
     return om.e4m3_to_f64(bits) / 2.0
 
 
+def _e4m3_encode_variant(x, tie_up=False, truncate=False, saturate=True):
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    vals, codes = om._e4m3_finite_table()
+    a = np.abs(x)
+    hi = np.minimum(np.searchsorted(vals, a, side="left"), len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - vals[lo], vals[hi] - a
+    if truncate:
+        pick_hi = np.zeros_like(a, dtype=bool)
+    elif tie_up:
+        pick_hi = dhi <= dlo
+    else:
+        pick_hi = (dhi < dlo) | ((dhi == dlo) & ((codes[hi] & 1) == 0))
+    c = np.where(pick_hi, codes[hi], codes[lo])
+    c = np.where(vals[hi] == a, codes[hi], c)
+    c = np.where(a >= vals[-1], codes[-1] if saturate else 0x7F, c)
+    c = np.where((a == vals[-1]), codes[-1], c)
+    return (c | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+_orig_append = om.kv_append
+
+
+def _append_ignores_owner(kv, bt, pos, new, part_id, num_parts, *a, **k):
+    return _orig_append(kv, bt, pos, new, 0, 1, *a, **k)
+
+
+def _append_row_off_by_one(kv, bt, pos, new, part_id, num_parts, *a, **k):
+    pos = np.where(np.asarray(pos) >= 0, np.asarray(pos) + 1, pos)
+    return _orig_append(kv, bt, pos, new, part_id, num_parts, *a, **k)
+
+
+def _append_scale_multiplies(kv, bt, pos, new, part_id, num_parts, kv_dtype="bf16",
+                             kv_scale=1.0, **k):
+    return _orig_append(kv, bt, pos, new, part_id, num_parts, kv_dtype, 1.0 / kv_scale, **k)
+
+
 MUTANTS = {
+    "e4m3 encode truncates": ("f32_to_e4m3", lambda x: _e4m3_encode_variant(x, truncate=True)),
+    "e4m3 ties away from zero": ("f32_to_e4m3", lambda x: _e4m3_encode_variant(x, tie_up=True)),
+    "e4m3 no saturation": ("f32_to_e4m3", lambda x: _e4m3_encode_variant(x, saturate=False)),
+    "append ignores the owner rule": ("kv_append", _append_ignores_owner),
+    "append one row off": ("kv_append", _append_row_off_by_one),
+    "append multiplies by the scale": ("kv_append", _append_scale_multiplies),
     "blocked owner rule": ("owned_tokens", _blocked_owner),
     "owner off by one": ("owned_tokens", _off_by_one_owner),
     "page / row swapped": ("gather_rows", _swapped_page_row),
