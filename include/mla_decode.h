@@ -1,7 +1,7 @@
 /*
  * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA absorbed paged-decode library.
  *
- * Three operations, all from the decode-context-parallel (DCP) pages:
+ * Operations, all from the decode-context-parallel (DCP) pages:
  *
  *  mla_decode_partial  one partition's attention over a paged latent KV cache,
  *                      returning the partition-local pair (out, lse).
@@ -16,6 +16,8 @@
  *                      sglang pull 33926, implementation steps 3 (FP8 KV path)
  *                      and 4 (under DCP the fused KV write is off and the
  *                      pool's own write stores the rank's rows).
+ *  mla_decode_dcp      all P partitions in one call (one decode launch for P | 8)
+ *                      and their merge: the DCP ranks emulated on one GPU.
  *  mla_lse_combine     the LSE-weighted softmax merge of P partial results.
  *                      sglang pull 33364 ([Attention][DCP] Add symm_a2a ...),
  *                      "Modifications", kernel 4 (wait_lse_combine_kernel), here
@@ -140,6 +142,39 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
                        const int32_t *seq_lens, int part_id, int num_parts, float sm_scale,
                        int lse_base, void *out, float *lse, const mla_decode_desc *d,
                        void *workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * All partitions of a DCP decode in one call: the partial results of every
+ * partition r = 0..num_parts-1 (each exactly what mla_decode_partial with
+ * part_id = r returns, up to the rounding order of requests split across
+ * SMs) and their LSE-weighted merge.  On the pages each DCP rank returns its
+ * partition-local (out, lse) and the ranks' results are merged at the
+ * attention output (sglang pull 33926, implementation step 3; pull 33364,
+ * "Modifications", kernel 4); this call emulates all the ranks on one GPU.
+ *
+ *  q, kv_pages, block_table, seq_lens, sm_scale, lse_base, d
+ *              as for mla_decode_partial.
+ *  partials     bf16 [num_parts, B, 1, H, 512]: partition r's out.
+ *  partial_lses fp32 [num_parts, B, 1, H] in lse_base: partition r's lse
+ *               (-inf where it owns no token of the request).
+ *  out          bf16 [B, 1, H, 512]: the merge over the partitions (as
+ *               mla_lse_combine computes it from partials / partial_lses).
+ *  out_lse      optional fp32 [B, 1, H]: the merged lse, or NULL.
+ *  workspace    >= mla_decode_dcp_workspace_size(d, num_parts, 0) bytes, same
+ *               rules as for mla_decode_partial.
+ *
+ * num_parts in {1, 2, 4, 8}: one decode launch covers every (partition,
+ * request) pair, then one split merge and the combine (three kernels).
+ * Other num_parts (up to 256): one decode call per partition, then the
+ * combine.  Errors and bounds reporting as for mla_decode_partial.
+ */
+size_t mla_decode_dcp_workspace_size(const mla_decode_desc *d, int num_parts, int num_sms);
+
+int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_table,
+                   const int32_t *seq_lens, int num_parts, float sm_scale, int lse_base,
+                   void *partials, float *partial_lses, void *out, float *out_lse,
+                   const mla_decode_desc *d, void *workspace, size_t workspace_bytes,
+                   mla_stream_t stream);
 
 /*
  * mla_decode_partial without a workspace argument.  The method on the pages

@@ -71,6 +71,11 @@ def load_library():
         lib.mla_decode_workspace_size.restype = sz
         lib.mla_decode_check_workspace.argtypes = [vp, vp]
         lib.mla_decode_check_workspace.restype = i32
+        lib.mla_decode_dcp.argtypes = [vp, vp, vp, vp, i32, f32, i32, vp, vp, vp, vp,
+                                       ctypes.POINTER(DecodeDesc), vp, sz, vp]
+        lib.mla_decode_dcp.restype = i32
+        lib.mla_decode_dcp_workspace_size.argtypes = [ctypes.POINTER(DecodeDesc), i32, i32]
+        lib.mla_decode_dcp_workspace_size.restype = sz
         lib.mla_kv_append.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(DecodeDesc), vp, vp]
         lib.mla_kv_append.restype = i32
         lib.mla_lse_combine.argtypes = [vp, vp, i32, vp, ctypes.POINTER(CombineDesc), vp]
@@ -219,6 +224,65 @@ def kv_append(kv_new, kv_pages, block_table, positions, part_id: int = 0, num_pa
             error_word.data_ptr() if error_word is not None else None, _stream_ptr(stream, dev))
     _check(st)
     return kv_pages
+
+
+def make_dcp_workspace(q, kv_pages, block_table, num_parts: int, kv_scale: float = 1.0):
+    """A zero-filled workspace for decode_dcp over num_parts partitions."""
+    d = _decode_desc(q, kv_pages, block_table, kv_scale)
+    with torch.cuda.device(q.device):
+        n = load_library().mla_decode_dcp_workspace_size(ctypes.byref(d), int(num_parts), 0)
+    if n == 0:
+        raise MlaError(-2, "cannot size a workspace for these shapes")
+    return torch.zeros(n, dtype=torch.uint8, device=q.device)
+
+
+def decode_dcp(q, kv_pages, block_table, seq_lens, num_parts: int, sm_scale: float,
+               lse_base: int, *, partials=None, partial_lses=None, out=None, out_lse=None,
+               kv_scale: float = 1.0, workspace=None, stream=None):
+    """mla_decode_dcp: every partition's (out, lse) and their merge in one call.
+
+    Returns (out [B,1,H,512], out_lse [B,1,H] or None, partials [P,B,1,H,512],
+    partial_lses [P,B,1,H]); the output tensors are allocated when not given.
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("decode_dcp runs on CUDA tensors only")
+    _need(q, "q", (torch.bfloat16,), dev)
+    _need(kv_pages, "kv_pages", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn), dev)
+    _need(block_table, "block_table", (torch.int32,), dev)
+    _need(seq_lens, "seq_lens", (torch.int32,), dev)
+    d = _decode_desc(q, kv_pages, block_table, kv_scale)
+    B, H, P = d.batch, d.num_heads, int(num_parts)
+    if seq_lens.numel() != B or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("seq_lens / block_table do not match the batch")
+    if partials is None:
+        partials = torch.empty(P, B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+    if partial_lses is None:
+        partial_lses = torch.empty(P, B, 1, H, dtype=torch.float32, device=dev)
+    if out is None:
+        out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+    _need(partials, "partials", (torch.bfloat16,), dev)
+    _need(partial_lses, "partial_lses", (torch.float32,), dev)
+    _need(out, "out", (torch.bfloat16,), dev)
+    if partials.numel() != P * B * H * 512 or partial_lses.numel() != P * B * H:
+        raise ValueError("partials must be [P,B,1,H,512] and partial_lses [P,B,1,H]")
+    if out.numel() != B * H * 512:
+        raise ValueError("out must be [B,1,H,512]")
+    if out_lse is not None:
+        _need(out_lse, "out_lse", (torch.float32,), dev)
+        if out_lse.numel() != B * H:
+            raise ValueError("out_lse must be [B,1,H]")
+    if workspace is None:
+        workspace = make_dcp_workspace(q, kv_pages, block_table, P, kv_scale)
+    _need(workspace, "workspace", (torch.uint8,), dev)
+    with torch.cuda.device(dev):
+        st = load_library().mla_decode_dcp(
+            q.data_ptr(), kv_pages.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), P,
+            float(sm_scale), int(lse_base), partials.data_ptr(), partial_lses.data_ptr(),
+            out.data_ptr(), out_lse.data_ptr() if out_lse is not None else None, ctypes.byref(d),
+            workspace.data_ptr(), workspace.numel(), _stream_ptr(stream, dev))
+    _check(st)
+    return out, out_lse, partials, partial_lses
 
 
 def check_workspace(workspace: torch.Tensor, stream=None) -> int:

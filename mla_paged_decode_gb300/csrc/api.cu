@@ -115,12 +115,16 @@ bool tensor_core_path(const mla_decode_desc *, int num_parts) {
 }
 
 // Q as [B*H rows, 576] bf16, one 64-column swizzled box of min(64, H) rows;
-// partition r's rows of a bf16 cache as a 4-D view (64 dims, 8 rows of stride
-// P, 9 blocks of 64 dims, groups of 8 rows), one box = one page's owned rows;
-// of an e4m3 cache as a 2-D view (144 words of 4 fp8 values, rows of stride
-// P), one unswizzled box = one page's 64/P owned rows of 576 B.
+// partition rows of a bf16 cache as a 5-D view (64 dims, 8 rows of stride P,
+// 9 blocks of 64 dims, groups of 8 rows, partitions), one box = one page's
+// owned rows; of an e4m3 cache as a 3-D view (144 words of 4 fp8 values,
+// rows of stride P, partitions), one unswizzled box = one page's 64/P owned
+// rows of 576 B.  For one partition (`part_id`) the base is offset to its
+// first row and the partition dimension is left off (4-D / 2-D maps, the
+// faster boxes); for all P partitions (`all_parts`) it is added, with a stride
+// of one row (5-D / 3-D maps, coordinate r).
 int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, int part_id,
-                     int num_parts, CUtensorMap *tm_q, CUtensorMap *tm_kv) {
+                     int num_parts, bool all_parts, CUtensorMap *tm_q, CUtensorMap *tm_kv) {
   EncodeTiled enc = encode_tiled();
   if (!enc) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled unavailable");
@@ -141,24 +145,26 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
     const cuuint64_t P = cuuint64_t(num_parts);
     const cuuint32_t R = cuuint32_t(mla::kPage / num_parts);
     const cuuint64_t row8 = cuuint64_t(mla::kDqk);
-    const char *base = static_cast<const char *>(kv) + size_t(part_id) * row8;
-    cuuint64_t dims[2] = {row8 / 4, cuuint64_t(d->num_pages) * R};
-    cuuint64_t strides[1] = {P * row8};
-    cuuint32_t box[2] = {cuuint32_t(row8 / 4), R};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<char *>(base), dims,
+    const char *base = static_cast<const char *>(kv) + (all_parts ? 0 : size_t(part_id) * row8);
+    cuuint64_t dims[3] = {row8 / 4, cuuint64_t(d->num_pages) * R, P};
+    cuuint64_t strides[2] = {P * row8, row8};
+    cuuint32_t box[3] = {cuuint32_t(row8 / 4), R, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT32, all_parts ? 3 : 2,
+                     const_cast<char *>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3", r);
   } else {
     const cuuint64_t P = cuuint64_t(num_parts);
     const cuuint32_t G = cuuint32_t(8 / num_parts);
-    const char *base = static_cast<const char *>(kv) + size_t(part_id) * row;
-    cuuint64_t dims[4] = {64, 8, cuuint64_t(mla::kDqk / 64), cuuint64_t(d->num_pages) * G};
-    cuuint64_t strides[3] = {P * row, 128, 8 * P * row};
-    cuuint32_t box[4] = {64, 8, cuuint32_t(mla::kDqk / 64), G};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = enc(tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<char *>(base), dims,
+    const char *base = static_cast<const char *>(kv) + (all_parts ? 0 : size_t(part_id) * row);
+    cuuint64_t dims[5] = {64, 8, cuuint64_t(mla::kDqk / 64), cuuint64_t(d->num_pages) * G, P};
+    cuuint64_t strides[4] = {P * row, 128, 8 * P * row, row};
+    cuuint32_t box[5] = {64, 8, cuuint32_t(mla::kDqk / 64), G, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, all_parts ? 5 : 4,
+                     const_cast<char *>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv", r);
@@ -194,6 +200,55 @@ int check_cache_desc(const mla_decode_desc *d) {
 
 int head_groups_of(const mla_decode_desc *d) {
   return (d->num_heads + kSimtHeadsPerGroup - 1) / kSimtHeadsPerGroup;
+}
+
+// Builds the decode parameters and enqueues the decode kernel and its split
+// merge (arguments already validated).  `fused`: all num_parts partitions in
+// one launch (tensor-core path only); out / lse are then [P, B, ...].
+int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_table,
+                   const int32_t *seq_lens, int part_id, int num_parts, bool fused,
+                   float sm_scale, int lse_base, void *out, float *lse, const mla_decode_desc *d,
+                   void *workspace, int grid, cudaStream_t s) {
+  const bool tc = tensor_core_path(d, num_parts);
+  if (fused && !tc) return MLA_ERR_ARG;
+  const int per_group = tc ? kTcHeadsPerGroup : kSimtHeadsPerGroup;
+  const int groups = (d->num_heads + per_group - 1) / per_group;
+  const int vbatch = fused ? num_parts * d->batch : d->batch;
+  mla::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.kv = kv_pages;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.lse = lse;
+  p.ws = static_cast<unsigned char *>(workspace);
+  p.wl = mla::workspace_layout(vbatch * groups, grid);
+  p.batch = vbatch;
+  p.heads = d->num_heads;
+  p.head_groups = groups;
+  p.heads_per_group = per_group;
+  p.num_pages = d->num_pages;
+  p.max_pages = d->max_pages_per_seq;
+  p.part_id = fused ? 0 : part_id;
+  p.num_parts = num_parts;
+  p.fused = fused ? 1 : 0;
+  p.req_batch = d->batch;
+  p.kv_e4m3 = d->kv_dtype == MLA_KV_E4M3;
+  p.kv_scale = p.kv_e4m3 ? d->kv_scale : 1.f;
+  p.score_scale_log2 = sm_scale * mla::kLog2e;
+  p.lse_base2 = lse_base == MLA_LSE_BASE2;
+  cudaError_t e;
+  if (tc) {
+    CUtensorMap tm_q, tm_kv;
+    int st = make_tensor_maps(q, kv_pages, d, part_id, num_parts, fused, &tm_q, &tm_kv);
+    if (st != MLA_OK) return st;
+    const int h = d->num_heads < kTcHeadsPerGroup ? d->num_heads : kTcHeadsPerGroup;
+    const int npv = ((h + 15) / 16) * 16;
+    e = mla::launch_decode_tc(p, npv, h, 8 / num_parts, tm_q, tm_kv, grid, s);
+  } else {
+    e = mla::launch_decode_simt(p, grid, s);
+  }
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 
 }  // namespace
@@ -251,47 +306,66 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
 
   DeviceFacts f = current_device(&st);
   if (st != MLA_OK) return st;
-  const bool tc = tensor_core_path(d, num_parts);
-  const int per_group = tc ? kTcHeadsPerGroup : kSimtHeadsPerGroup;
-  const int groups = (d->num_heads + per_group - 1) / per_group;
-  const int grid = f.sms;
-  if (workspace_bytes < mla::workspace_layout(d->batch * head_groups_of(d), grid).total)
+  if (workspace_bytes < mla::workspace_layout(d->batch * head_groups_of(d), f.sms).total)
     return MLA_ERR_WORKSPACE;
-  const mla::WorkspaceLayout wl = mla::workspace_layout(d->batch * groups, grid);
+  return enqueue_decode(q, kv_pages, block_table, seq_lens, part_id, num_parts, false, sm_scale,
+                        lse_base, out, lse, d, workspace, f.sms,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
 
-  mla::DecodeParams p;
-  p.q = static_cast<const __nv_bfloat16 *>(q);
-  p.kv = kv_pages;
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
-  p.out = static_cast<__nv_bfloat16 *>(out);
-  p.lse = lse;
-  p.ws = static_cast<unsigned char *>(workspace);
-  p.wl = wl;
-  p.batch = d->batch;
-  p.heads = d->num_heads;
-  p.head_groups = groups;
-  p.heads_per_group = per_group;
-  p.num_pages = d->num_pages;
-  p.max_pages = d->max_pages_per_seq;
-  p.part_id = part_id;
-  p.num_parts = num_parts;
-  p.kv_e4m3 = d->kv_dtype == MLA_KV_E4M3;
-  p.kv_scale = p.kv_e4m3 ? d->kv_scale : 1.f;
-  p.score_scale_log2 = sm_scale * mla::kLog2e;
-  p.lse_base2 = lse_base == MLA_LSE_BASE2;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (tc) {
-    CUtensorMap tm_q, tm_kv;
-    st = make_tensor_maps(q, kv_pages, d, part_id, num_parts, &tm_q, &tm_kv);
-    if (st != MLA_OK) return st;
-    const int h = d->num_heads < kTcHeadsPerGroup ? d->num_heads : kTcHeadsPerGroup;
-    const int npv = ((h + 15) / 16) * 16;
-    e = mla::launch_decode_tc(p, npv, h, 8 / num_parts, tm_q, tm_kv, grid, s);
-  } else {
-    e = mla::launch_decode_simt(p, grid, s);
+size_t mla_decode_dcp_workspace_size(const mla_decode_desc *d, int num_parts, int num_sms) {
+  if (check_desc(d) != MLA_OK || num_parts < 1) return 0;
+  if (num_sms <= 0) {
+    int st = 0;
+    DeviceFacts f = current_device(&st);
+    if (f.sms <= 0) return 0;
+    num_sms = f.sms;
   }
+  const long long virt = (long long)num_parts * d->batch * head_groups_of(d);
+  if (virt > (1LL << 30)) return 0;
+  return mla::workspace_layout(int(virt), num_sms).total;
+}
+
+int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_table,
+                   const int32_t *seq_lens, int num_parts, float sm_scale, int lse_base,
+                   void *partials, float *partial_lses, void *out, float *out_lse,
+                   const mla_decode_desc *d, void *workspace, size_t workspace_bytes,
+                   mla_stream_t stream) {
+  int st = check_desc(d);
+  if (st != MLA_OK) return st;
+  if (num_parts < 1 || num_parts > mla::combine_max_parts()) return MLA_ERR_PARTITION;
+  if (lse_base != MLA_LSE_NATURAL && lse_base != MLA_LSE_BASE2) return MLA_ERR_ARG;
+  if (!std::isfinite(sm_scale)) return MLA_ERR_ARG;
+  if (d->batch == 0) return MLA_OK;
+  if ((long long)num_parts * d->batch * d->num_heads > (1LL << 30)) return MLA_ERR_SHAPE;
+  if (!q || !kv_pages || !block_table || !seq_lens || !partials || !partial_lses || !out ||
+      !workspace)
+    return MLA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(kv_pages, 16) || !aligned(partials, 16) ||
+      !aligned(partial_lses, 4) || !aligned(out, 16) || !aligned(out_lse, 4) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+    return MLA_ERR_ALIGN;
+  DeviceFacts f = current_device(&st);
+  if (st != MLA_OK) return st;
+  if (workspace_bytes < mla_decode_dcp_workspace_size(d, num_parts, f.sms))
+    return MLA_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t rows = size_t(d->batch) * d->num_heads;
+  if (tensor_core_path(d, num_parts)) {
+    // every partition in one decode launch (and one split merge)
+    st = enqueue_decode(q, kv_pages, block_table, seq_lens, 0, num_parts, true, sm_scale,
+                        lse_base, partials, partial_lses, d, workspace, f.sms, s);
+    if (st != MLA_OK) return st;
+  } else {
+    for (int r = 0; r < num_parts; ++r) {
+      st = enqueue_decode(q, kv_pages, block_table, seq_lens, r, num_parts, false, sm_scale,
+                          lse_base, static_cast<__nv_bfloat16 *>(partials) + r * rows * mla::kDv,
+                          partial_lses + r * rows, d, workspace, f.sms, s);
+      if (st != MLA_OK) return st;
+    }
+  }
+  cudaError_t e = mla::launch_lse_combine(partials, partial_lses, num_parts, out, out_lse,
+                                          int(rows), mla::kDv, lse_base == MLA_LSE_BASE2, s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 

@@ -53,6 +53,11 @@ struct DecodeParams {
   int batch, heads, head_groups, heads_per_group;
   int num_pages, max_pages;
   int part_id, num_parts;
+  // All partitions in one launch (tensor-core kernel only): output row bv of
+  // `batch` = num_parts * req_batch rows is request bv % req_batch of
+  // partition bv / req_batch; out / lse are then [P, B, ...].  Otherwise
+  // fused = 0 and req_batch = batch.
+  int fused = 0, req_batch = 0;
   int kv_e4m3;
   float kv_scale;             // 1 for bf16
   float score_scale_log2;     // sm_scale * log2(e): scores kept in the base-2 domain
@@ -64,6 +69,15 @@ struct DecodeParams {
 // Tokens owned by partition r of P out of a global length L: t < L, t mod P == r.
 __device__ __forceinline__ int local_len(int L, int P, int r) {
   return L / P + (r < L % P ? 1 : 0);
+}
+
+// Output row bv -> the input request it reads (q, block table, length) and
+// the partition it attends for.
+__device__ __forceinline__ int req_of(const DecodeParams &p, int bv) {
+  return p.fused ? bv % p.req_batch : bv;
+}
+__device__ __forceinline__ int part_of(const DecodeParams &p, int bv) {
+  return p.fused ? bv / p.req_batch : p.part_id;
 }
 
 // Clamp a global length to what the block table can hold; flag a bad one.
@@ -78,9 +92,9 @@ __device__ __forceinline__ int checked_len(const DecodeParams &p, int b, int *er
 }
 
 __device__ __forceinline__ int request_tiles(const DecodeParams &p, int v) {
-  int b = v / p.head_groups;
-  int L = checked_len(p, b, nullptr);
-  int n = local_len(L, p.num_parts, p.part_id);
+  int bv = v / p.head_groups;
+  int L = checked_len(p, req_of(p, bv), nullptr);
+  int n = local_len(L, p.num_parts, part_of(p, bv));
   return (n + kTile - 1) / kTile;
 }
 

@@ -97,10 +97,14 @@ struct TcMisc {
 static_assert(sizeof(TcMisc) + 1024 <= tc::kSmemBytes - tc::kOffMisc, "shared memory budget");
 
 // The requests (and tile ranges) this CTA owns, in order; every role walks it.
+// FUSED: all partitions in one launch (output row b = partition * B + input
+// request); otherwise one partition, p.part_id, and row b is request b.
+template <bool FUSED>
 struct Walk {
   const DecodeParams &p;
   const CtaRange &r;
   int V, v, b, g, n, tiles;
+  int rb, part, pc;  // input request of output row b, its partition, the map's partition coordinate
   long long pv, t0, t1;
   __device__ Walk(const DecodeParams &p_, const CtaRange &r_)
       : p(p_), r(r_), V(p_.batch * p_.head_groups), v(r_.v_begin), pv(r_.p_begin) {}
@@ -112,7 +116,10 @@ struct Walk {
       t1 = min(r.end, pv + tiles) - pv;
       b = v / p.head_groups;
       g = v % p.head_groups;
-      n = local_len(checked_len(p, b, nullptr), p.num_parts, p.part_id);
+      rb = FUSED ? b % p.req_batch : b;
+      part = FUSED ? b / p.req_batch : p.part_id;
+      pc = FUSED ? part : 0;
+      n = local_len(checked_len(p, rb, nullptr), p.num_parts, part);
       return true;
     }
     return false;
@@ -121,8 +128,9 @@ struct Walk {
 };
 
 // One position in the walk: request + tile.
+template <bool FUSED>
 struct TileCursor {
-  Walk w;
+  Walk<FUSED> w;
   long long t;
   bool live;
   __device__ TileCursor(const DecodeParams &p, const CtaRange &r) : w(p, r), t(0) {
@@ -143,19 +151,20 @@ struct TileCursor {
 
 __device__ __forceinline__ uint32_t bar_addr(uint64_t &b) { return smem_u32(&b); }
 
-// Logical pages [lp0, lp1] that hold tile t's owned tokens (n tokens owned).
-__device__ __forceinline__ void tile_pages(const DecodeParams &p, long long t, int n, int *lp0,
-                                           int *lp1) {
+// Logical pages [lp0, lp1] that hold tile t's owned tokens (n tokens owned by
+// partition `part`).
+__device__ __forceinline__ void tile_pages(const DecodeParams &p, int part, long long t, int n,
+                                           int *lp0, int *lp1) {
   const int jl = min(int(t) * kTile + kTile, n) - 1;
   *lp0 = int(t) * p.num_parts;
-  *lp1 = int((p.part_id + (long long)p.num_parts * jl) / kPage);
+  *lp1 = int((part + (long long)p.num_parts * jl) / kPage);
 }
 
 // ------------------------------------------------------------------ producer
 
 constexpr int kPrefetchAhead = 2;  // tiles whose pages are pulled into L2 ahead of the stage
 
-template <bool F8>
+template <bool F8, bool FUSED>
 __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                             uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
                             int *err) {
@@ -179,19 +188,26 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   // kPrefetchAhead tiles early, when the page is prefetched into L2 (the
   // 129 MB L2 gives the two shared-memory stages more HBM requests in
   // flight), and carried in `ring` until its tile is loaded.
-  TileCursor ahead(p, r);
+  TileCursor<FUSED> ahead(p, r);
   auto next_ahead = [&]() {
     int pg = -1;
     if (ahead.live) {
       int lp0, lp1;
-      tile_pages(p, ahead.t, ahead.w.n, &lp0, &lp1);
+      tile_pages(p, ahead.w.part, ahead.t, ahead.w.n, &lp0, &lp1);
       if (lane <= lp1 - lp0) {
-        pg = p.block_table[size_t(ahead.w.b) * p.max_pages + lp0 + lane];
+        pg = p.block_table[size_t(ahead.w.rb) * p.max_pages + lp0 + lane];
         if (pg >= 0 && pg < p.num_pages) {
-          if (F8)
-            tma_prefetch_2d(tm_kv, 0, pg * rows_per_page);
-          else
-            tma_prefetch_4d(tm_kv, 0, 0, 0, pg * tp.groups_per_page);
+          if (F8) {
+            if (FUSED)
+              tma_prefetch_3d(tm_kv, 0, pg * rows_per_page, ahead.w.pc);
+            else
+              tma_prefetch_2d(tm_kv, 0, pg * rows_per_page);
+          } else {
+            if (FUSED)
+              tma_prefetch_5d(tm_kv, 0, 0, 0, pg * tp.groups_per_page, ahead.w.pc);
+            else
+              tma_prefetch_4d(tm_kv, 0, 0, 0, pg * tp.groups_per_page);
+          }
         }
       }
       ahead.step();
@@ -202,10 +218,10 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 #pragma unroll
   for (int i = 0; i < kPrefetchAhead; ++i) ring[i] = next_ahead();
 
-  TileCursor cur(p, r);
+  TileCursor<FUSED> cur(p, r);
   while (cur.live) {
     if (cur.first()) {
-      checked_len(p, cur.w.b, err);
+      checked_len(p, cur.w.rb, err);
       if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(m.q_empty), (q_it & 1) ^ 1, abort, kTimeoutNs))) {
         ok = false;
         break;
@@ -214,13 +230,13 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
       __syncwarp();
       if (lane < kKb)
         tma_load_2d(sQ + lane * (64 * 128), tm_q, bar_addr(m.q_full), lane * 64,
-                    cur.w.b * p.heads + cur.w.g * kHeads);
+                    cur.w.rb * p.heads + cur.w.g * kHeads);
       last_q = q_it & 1;
       ++q_it;
     }
     const int s = kv_it & 1;
     int lp0, lp1;
-    tile_pages(p, cur.t, cur.w.n, &lp0, &lp1);
+    tile_pages(p, cur.w.part, cur.t, cur.w.n, &lp0, &lp1);
     const bool mine = lane <= lp1 - lp0;
     int pg = ring[0];
     if (mine && (pg < 0 || pg >= p.num_pages)) {
@@ -237,12 +253,19 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
     if (lane == 0) mbar_arrive_expect_tx(bar_addr(m.kv_full[s]), bytes);
     __syncwarp();
     if (load) {
-      if (F8)
-        tma_load_2d(dst0 + s * kStageBytes + lane * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0,
-                    pg * rows_per_page);
-      else
-        tma_load_4d(dst0 + s * kStageBytes + lane * page_bytes, tm_kv, bar_addr(m.kv_full[s]), 0,
-                    0, 0, pg * tp.groups_per_page);
+      const uint32_t dst = dst0 + s * kStageBytes + lane * page_bytes;
+      if (F8) {
+        if (FUSED)
+          tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, pg * rows_per_page, cur.w.pc);
+        else
+          tma_load_2d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, pg * rows_per_page);
+      } else {
+        if (FUSED)
+          tma_load_5d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, 0, 0, pg * tp.groups_per_page,
+                      cur.w.pc);
+        else
+          tma_load_4d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, 0, 0, pg * tp.groups_per_page);
+      }
     }
     last_kv[s] = (kv_it >> 1) & 1;
     ++kv_it;
@@ -267,7 +290,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 
 // Descriptors: an offset is added to the encoded start address (bits 0..13,
 // address >> 4), which never carries because shared addresses stay below 256 KB.
-template <bool F8>
+template <bool F8, bool FUSED>
 __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                          uint32_t sKv, uint32_t tmem, int chain, int *err) {
   using namespace tc;
@@ -282,7 +305,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
   uint32_t s_it = 0, q_it = 0;
   bool ok = true;
-  for (TileCursor sc(p, r); sc.live; sc.step(), ++s_it) {
+  for (TileCursor<FUSED> sc(p, r); sc.live; sc.step(), ++s_it) {
     const int st = s_it & 1;
     const uint32_t ph = (s_it >> 1) & 1;
     if (!mbar_wait(bar_addr(kv_ready[st]), ph, abort, kTimeoutNs)) { ok = false; break; }
@@ -311,7 +334,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
 
 // O^T(chunk c) (+)= V^T(tile) P^T over ceil(nv/16) steps of 16 tokens; issuer
 // `half` takes value chunks 2 half and 2 half + 1.
-template <bool F8>
+template <bool F8, bool FUSED>
 __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
                           uint32_t tmem, int half, int *err) {
   using namespace tc;
@@ -323,7 +346,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
   uint32_t pv_it = 0, o_it = 0;
   bool ok = true;
-  for (TileCursor pc(p, r); pc.live; pc.step(), ++pv_it) {
+  for (TileCursor<FUSED> pc(p, r); pc.live; pc.step(), ++pv_it) {
     if (!mbar_wait(bar_addr(m.p_full[pv_it & 1]), (pv_it >> 1) & 1, abort, kTimeoutNs)) {
       ok = false;
       break;
@@ -421,7 +444,7 @@ __device__ __noinline__ void zero_value_tail(unsigned char *stage, int nv, int g
   }
 }
 
-template <bool F8>
+template <bool F8, bool FUSED>
 __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
                            unsigned char *smem, uint32_t tmem, int *err) {
   using namespace tc;
@@ -439,7 +462,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
   uint32_t kv_it = 0, p_it = 0, o_it = 0;
   bool ok = true;
 
-  Walk w(p, r);
+  Walk<FUSED> w(p, r);
   for (; ok && w.next(); w.advance()) {
     const int hn = min(kHeads, p.heads - w.g * kHeads);
     float mrun[2] = {-INFINITY, -INFINITY};  // running max (base-2 units) of each head
@@ -749,6 +772,7 @@ __device__ __noinline__ bool convert_q(const TcParams &tp, TcMisc &m, unsigned c
   return true;
 }
 
+template <bool FUSED>
 __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r, TcMisc &m,
                                            unsigned char *smem, int *err) {
   using namespace tc;
@@ -768,7 +792,7 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
   uint32_t kv_it = 0, q_it = 0;
   float qinv = 1.f;
   bool ok = true;
-  for (TileCursor c(p, r); c.live; c.step(), ++kv_it) {
+  for (TileCursor<FUSED> c(p, r); c.live; c.step(), ++kv_it) {
     if (c.first()) {
       if (!convert_q(tp, m, smem, c.w.g, q_it, &qinv)) { ok = false; break; }
       ++q_it;
@@ -833,7 +857,7 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
 
 // ------------------------------------------------------------------ kernel
 
-template <bool F8>
+template <bool F8, bool FUSED>
 __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     decode_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_kv) {
@@ -894,15 +918,15 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
 
   if (r.start < r.end) {
     if (warp == 0) {
-      tc_producer<F8>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
+      tc_producer<F8, FUSED>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
     } else if (warp == 1 || warp == 2) {
-      if (lane == 0) tc_mma_s<F8>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
+      if (lane == 0) tc_mma_s<F8, FUSED>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
     } else if (warp == 3 || warp == 8) {
-      if (lane == 0) tc_mma_pv<F8>(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
+      if (lane == 0) tc_mma_pv<F8, FUSED>(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
     } else if (warp < 8) {
-      tc_softmax<F8>(tp, r, m, smem, tmem, err);
+      tc_softmax<F8, FUSED>(tp, r, m, smem, tmem, err);
     } else if (F8) {
-      tc_convert(tp, r, m, smem, err);
+      tc_convert<FUSED>(tp, r, m, smem, err);
     }
   }
   tc_fence_before();
@@ -917,30 +941,36 @@ int tc_smem_bytes() { return tc::kSmemBytes; }
 
 cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream);
 
-cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
-                             const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
-                             cudaStream_t stream) {
-  static int configured[64][2] = {};
-  const bool f8 = p.kv_e4m3 != 0;
+template <bool F8, bool FUSED>
+static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
+                             int grid, cudaStream_t stream) {
+  static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev][f8]) {
-    cudaError_t e = cudaFuncSetAttribute(f8 ? decode_tc_kernel<true> : decode_tc_kernel<false>,
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<F8, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          tc::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev][f8] = 1;
+    configured[dev] = 1;
   }
+  decode_tc_kernel<F8, FUSED><<<grid, tc_threads<F8>(), tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
+                             const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
+                             cudaStream_t stream) {
   TcParams tp;
   tp.p = p;
   tp.npv = npv;
   tp.q_rows = q_rows;
   tp.groups_per_page = groups_per_page;
-  if (f8)
-    decode_tc_kernel<true><<<grid, tc::kThreadsF8, tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
-  else
-    decode_tc_kernel<false><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
-  cudaError_t e = cudaGetLastError();
+  const bool f8 = p.kv_e4m3 != 0, fused = p.fused != 0;
+  cudaError_t e = f8 ? (fused ? launch_tc<true, true>(tp, tm_q, tm_kv, grid, stream)
+                              : launch_tc<true, false>(tp, tm_q, tm_kv, grid, stream))
+                     : (fused ? launch_tc<false, true>(tp, tm_q, tm_kv, grid, stream)
+                              : launch_tc<false, false>(tp, tm_q, tm_kv, grid, stream));
   return e == cudaSuccess ? launch_split_merge(p, grid, stream) : e;
 }
 

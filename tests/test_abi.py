@@ -169,3 +169,28 @@ def test_append_rejects_bad_partition_pointers_and_alignment(lib):
     assert _append(lib, _desc(), kv=FAKE + 4) == -4
     assert _append(lib, _desc(), err=FAKE + 2) == -4
     assert _append(lib, _desc(batch=0), kv_new=0, kv=0) == 0
+
+
+def _dcp(lib, d, *, num_parts=2, partials=FAKE, out=FAKE, out_lse=None, ws=FAKE, ws_bytes=1 << 40):
+    return lib.mla_decode_dcp(FAKE, FAKE, FAKE, FAKE, num_parts, 0.1, 0, partials, FAKE, out,
+                              out_lse, ctypes.byref(d) if d is not None else None, ws, ws_bytes,
+                              None)
+
+
+def test_dcp_rejects_bad_arguments(lib):
+    assert _dcp(lib, _desc(q_len=2)) == -2
+    assert _dcp(lib, _desc(), num_parts=0) == -3
+    assert _dcp(lib, _desc(), num_parts=257) == -3
+    assert _dcp(lib, None) == -1
+    assert _dcp(lib, _desc(), partials=0) == -1
+    assert _dcp(lib, _desc(), out=FAKE + 8) == -4
+    assert _dcp(lib, _desc(), out_lse=FAKE + 2) == -4
+    assert _dcp(lib, _desc(batch=0), partials=0, out=0, ws=0) == 0
+
+
+def test_dcp_workspace_covers_every_partition(lib):
+    d = _desc(batch=64, num_heads=16)
+    one = lib.mla_decode_workspace_size(ctypes.byref(d), 152)
+    eight = lib.mla_decode_dcp_workspace_size(ctypes.byref(d), 8, 152)
+    assert eight > one and eight % 256 == 0
+    assert lib.mla_decode_dcp_workspace_size(ctypes.byref(d), 0, 152) == 0
