@@ -522,14 +522,132 @@ def run_append(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def run_dcp8(args, world, rank, local):
+    """--op dcp8: the decode-context-parallel workload (B=64, H=16, P=8; 60
+    requests of 131072 tokens and four of 1, 3, 5, 7) as one mla_decode_dcp
+    call per step: every partition's (out, lse) and their combine."""
+    import mla_paged_decode_gb300 as mla
+    from mla_paged_decode_gb300 import build
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    if rank == 0 or not os.path.exists(mla.library_path()):
+        build.build()
+    barrier(world)
+    mla.load_library()
+    case = workloads.config_dcp8(device=dev, seed=args.seed)
+    B, H, P = case.batch, case.heads, case.num_parts
+    kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
+    ws = mla.make_dcp_workspace(case.q, case.kv_pages, case.block_table, P)
+    parts = torch.empty(P, B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+    plse = torch.empty(P, B, 1, H, dtype=torch.float32, device=dev)
+    out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+    out_lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q=case.q, bt=case.block_table, sl=case.seq_lens):
+        mla.decode_dcp(q, case.kv_pages, bt, sl, P, case.sm_scale, 1, partials=parts,
+                       partial_lses=plse, out=out, out_lse=out_lse, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = ClockSampler(local)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    assert mla.check_workspace(ws) == 0
+    q_h, bt_h, sl_h = (case.q.cpu().pin_memory(), case.block_table.cpu().pin_memory(),
+                       case.seq_lens.cpu().pin_memory())
+    q_d, bt_d, sl_d = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        step(q_d, bt_d, sl_d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(out_lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    per_s = ms / 1e3 / args.steps
+    peak, peak_kind = measured_peaks()
+    tpeak, tpeak_kind = measured_bf16_tflops()
+    flops = float(case.seq_lens.sum().item()) * H * (2 * 576 + 2 * 512)
+    line = {
+        "metric": "MLA decode tokens/s and KV-read HBM GB/s (fraction of roofline) on 1 GB300",
+        "value": aggregate(ms, args.steps, B, world), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": case.name, "batch": B, "heads": H, "q_len": 1, "num_parts": P,
+                   "seq_lens": "60 x 131072 + {1, 3, 5, 7}", "page_size": 64,
+                   "pool_pages": case.num_pages, "kv_dtype": "bf16", "kv_bytes_per_step": kv_bytes,
+                   "l2": "inputs larger than L2: %.2f GB of KV read per step, no flush" % (kv_bytes / 1e9),
+                   "parallelism": "DCP partitions emulated on one GPU"},
+        "roofline": {"bound": "hbm", "achieved": kv_bytes / per_s / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": kv_bytes / per_s / 1e9 / peak,
+                     "peak_source": peak_kind, "frac_of_8tbs": kv_bytes / per_s / 1e9 / 8000.0,
+                     "traffic": None,
+                     "kernel": "mla_decode_dcp: one decode launch over the 8 partitions, split "
+                               "merge and LSE combine, timed together per call",
+                     "tensor_tflops": flops / per_s / 1e12, "tensor_peak_tflops": tpeak,
+                     "tensor_frac": flops / per_s / 1e12 / tpeak, "tensor_peak_source": tpeak_kind},
+        "e2e": {"value": aggregate(e_ms, args.steps, B, world), "unit": "tokens/s",
+                "h2d_bytes_per_step": q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4,
+                "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clock_info,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from casebits import subcase_bits
+        spent, tokens, done = 0.0, 0, 0
+        while spent < args.cpu_seconds and done < B:
+            q, kv, bt, lens = subcase_bits(case, [done])
+            a = time.perf_counter()
+            for r in range(P):
+                oracle.decode_partial(q, kv, bt, lens, r, P, case.sm_scale, 1)
+            spent += time.perf_counter() - a
+            tokens += int(lens[0])
+            done += 1
+        line["cpu_baseline"] = {"value": done / spent, "unit": "tokens/s", "cores": _oracle_threads(),
+                                "kind": "oracle",
+                                "sample": f"all {P} partitions of the first {done} of {B} requests "
+                                          f"({tokens} cached tokens), fp64 numpy, {spent:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["decode", "kv_append"], default="decode",
-                    help="decode (the headline) or the KV append of one row per request")
+    ap.add_argument("--op", choices=["decode", "dcp8", "kv_append"], default="decode",
+                    help="decode (the headline), dcp8 (the 8-partition DCP workload in one "
+                         "mla_decode_dcp call), or the KV append of one row per request")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -547,6 +665,12 @@ def main(argv=None):
                               "the append's CPU oracle is reported as cpu_baseline of --op kv_append"}))
             return
         run_append(args, world, rank, local)
+    elif args.op == "dcp8":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the DCP workload's CPU oracle is reported as cpu_baseline of --op dcp8"}))
+            return
+        run_dcp8(args, world, rank, local)
     elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
