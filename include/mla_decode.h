@@ -244,6 +244,51 @@ int mla_kv_append(const void *kv_new, void *kv_pages, const int32_t *block_table
                   const int32_t *positions, int part_id, int num_parts,
                   const mla_decode_desc *d, int32_t *error_word, mla_stream_t stream);
 
+/* Sizes of the DCP rank metadata. */
+typedef struct mla_dcp_meta_desc {
+  int32_t batch;              /* B requests (0 is a no-op)                         */
+  int32_t num_req_slots;      /* rows of req_to_token (>= 1)                       */
+  int32_t req_to_token_width; /* token slots per row of req_to_token (>= 1)        */
+  int32_t max_pages_per_seq;  /* columns of block_table (>= 1)                     */
+  int32_t extra_tokens;       /* added to every global length: the draft tokens of
+                                 a target-verify step, 0 for decode (>= 0)         */
+  int32_t pad_value;          /* block_table entries past a request's pages        */
+  int32_t page_size;          /* must be 64                                        */
+} mla_dcp_meta_desc;
+
+/*
+ * A DCP rank's per-step decode metadata, built on the device (sglang pull
+ * 33926, implementation step 1 and the code of _apply_dcp_cuda_graph_metadata:
+ * each step writes the global and the rank-local lengths into buffers that a
+ * captured CUDA graph keeps reading, then rebuilds the page table over the
+ * rank's own slice).  For partition part_id of num_parts and every request b:
+ *
+ *  global_lens[b] = seq_lens[b] + d->extra_tokens
+ *  local_lens[b]  = tokens of global_lens[b] the partition owns
+ *                   (t mod num_parts == part_id)
+ *  block_table[b][i] = req_to_token[req_pool_indices[b]][64 i] / 64 for the
+ *                   request's ceil(local_lens[b] / 64) local pages, then
+ *                   d->pad_value up to max_pages_per_seq.
+ *
+ * req_to_token (int32 [num_req_slots, req_to_token_width]) gives, for a
+ * request's j-th LOCAL token, its slot in the rank's compact pool (slot / 64
+ * = pool page, slot % 64 = row).  With these, mla_decode_partial(num_parts =
+ * 1) over the rank's compact pool with local_lens and block_table returns the
+ * rank's (out, lse) -- the same result as the partition of the global cache.
+ *
+ * A request with a negative global length (local length 0), a pool index
+ * outside req_to_token, or more pages than max_pages_per_seq or the width of
+ * req_to_token gets a table row of pad_value; a negative slot gives
+ * pad_value for its page; either ORs bit 0 into the optional device
+ * `error_word`.  All outputs are device int32 arrays written in full; the
+ * call allocates nothing and enqueues one kernel.
+ */
+int mla_dcp_local_metadata(const int32_t *seq_lens, const int32_t *req_pool_indices,
+                           const int32_t *req_to_token, int part_id, int num_parts,
+                           const mla_dcp_meta_desc *d, int32_t *global_lens,
+                           int32_t *local_lens, int32_t *block_table, int32_t *error_word,
+                           mla_stream_t stream);
+
 /* Sizes of an LSE combine. */
 typedef struct mla_combine_desc {
   int32_t num_tokens; /* T (0 is a no-op)                                         */

@@ -53,6 +53,13 @@ def library_path() -> str:
     return _LIB_PATH
 
 
+class DcpMetaDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_req_slots", ctypes.c_int32),
+                ("req_to_token_width", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+                ("extra_tokens", ctypes.c_int32), ("pad_value", ctypes.c_int32),
+                ("page_size", ctypes.c_int32)]
+
+
 def load_library():
     """Loads the built library (raises if it is missing)."""
     global _lib
@@ -76,6 +83,9 @@ def load_library():
         lib.mla_decode_dcp.restype = i32
         lib.mla_decode_dcp_workspace_size.argtypes = [ctypes.POINTER(DecodeDesc), i32, i32]
         lib.mla_decode_dcp_workspace_size.restype = sz
+        lib.mla_dcp_local_metadata.argtypes = [vp, vp, vp, i32, i32, ctypes.POINTER(DcpMetaDesc),
+                                               vp, vp, vp, vp, vp]
+        lib.mla_dcp_local_metadata.restype = i32
         lib.mla_kv_append.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(DecodeDesc), vp, vp]
         lib.mla_kv_append.restype = i32
         lib.mla_lse_combine.argtypes = [vp, vp, i32, vp, ctypes.POINTER(CombineDesc), vp]
@@ -283,6 +293,46 @@ def decode_dcp(q, kv_pages, block_table, seq_lens, num_parts: int, sm_scale: flo
             workspace.data_ptr(), workspace.numel(), _stream_ptr(stream, dev))
     _check(st)
     return out, out_lse, partials, partial_lses
+
+
+def dcp_local_metadata(seq_lens, req_pool_indices, req_to_token, part_id: int, num_parts: int,
+                       *, max_pages: int, extra_tokens: int = 0, pad_value: int = 0,
+                       global_lens=None, local_lens=None, block_table=None, error_word=None,
+                       stream=None):
+    """mla_dcp_local_metadata: a DCP rank's global and local lengths and its
+    rank-local page table [B, max_pages], built on the device (into the given
+    buffers when passed, so a captured graph can keep reading them).
+    Returns (global_lens, local_lens, block_table)."""
+    dev = seq_lens.device
+    if dev.type != "cuda":
+        raise ValueError("dcp_local_metadata runs on CUDA tensors only")
+    _need(seq_lens, "seq_lens", (torch.int32,), dev)
+    _need(req_pool_indices, "req_pool_indices", (torch.int32,), dev)
+    _need(req_to_token, "req_to_token", (torch.int32,), dev)
+    B = seq_lens.numel()
+    if req_pool_indices.numel() != B or req_to_token.dim() != 2:
+        raise ValueError("req_pool_indices must be [B] and req_to_token [slots, width]")
+    global_lens = global_lens if global_lens is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    local_lens = local_lens if local_lens is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    block_table = block_table if block_table is not None else torch.empty(
+        B, int(max_pages), dtype=torch.int32, device=dev)
+    for t, n in ((global_lens, "global_lens"), (local_lens, "local_lens"), (block_table, "block_table")):
+        _need(t, n, (torch.int32,), dev)
+    if global_lens.numel() != B or local_lens.numel() != B or block_table.numel() != B * int(max_pages):
+        raise ValueError("output buffers do not match the batch and max_pages")
+    if error_word is not None:
+        _need(error_word, "error_word", (torch.int32,), dev)
+    d = DcpMetaDesc(batch=B, num_req_slots=req_to_token.shape[0],
+                    req_to_token_width=req_to_token.shape[1], max_pages_per_seq=int(max_pages),
+                    extra_tokens=int(extra_tokens), pad_value=int(pad_value), page_size=64)
+    with torch.cuda.device(dev):
+        st = load_library().mla_dcp_local_metadata(
+            seq_lens.data_ptr(), req_pool_indices.data_ptr(), req_to_token.data_ptr(), int(part_id),
+            int(num_parts), ctypes.byref(d), global_lens.data_ptr(), local_lens.data_ptr(),
+            block_table.data_ptr(), error_word.data_ptr() if error_word is not None else None,
+            _stream_ptr(stream, dev))
+    _check(st)
+    return global_lens, local_lens, block_table
 
 
 def check_workspace(workspace: torch.Tensor, stream=None) -> int:

@@ -15,6 +15,12 @@
 
 namespace mla {
 cudaError_t launch_decode_simt(const DecodeParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_dcp_metadata(const int32_t *seq_lens, const int32_t *req_pool_indices,
+                                const int32_t *req_to_token, int batch, int r2t_rows,
+                                int r2t_width, int extra, int part_id, int num_parts,
+                                int32_t *global_lens, int32_t *local_lens, int32_t *table,
+                                int max_pages, int32_t pad, int32_t *error_word,
+                                cudaStream_t stream);
 cudaError_t launch_kv_append(const void *kv_new, void *kv_pages, const int32_t *block_table,
                              const int32_t *positions, int batch, int part_id, int num_parts,
                              int num_pages, int max_pages, int e4m3, float kv_scale,
@@ -386,6 +392,35 @@ int mla_kv_append(const void *kv_new, void *kv_pages, const int32_t *block_table
                                         part_id, num_parts, d->num_pages, d->max_pages_per_seq,
                                         d->kv_dtype == MLA_KV_E4M3, d->kv_scale, error_word,
                                         reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
+int mla_dcp_local_metadata(const int32_t *seq_lens, const int32_t *req_pool_indices,
+                           const int32_t *req_to_token, int part_id, int num_parts,
+                           const mla_dcp_meta_desc *d, int32_t *global_lens,
+                           int32_t *local_lens, int32_t *block_table, int32_t *error_word,
+                           mla_stream_t stream) {
+  if (!d) return MLA_ERR_NULL;
+  if (num_parts < 1 || part_id < 0 || part_id >= num_parts) return MLA_ERR_PARTITION;
+  if (d->batch < 0 || d->num_req_slots < 1 || d->req_to_token_width < 1 ||
+      d->max_pages_per_seq < 1 || d->page_size != mla::kPage)
+    return MLA_ERR_SHAPE;
+  if (d->extra_tokens < 0) return MLA_ERR_ARG;
+  if (d->batch == 0) return MLA_OK;
+  if (!seq_lens || !req_pool_indices || !req_to_token || !global_lens || !local_lens ||
+      !block_table)
+    return MLA_ERR_NULL;
+  if (!aligned(seq_lens, 4) || !aligned(req_pool_indices, 4) || !aligned(req_to_token, 4) ||
+      !aligned(global_lens, 4) || !aligned(local_lens, 4) || !aligned(block_table, 4) ||
+      !aligned(error_word, 4))
+    return MLA_ERR_ALIGN;
+  int st = 0;
+  current_device(&st);
+  if (st != MLA_OK) return st;
+  cudaError_t e = mla::launch_dcp_metadata(
+      seq_lens, req_pool_indices, req_to_token, d->batch, d->num_req_slots, d->req_to_token_width,
+      d->extra_tokens, part_id, num_parts, global_lens, local_lens, block_table,
+      d->max_pages_per_seq, d->pad_value, error_word, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 

@@ -54,6 +54,52 @@ def local_len(seq_len: int, num_parts: int, part_id: int) -> int:
     return seq_len // num_parts + (1 if part_id < seq_len % num_parts else 0)
 
 
+def dcp_local_metadata(seq_lens, req_pool_indices, req_to_token, part_id: int, num_parts: int,
+                       extra_tokens: int = 0, max_pages: int = 1, pad_value: int = 0,
+                       page_size: int = 64):
+    """A DCP rank's decode metadata (sglang pull 33926,
+    ``_apply_dcp_cuda_graph_metadata``: global and rank-local lengths written
+    once per step into capture-stable buffers, then the page table rebuilt
+    over the rank's own slice).  Global lengths are L_b + extra_tokens (the
+    draft tokens of a target-verify step); local lengths are n_r(L); the
+    rank-local page table over the rank's compact pool maps local page i of
+    request b to the pool page holding its local token 64 i:
+    req_to_token[req_pool_indices[b], 64 i] // 64, for i < ceil(n / 64), and
+    pad_value after.  A request is counted bad (and its whole table row is
+    pad_value) if its global length is negative (local length 0), its pool
+    index is outside req_to_token, its pages do not fit max_pages or the
+    width of req_to_token; a negative token slot gives pad_value for that
+    page and also counts the request.  Returns (global, local, table, bad)."""
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    r2t = np.asarray(req_to_token)
+    B = len(seq_lens)
+    glob = (seq_lens + extra_tokens).astype(np.int32)
+    loc = np.zeros(B, dtype=np.int32)
+    table = np.full((B, max_pages), pad_value, dtype=np.int32)
+    bad = 0
+    for b in range(B):
+        L = int(glob[b])
+        if L < 0:
+            bad += 1
+            continue
+        loc[b] = local_len(L, num_parts, part_id)
+        req = int(req_pool_indices[b])
+        npages = -(-int(loc[b]) // page_size)
+        if req < 0 or req >= r2t.shape[0] or npages > max_pages or \
+                (npages > 0 and (npages - 1) * page_size >= r2t.shape[1]):
+            bad += 1
+            continue
+        neg = False
+        for i in range(npages):
+            slot = int(r2t[req, i * page_size])
+            if slot < 0:
+                neg = True
+            else:
+                table[b, i] = slot // page_size
+        bad += int(neg)
+    return glob, loc, table, bad
+
+
 def owned_tokens(seq_len: int, num_parts: int, part_id: int) -> np.ndarray:
     """Global 0-based token indices t < seq_len with t mod P == part_id
     (pull 33926, motivation: round-robin owner rule)."""

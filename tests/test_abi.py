@@ -194,3 +194,25 @@ def test_dcp_workspace_covers_every_partition(lib):
     eight = lib.mla_decode_dcp_workspace_size(ctypes.byref(d), 8, 152)
     assert eight > one and eight % 256 == 0
     assert lib.mla_decode_dcp_workspace_size(ctypes.byref(d), 0, 152) == 0
+
+
+def _meta(lib, part_id=0, num_parts=2, seq=FAKE, out=FAKE, err=None, **kw):
+    base = dict(batch=4, num_req_slots=8, req_to_token_width=256, max_pages_per_seq=4,
+                extra_tokens=0, pad_value=0, page_size=64)
+    base.update(kw)
+    d = mla.DcpMetaDesc(**base)
+    return lib.mla_dcp_local_metadata(seq, FAKE, FAKE, part_id, num_parts, ctypes.byref(d), out,
+                                      FAKE, FAKE, err, None)
+
+
+def test_dcp_metadata_rejects_bad_arguments(lib):
+    assert _meta(lib, num_parts=0) == -3
+    assert _meta(lib, part_id=2) == -3
+    assert _meta(lib, page_size=32) == -2
+    assert _meta(lib, num_req_slots=0) == -2
+    assert _meta(lib, max_pages_per_seq=0) == -2
+    assert _meta(lib, extra_tokens=-1) == -6
+    assert _meta(lib, seq=0) == -1
+    assert _meta(lib, out=FAKE + 2) == -4
+    assert _meta(lib, err=FAKE + 1) == -4
+    assert _meta(lib, batch=0, seq=0, out=0) == 0

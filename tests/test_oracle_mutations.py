@@ -73,8 +73,18 @@ def _pin_append():
     ap.test_decode_after_append_attends_to_the_new_row()
 
 
+def _pin_meta():
+    import test_oracle_dcp_meta as dm
+    for n in (1, 2, 3, 8):
+        dm.test_local_lengths_count_the_owned_tokens(n)
+    dm.test_table_recovers_the_page_assignment()
+    dm.test_bad_requests_are_counted_and_padded()
+    for r, P in [(0, 1), (1, 2), (2, 4), (5, 8)]:
+        dm.test_decode_over_the_compact_pool_is_the_partition(r, P)
+
+
 PINS = [lambda: _pin_brute(0), lambda: _pin_brute(1), _pin_full_dims, _pin_closed_forms,
-        _pin_partitions, _pin_combine, _pin_formats, _pin_append]
+        _pin_partitions, _pin_combine, _pin_formats, _pin_append, _pin_meta]
 
 
 def pin_failures() -> int:
@@ -208,7 +218,33 @@ def _append_scale_multiplies(kv, bt, pos, new, part_id, num_parts, kv_dtype="bf1
     return _orig_append(kv, bt, pos, new, part_id, num_parts, kv_dtype, 1.0 / kv_scale, **k)
 
 
+_orig_meta = om.dcp_local_metadata
+
+
+def _meta_ignores_extra(seq_lens, idx, r2t, part_id, num_parts, extra_tokens=0, **k):
+    return _orig_meta(seq_lens, idx, r2t, part_id, num_parts, 0, **k)
+
+
+def _meta_page_of_token_i(seq_lens, idx, r2t, part_id, num_parts, extra_tokens=0, max_pages=1,
+                          pad_value=0, page_size=64):
+    g, loc, table, bad = _orig_meta(seq_lens, idx, r2t, part_id, num_parts, extra_tokens,
+                                    max_pages, pad_value, page_size)
+    r2t = np.asarray(r2t)
+    for b in range(len(loc)):
+        for i in range(-(-int(loc[b]) // page_size)):
+            if table[b, i] != pad_value and i < r2t.shape[1] and r2t[int(idx[b]), i] >= 0:
+                table[b, i] = r2t[int(idx[b]), i] // page_size
+    return g, loc, table, bad
+
+
+def _local_len_off_by_one(seq_len, num_parts, part_id):
+    return seq_len // num_parts + (1 if part_id <= seq_len % num_parts else 0)
+
+
 MUTANTS = {
+    "metadata ignores the draft tokens": ("dcp_local_metadata", _meta_ignores_extra),
+    "metadata page of token i, not 64 i": ("dcp_local_metadata", _meta_page_of_token_i),
+    "local length off by one": ("local_len", _local_len_off_by_one),
     "e4m3 encode truncates": ("f32_to_e4m3", lambda x: _e4m3_encode_variant(x, truncate=True)),
     "e4m3 ties away from zero": ("f32_to_e4m3", lambda x: _e4m3_encode_variant(x, tie_up=True)),
     "e4m3 no saturation": ("f32_to_e4m3", lambda x: _e4m3_encode_variant(x, saturate=False)),
