@@ -284,6 +284,40 @@ def decode_partial(q_bits: np.ndarray, kv_bits: np.ndarray, block_table: np.ndar
     return np.stack(outs), np.stack(lses)
 
 
+def decode_partial_causal(q_bits: np.ndarray, kv_bits: np.ndarray, block_table: np.ndarray,
+                          seq_lens, part_id: int, num_parts: int, sm_scale: float,
+                          lse_base: int = LSE_NATURAL, kv_dtype: str = "bf16",
+                          kv_scale: float = 1.0, page_size: int = 64, requests=None,
+                          d_v: int = D_V):
+    """Several query tokens per request (q_len = T: multi-token prediction /
+    target verify).  The cache already holds the T new tokens (the KV length
+    of a target-verify step is the prefix plus the draft tokens, sglang pull
+    33926's metadata code), so query token i of request b is global token
+    L_b - T + i and attends causally: to the tokens the partition owns among
+    t < L_b - T + i + 1.  A query token with none gets (0, -inf).
+
+    q_bits: uint16 [B, T, H, 576].  Returns out [B', T, H, 512] and lse
+    [B', T, H] (requested base), fp64.
+    """
+    q_bits = np.asarray(q_bits)
+    T = q_bits.shape[1]
+    rows = range(len(seq_lens)) if requests is None else list(requests)
+    outs, lses = [], []
+    for b in rows:
+        ob, lb = [], []
+        for i in range(T):
+            vis = max(0, int(seq_lens[b]) - T + i + 1)
+            toks = owned_tokens(vis, num_parts, part_id)
+            k = dequant_rows(gather_rows(kv_bits, block_table[b], toks, page_size),
+                             kv_dtype, kv_scale)
+            o, l = attend(bf16_to_f64(q_bits[b, i]), k, sm_scale, d_v)
+            ob.append(o)
+            lb.append(lse_to_base(l, lse_base))
+        outs.append(np.stack(ob))
+        lses.append(np.stack(lb))
+    return np.stack(outs), np.stack(lses)
+
+
 def decode_full(q_bits, kv_bits, block_table, seq_lens, sm_scale, lse_base=LSE_NATURAL,
                 **kw):
     """The unpartitioned result: every token < L attended (P = 1)."""

@@ -83,8 +83,17 @@ def _pin_meta():
         dm.test_decode_over_the_compact_pool_is_the_partition(r, P)
 
 
+def _pin_causal():
+    import test_oracle_causal as tc
+    tc.test_one_query_token_is_the_single_token_decode()
+    for T, P in [(2, 1), (3, 2), (4, 8), (8, 3)]:
+        tc.test_query_token_i_sees_the_first_L_minus_T_plus_i_plus_1_tokens(T, P)
+    tc.test_partitions_merge_to_the_unpartitioned_causal_result()
+    tc.test_query_tokens_that_see_nothing_are_neutral()
+
+
 PINS = [lambda: _pin_brute(0), lambda: _pin_brute(1), _pin_full_dims, _pin_closed_forms,
-        _pin_partitions, _pin_combine, _pin_formats, _pin_append, _pin_meta]
+        _pin_partitions, _pin_combine, _pin_formats, _pin_append, _pin_meta, _pin_causal]
 
 
 def pin_failures() -> int:
@@ -241,7 +250,35 @@ def _local_len_off_by_one(seq_len, num_parts, part_id):
     return seq_len // num_parts + (1 if part_id <= seq_len % num_parts else 0)
 
 
+def _causal_variant(shift=0, no_bound=False, reverse=False):
+    def f(q_bits, kv_bits, block_table, seq_lens, part_id, num_parts, sm_scale,
+          lse_base=om.LSE_NATURAL, kv_dtype="bf16", kv_scale=1.0, page_size=64, requests=None,
+          d_v=om.D_V):
+        q_bits = np.asarray(q_bits)
+        T = q_bits.shape[1]
+        rows = range(len(seq_lens)) if requests is None else list(requests)
+        outs, lses = [], []
+        for b in rows:
+            ob, lb = [], []
+            for i in range(T):
+                ii = T - 1 - i if reverse else i
+                vis = int(seq_lens[b]) if no_bound else max(0, int(seq_lens[b]) - T + ii + 1 + shift)
+                toks = om.owned_tokens(vis, num_parts, part_id)
+                k = om.dequant_rows(om.gather_rows(kv_bits, block_table[b], toks, page_size),
+                                    kv_dtype, kv_scale)
+                o, l = om.attend(om.bf16_to_f64(q_bits[b, i]), k, sm_scale, d_v)
+                ob.append(o)
+                lb.append(om.lse_to_base(l, lse_base))
+            outs.append(np.stack(ob))
+            lses.append(np.stack(lb))
+        return np.stack(outs), np.stack(lses)
+    return f
+
+
 MUTANTS = {
+    "causal bound dropped": ("decode_partial_causal", _causal_variant(no_bound=True)),
+    "causal bound one token late": ("decode_partial_causal", _causal_variant(shift=1)),
+    "query tokens in reverse order": ("decode_partial_causal", _causal_variant(reverse=True)),
     "metadata ignores the draft tokens": ("dcp_local_metadata", _meta_ignores_extra),
     "metadata page of token i, not 64 i": ("dcp_local_metadata", _meta_page_of_token_i),
     "local length off by one": ("local_len", _local_len_off_by_one),
