@@ -262,26 +262,26 @@ def decode_dcp(q, kv_pages, block_table, seq_lens, num_parts: int, sm_scale: flo
     _need(block_table, "block_table", (torch.int32,), dev)
     _need(seq_lens, "seq_lens", (torch.int32,), dev)
     d = _decode_desc(q, kv_pages, block_table, kv_scale)
-    B, H, P = d.batch, d.num_heads, int(num_parts)
+    B, T, H, P = d.batch, d.q_len, d.num_heads, int(num_parts)
     if seq_lens.numel() != B or block_table.dim() != 2 or block_table.shape[0] != B:
         raise ValueError("seq_lens / block_table do not match the batch")
     if partials is None:
-        partials = torch.empty(P, B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+        partials = torch.empty(P, B, T, H, 512, dtype=torch.bfloat16, device=dev)
     if partial_lses is None:
-        partial_lses = torch.empty(P, B, 1, H, dtype=torch.float32, device=dev)
+        partial_lses = torch.empty(P, B, T, H, dtype=torch.float32, device=dev)
     if out is None:
-        out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(B, T, H, 512, dtype=torch.bfloat16, device=dev)
     _need(partials, "partials", (torch.bfloat16,), dev)
     _need(partial_lses, "partial_lses", (torch.float32,), dev)
     _need(out, "out", (torch.bfloat16,), dev)
-    if partials.numel() != P * B * H * 512 or partial_lses.numel() != P * B * H:
-        raise ValueError("partials must be [P,B,1,H,512] and partial_lses [P,B,1,H]")
-    if out.numel() != B * H * 512:
-        raise ValueError("out must be [B,1,H,512]")
+    if partials.numel() != P * B * T * H * 512 or partial_lses.numel() != P * B * T * H:
+        raise ValueError("partials must be [P,B,q_len,H,512] and partial_lses [P,B,q_len,H]")
+    if out.numel() != B * T * H * 512:
+        raise ValueError("out must be [B,q_len,H,512]")
     if out_lse is not None:
         _need(out_lse, "out_lse", (torch.float32,), dev)
-        if out_lse.numel() != B * H:
-            raise ValueError("out_lse must be [B,1,H]")
+        if out_lse.numel() != B * T * H:
+            raise ValueError("out_lse must be [B,q_len,H]")
     if workspace is None:
         workspace = make_dcp_workspace(q, kv_pages, block_table, P, kv_scale)
     _need(workspace, "workspace", (torch.uint8,), dev)

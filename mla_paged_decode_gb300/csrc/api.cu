@@ -138,9 +138,10 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
   }
   const cuuint64_t row = cuuint64_t(mla::kDqk) * 2;
   {
-    cuuint64_t dims[2] = {cuuint64_t(mla::kDqk), cuuint64_t(d->batch) * cuuint64_t(d->num_heads)};
+    const cuuint64_t qrows = cuuint64_t(d->q_len) * cuuint64_t(d->num_heads);
+    cuuint64_t dims[2] = {cuuint64_t(mla::kDqk), cuuint64_t(d->batch) * qrows};
     cuuint64_t strides[1] = {row};
-    cuuint32_t box[2] = {64, cuuint32_t(d->num_heads < 64 ? d->num_heads : 64)};
+    cuuint32_t box[2] = {64, cuuint32_t(qrows < 64 ? qrows : 64)};
     cuuint32_t es[2] = {1, 1};
     CUresult r = enc(tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q), dims, strides,
                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -179,11 +180,14 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
 }
 
 constexpr int kSimtHeadsPerGroup = 32;
+// Query tokens per request: several (multi-token prediction / target verify)
+// only on the tensor-core path; the CUDA-core kernel takes one.
+constexpr int kMaxQLen = 16;
 
 int check_desc(const mla_decode_desc *d) {
   if (!d) return MLA_ERR_NULL;
   if (d->batch < 0 || d->num_pages < 1 || d->max_pages_per_seq < 1) return MLA_ERR_SHAPE;
-  if (d->q_len != 1) return MLA_ERR_SHAPE;
+  if (d->q_len < 1 || d->q_len > kMaxQLen) return MLA_ERR_SHAPE;
   if (d->head_dim_qk != mla::kDqk || d->head_dim_v != mla::kDv) return MLA_ERR_SHAPE;
   if (d->page_size != mla::kPage) return MLA_ERR_SHAPE;
   if (d->num_heads < 1 || d->num_heads > 128) return MLA_ERR_SHAPE;
@@ -204,8 +208,11 @@ int check_cache_desc(const mla_decode_desc *d) {
   return MLA_OK;
 }
 
+// Rows of one request: q_len query tokens x num_heads heads.
+int rows_of(const mla_decode_desc *d) { return d->q_len * d->num_heads; }
+
 int head_groups_of(const mla_decode_desc *d) {
-  return (d->num_heads + kSimtHeadsPerGroup - 1) / kSimtHeadsPerGroup;
+  return (rows_of(d) + kSimtHeadsPerGroup - 1) / kSimtHeadsPerGroup;
 }
 
 // Builds the decode parameters and enqueues the decode kernel and its split
@@ -217,8 +224,10 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
                    void *workspace, int grid, cudaStream_t s) {
   const bool tc = tensor_core_path(d, num_parts);
   if (fused && !tc) return MLA_ERR_ARG;
+  if (d->q_len > 1 && !tc) return MLA_ERR_SHAPE;
   const int per_group = tc ? kTcHeadsPerGroup : kSimtHeadsPerGroup;
-  const int groups = (d->num_heads + per_group - 1) / per_group;
+  const int rows = rows_of(d);
+  const int groups = (rows + per_group - 1) / per_group;
   const int vbatch = fused ? num_parts * d->batch : d->batch;
   mla::DecodeParams p;
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -230,9 +239,11 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
   p.ws = static_cast<unsigned char *>(workspace);
   p.wl = mla::workspace_layout(vbatch * groups, grid);
   p.batch = vbatch;
-  p.heads = d->num_heads;
+  p.heads = rows;
   p.head_groups = groups;
   p.heads_per_group = per_group;
+  p.q_len = d->q_len;
+  p.q_heads = d->num_heads;
   p.num_pages = d->num_pages;
   p.max_pages = d->max_pages_per_seq;
   p.part_id = fused ? 0 : part_id;
@@ -248,7 +259,7 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
     CUtensorMap tm_q, tm_kv;
     int st = make_tensor_maps(q, kv_pages, d, part_id, num_parts, fused, &tm_q, &tm_kv);
     if (st != MLA_OK) return st;
-    const int h = d->num_heads < kTcHeadsPerGroup ? d->num_heads : kTcHeadsPerGroup;
+    const int h = rows < kTcHeadsPerGroup ? rows : kTcHeadsPerGroup;
     const int npv = ((h + 15) / 16) * 16;
     e = mla::launch_decode_tc(p, npv, h, 8 / num_parts, tm_q, tm_kv, grid, s);
   } else {
@@ -267,7 +278,7 @@ const char *mla_status_string(int status) {
   switch (status) {
     case MLA_OK: return "ok";
     case MLA_ERR_NULL: return "a required pointer is NULL";
-    case MLA_ERR_SHAPE: return "unsupported shape (q_len must be 1, Dqk 576, Dv 512, page 64, heads 1..128)";
+    case MLA_ERR_SHAPE: return "unsupported shape (q_len 1..16, and 1 unless num_parts divides 8; Dqk 576, Dv 512, page 64, heads 1..128)";
     case MLA_ERR_PARTITION: return "bad partition (need num_parts >= 1 and 0 <= part_id < num_parts)";
     case MLA_ERR_ALIGN: return "misaligned pointer (16 B for tensors, 256 B for the workspace)";
     case MLA_ERR_WORKSPACE: return "workspace too small";
@@ -301,6 +312,7 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
   int st = check_desc(d);
   if (st != MLA_OK) return st;
   if (num_parts < 1 || part_id < 0 || part_id >= num_parts) return MLA_ERR_PARTITION;
+  if (d->q_len > 1 && !tensor_core_path(d, num_parts)) return MLA_ERR_SHAPE;
   if (lse_base != MLA_LSE_NATURAL && lse_base != MLA_LSE_BASE2) return MLA_ERR_ARG;
   if (!std::isfinite(sm_scale)) return MLA_ERR_ARG;
   if (d->batch == 0) return MLA_OK;
@@ -343,7 +355,8 @@ int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_tab
   if (lse_base != MLA_LSE_NATURAL && lse_base != MLA_LSE_BASE2) return MLA_ERR_ARG;
   if (!std::isfinite(sm_scale)) return MLA_ERR_ARG;
   if (d->batch == 0) return MLA_OK;
-  if ((long long)num_parts * d->batch * d->num_heads > (1LL << 30)) return MLA_ERR_SHAPE;
+  if ((long long)num_parts * d->batch * rows_of(d) > (1LL << 30)) return MLA_ERR_SHAPE;
+  if (d->q_len > 1 && !tensor_core_path(d, num_parts)) return MLA_ERR_SHAPE;
   if (!q || !kv_pages || !block_table || !seq_lens || !partials || !partial_lses || !out ||
       !workspace)
     return MLA_ERR_NULL;
@@ -356,7 +369,7 @@ int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_tab
   if (workspace_bytes < mla_decode_dcp_workspace_size(d, num_parts, f.sms))
     return MLA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t rows = size_t(d->batch) * d->num_heads;
+  const size_t rows = size_t(d->batch) * rows_of(d);
   if (tensor_core_path(d, num_parts)) {
     // every partition in one decode launch (and one split merge)
     st = enqueue_decode(q, kv_pages, block_table, seq_lens, 0, num_parts, true, sm_scale,

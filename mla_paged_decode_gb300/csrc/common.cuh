@@ -58,6 +58,10 @@ struct DecodeParams {
   // partition bv / req_batch; out / lse are then [P, B, ...].  Otherwise
   // fused = 0 and req_batch = batch.
   int fused = 0, req_batch = 0;
+  // Query tokens per request (tensor-core kernel only; 1 elsewhere): the
+  // `heads` rows of a request are then q_len x q_heads, row i * q_heads + h
+  // for query token i, and token i of T sees the global tokens t < L - T + i + 1.
+  int q_len = 1, q_heads = 0;
   int kv_e4m3;
   float kv_scale;             // 1 for bf16
   float score_scale_log2;     // sm_scale * log2(e): scores kept in the base-2 domain
@@ -91,11 +95,29 @@ __device__ __forceinline__ int checked_len(const DecodeParams &p, int b, int *er
   return L;
 }
 
-__device__ __forceinline__ int request_tiles(const DecodeParams &p, int v) {
+// Global tokens visible to row `row` of a request of length L, and to the
+// rows of head group g (its last row sees the most).
+__device__ __forceinline__ int row_len(const DecodeParams &p, int L, int row) {
+  return p.q_len <= 1 ? L : max(0, L - p.q_len + row / p.q_heads + 1);
+}
+__device__ __forceinline__ int group_len(const DecodeParams &p, int L, int g) {
+  return p.q_len <= 1 ? L : row_len(p, L, min(p.heads, (g + 1) * p.heads_per_group) - 1);
+}
+
+// Owned tokens of virtual request v (its group's widest row).
+// MULTI: requests may carry several query tokens (a compile-time switch, so
+// that single-token kernels keep the plain length rule in their code).
+template <bool MULTI = false>
+__device__ __forceinline__ int request_len(const DecodeParams &p, int v, int *err) {
   int bv = v / p.head_groups;
-  int L = checked_len(p, req_of(p, bv), nullptr);
-  int n = local_len(L, p.num_parts, part_of(p, bv));
-  return (n + kTile - 1) / kTile;
+  int L = checked_len(p, req_of(p, bv), err);
+  if (MULTI) L = group_len(p, L, v % p.head_groups);
+  return local_len(L, p.num_parts, part_of(p, bv));
+}
+
+template <bool MULTI = false>
+__device__ __forceinline__ int request_tiles(const DecodeParams &p, int v) {
+  return (request_len<MULTI>(p, v, nullptr) + kTile - 1) / kTile;
 }
 
 // ---------------------------------------------------------------- split schedule
@@ -137,12 +159,13 @@ __device__ __forceinline__ long long request_cost(int tiles) {
 
 // Block-wide: computes this CTA's range.  All threads must call it.
 // `scratch` needs blockDim.x / 32 + 1 long longs of shared memory.
+template <bool MULTI = false>
 __device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long long *scratch) {
   const int V = p.batch * p.head_groups;
   const int tid = threadIdx.x, nw = blockDim.x / 32, lane = tid & 31, warp = tid >> 5;
   // pass 1: total cost
   long long mine = 0;
-  for (int v = tid; v < V; v += blockDim.x) mine += request_cost(request_tiles(p, v));
+  for (int v = tid; v < V; v += blockDim.x) mine += request_cost(request_tiles<MULTI>(p, v));
   for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
   if (lane == 0) scratch[warp] = mine;
   __syncthreads();
@@ -168,7 +191,7 @@ __device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long lon
   long long base = 0;
   for (int v0 = 0; v0 < V; v0 += blockDim.x) {
     int v = v0 + tid;
-    const int tiles = v < V ? request_tiles(p, v) : 0;
+    const int tiles = v < V ? request_tiles<MULTI>(p, v) : 0;
     const long long cst = request_cost(tiles);
     long long incl = cst;
     for (int o = 1; o < 32; o <<= 1) {

@@ -99,7 +99,7 @@ static_assert(sizeof(TcMisc) + 1024 <= tc::kSmemBytes - tc::kOffMisc, "shared me
 // The requests (and tile ranges) this CTA owns, in order; every role walks it.
 // FUSED: all partitions in one launch (output row b = partition * B + input
 // request); otherwise one partition, p.part_id, and row b is request b.
-template <bool FUSED>
+template <bool FUSED, bool MULTI>
 struct Walk {
   const DecodeParams &p;
   const CtaRange &r;
@@ -110,7 +110,7 @@ struct Walk {
       : p(p_), r(r_), V(p_.batch * p_.head_groups), v(r_.v_begin), pv(r_.p_begin) {}
   __device__ bool next() {
     while (v < V && pv < r.end) {
-      tiles = request_tiles(p, v);
+      tiles = request_tiles<MULTI>(p, v);
       if (tiles == 0) { ++v; continue; }
       t0 = max(r.start, pv) - pv;
       t1 = min(r.end, pv + tiles) - pv;
@@ -119,7 +119,8 @@ struct Walk {
       rb = FUSED ? b % p.req_batch : b;
       part = FUSED ? b / p.req_batch : p.part_id;
       pc = FUSED ? part : 0;
-      n = local_len(checked_len(p, rb, nullptr), p.num_parts, part);
+      n = MULTI ? local_len(group_len(p, checked_len(p, rb, nullptr), g), p.num_parts, part)
+                : local_len(checked_len(p, rb, nullptr), p.num_parts, part);
       return true;
     }
     return false;
@@ -128,9 +129,9 @@ struct Walk {
 };
 
 // One position in the walk: request + tile.
-template <bool FUSED>
+template <bool FUSED, bool MULTI>
 struct TileCursor {
-  Walk<FUSED> w;
+  Walk<FUSED, MULTI> w;
   long long t;
   bool live;
   __device__ TileCursor(const DecodeParams &p, const CtaRange &r) : w(p, r), t(0) {
@@ -164,7 +165,7 @@ __device__ __forceinline__ void tile_pages(const DecodeParams &p, int part, long
 
 constexpr int kPrefetchAhead = 2;  // tiles whose pages are pulled into L2 ahead of the stage
 
-template <bool F8, bool FUSED>
+template <bool F8, bool FUSED, bool MULTI>
 __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                             uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
                             int *err) {
@@ -188,7 +189,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   // kPrefetchAhead tiles early, when the page is prefetched into L2 (the
   // 129 MB L2 gives the two shared-memory stages more HBM requests in
   // flight), and carried in `ring` until its tile is loaded.
-  TileCursor<FUSED> ahead(p, r);
+  TileCursor<FUSED, MULTI> ahead(p, r);
   auto next_ahead = [&]() {
     int pg = -1;
     if (ahead.live) {
@@ -218,7 +219,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 #pragma unroll
   for (int i = 0; i < kPrefetchAhead; ++i) ring[i] = next_ahead();
 
-  TileCursor<FUSED> cur(p, r);
+  TileCursor<FUSED, MULTI> cur(p, r);
   while (cur.live) {
     if (cur.first()) {
       checked_len(p, cur.w.rb, err);
@@ -290,7 +291,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 
 // Descriptors: an offset is added to the encoded start address (bits 0..13,
 // address >> 4), which never carries because shared addresses stay below 256 KB.
-template <bool F8, bool FUSED>
+template <bool F8, bool FUSED, bool MULTI>
 __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                          uint32_t sKv, uint32_t tmem, int chain, int *err) {
   using namespace tc;
@@ -305,7 +306,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
   uint32_t s_it = 0, q_it = 0;
   bool ok = true;
-  for (TileCursor<FUSED> sc(p, r); sc.live; sc.step(), ++s_it) {
+  for (TileCursor<FUSED, MULTI> sc(p, r); sc.live; sc.step(), ++s_it) {
     const int st = s_it & 1;
     const uint32_t ph = (s_it >> 1) & 1;
     if (!mbar_wait(bar_addr(kv_ready[st]), ph, abort, kTimeoutNs)) { ok = false; break; }
@@ -334,7 +335,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
 
 // O^T(chunk c) (+)= V^T(tile) P^T over ceil(nv/16) steps of 16 tokens; issuer
 // `half` takes value chunks 2 half and 2 half + 1.
-template <bool F8, bool FUSED>
+template <bool F8, bool FUSED, bool MULTI>
 __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
                           uint32_t tmem, int half, int *err) {
   using namespace tc;
@@ -346,7 +347,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
   uint32_t pv_it = 0, o_it = 0;
   bool ok = true;
-  for (TileCursor<FUSED> pc(p, r); pc.live; pc.step(), ++pv_it) {
+  for (TileCursor<FUSED, MULTI> pc(p, r); pc.live; pc.step(), ++pv_it) {
     if (!mbar_wait(bar_addr(m.p_full[pv_it & 1]), (pv_it >> 1) & 1, abort, kTimeoutNs)) {
       ok = false;
       break;
@@ -444,7 +445,7 @@ __device__ __noinline__ void zero_value_tail(unsigned char *stage, int nv, int g
   }
 }
 
-template <bool F8, bool FUSED>
+template <bool F8, bool FUSED, bool MULTI>
 __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
                            unsigned char *smem, uint32_t tmem, int *err) {
   using namespace tc;
@@ -462,9 +463,18 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
   uint32_t kv_it = 0, p_it = 0, o_it = 0;
   bool ok = true;
 
-  Walk<FUSED> w(p, r);
+  Walk<FUSED, MULTI> w(p, r);
   for (; ok && w.next(); w.advance()) {
     const int hn = min(kHeads, p.heads - w.g * kHeads);
+    // owned tokens each of this lane's two rows sees (all w.n unless a request
+    // carries several query tokens, each with its own causal bound)
+    int nrow[2] = {w.n, w.n};
+    if (MULTI) {  // query token i of T sees the global tokens t < L - T + i + 1
+      const int L = checked_len(p, w.rb, nullptr);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        nrow[h] = local_len(row_len(p, L, w.g * kHeads + row[h]), p.num_parts, w.part);
+    }
     float mrun[2] = {-INFINITY, -INFINITY};  // running max (base-2 units) of each head
     float ellp[2] = {0.f, 0.f};              // this lane's share of each head's sum
     for (long long t = w.t0; t < w.t1; ++t, ++kv_it, ++p_it) {
@@ -496,12 +506,13 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_addr(m.s_free[s]));
       }
-      if (nv < kTile) {  // the tile's tail: tokens past the request's end
+      const int nv0 = MULTI ? nrow[0] - int(t) * kTile : nv, nv1 = MULTI ? nrow[1] - int(t) * kTile : nv;
+      if ((MULTI ? min(nv0, nv1) : nv) < kTile) {  // the tile's tail: tokens past a row's last visible one
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const int tok = 8 * (k >> 1) + pair;
-          xp[k].x = tok < nv ? xp[k].x : -INFINITY;
-          xp[k].y = tok + 1 < nv ? xp[k].y : -INFINITY;
+          const int tok = 8 * (k >> 1) + pair, lim = (k & 1) ? nv1 : nv0;
+          xp[k].x = tok < lim ? xp[k].x : -INFINITY;
+          xp[k].y = tok + 1 < lim ? xp[k].y : -INFINITY;
         }
       }
       float tmax[2];
@@ -564,7 +575,9 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
       for (int h = 0; h < 2; ++h) {
         unsigned char *prow = smem + kOffKv + s * kStageBytes + (row[h] >> 3) * kAtomBytes + kPOff +
                               (row[h] & 7) * 128 + (lane & 3) * 4;
-        const float2 c2 = make_float2(cs, cs), m2 = make_float2(-mnew[h], -mnew[h]);
+        // a row that has seen no token yet keeps a -inf max: its P is 0
+        const float mref = MULTI && mnew[h] == -INFINITY ? 0.f : mnew[h];
+        const float2 c2 = make_float2(cs, cs), m2 = make_float2(-mref, -mref);
         float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -605,9 +618,9 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
       ell[h] += __shfl_xor_sync(0xffffffffu, ell[h], 2);
     }
     // ---- epilogue of this CTA's share of request v
-    if ((lane & 3) == 0) {  // per-head output scale: kv_scale / sum
-      m.ell[row[0]] = p.kv_scale / ell[0];
-      m.ell[row[1]] = p.kv_scale / ell[1];
+    if ((lane & 3) == 0) {  // per-head output scale: kv_scale / sum (0 for a row that saw nothing)
+      m.ell[row[0]] = !MULTI || ell[0] > 0.f ? p.kv_scale / ell[0] : 0.f;
+      m.ell[row[1]] = !MULTI || ell[1] > 0.f ? p.kv_scale / ell[1] : 0.f;
     }
     const bool got_o = mbar_wait(bar_addr(m.o_full), o_it & 1, abort, kTimeoutNs);
     if (!named_sync_and(2, 128, got_o)) { ok = false; break; }
@@ -772,7 +785,7 @@ __device__ __noinline__ bool convert_q(const TcParams &tp, TcMisc &m, unsigned c
   return true;
 }
 
-template <bool FUSED>
+template <bool FUSED, bool MULTI>
 __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r, TcMisc &m,
                                            unsigned char *smem, int *err) {
   using namespace tc;
@@ -792,7 +805,7 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
   uint32_t kv_it = 0, q_it = 0;
   float qinv = 1.f;
   bool ok = true;
-  for (TileCursor<FUSED> c(p, r); c.live; c.step(), ++kv_it) {
+  for (TileCursor<FUSED, MULTI> c(p, r); c.live; c.step(), ++kv_it) {
     if (c.first()) {
       if (!convert_q(tp, m, smem, c.w.g, q_it, &qinv)) { ok = false; break; }
       ++q_it;
@@ -857,7 +870,7 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
 
 // ------------------------------------------------------------------ kernel
 
-template <bool F8, bool FUSED>
+template <bool F8, bool FUSED, bool MULTI>
 __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     decode_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_kv) {
@@ -908,8 +921,8 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     tma_prefetch_desc(&tm_kv);
   }
   fence_proxy_async_smem();
-  write_empty_requests(p);
-  cta_schedule(p, &m.range, m.scratch);
+  write_empty_requests<MULTI>(p);
+  cta_schedule<MULTI>(p, &m.range, m.scratch);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -918,15 +931,15 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
 
   if (r.start < r.end) {
     if (warp == 0) {
-      tc_producer<F8, FUSED>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
+      tc_producer<F8, FUSED, MULTI>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
     } else if (warp == 1 || warp == 2) {
-      if (lane == 0) tc_mma_s<F8, FUSED>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
+      if (lane == 0) tc_mma_s<F8, FUSED, MULTI>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
     } else if (warp == 3 || warp == 8) {
-      if (lane == 0) tc_mma_pv<F8, FUSED>(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
+      if (lane == 0) tc_mma_pv<F8, FUSED, MULTI>(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
     } else if (warp < 8) {
-      tc_softmax<F8, FUSED>(tp, r, m, smem, tmem, err);
+      tc_softmax<F8, FUSED, MULTI>(tp, r, m, smem, tmem, err);
     } else if (F8) {
-      tc_convert<FUSED>(tp, r, m, smem, err);
+      tc_convert<FUSED, MULTI>(tp, r, m, smem, err);
     }
   }
   tc_fence_before();
@@ -941,21 +954,29 @@ int tc_smem_bytes() { return tc::kSmemBytes; }
 
 cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream);
 
-template <bool F8, bool FUSED>
+template <bool F8, bool FUSED, bool MULTI>
 static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
                              int grid, cudaStream_t stream) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<F8, FUSED>,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<F8, FUSED, MULTI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          tc::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  decode_tc_kernel<F8, FUSED><<<grid, tc_threads<F8>(), tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
+  decode_tc_kernel<F8, FUSED, MULTI>
+      <<<grid, tc_threads<F8>(), tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
   return cudaGetLastError();
+}
+
+template <bool F8, bool FUSED>
+static cudaError_t launch_tc_q(const TcParams &tp, const CUtensorMap &tm_q,
+                               const CUtensorMap &tm_kv, int grid, cudaStream_t stream) {
+  return tp.p.q_len > 1 ? launch_tc<F8, FUSED, true>(tp, tm_q, tm_kv, grid, stream)
+                        : launch_tc<F8, FUSED, false>(tp, tm_q, tm_kv, grid, stream);
 }
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
@@ -967,10 +988,10 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int gro
   tp.q_rows = q_rows;
   tp.groups_per_page = groups_per_page;
   const bool f8 = p.kv_e4m3 != 0, fused = p.fused != 0;
-  cudaError_t e = f8 ? (fused ? launch_tc<true, true>(tp, tm_q, tm_kv, grid, stream)
-                              : launch_tc<true, false>(tp, tm_q, tm_kv, grid, stream))
-                     : (fused ? launch_tc<false, true>(tp, tm_q, tm_kv, grid, stream)
-                              : launch_tc<false, false>(tp, tm_q, tm_kv, grid, stream));
+  cudaError_t e = f8 ? (fused ? launch_tc_q<true, true>(tp, tm_q, tm_kv, grid, stream)
+                              : launch_tc_q<true, false>(tp, tm_q, tm_kv, grid, stream))
+                     : (fused ? launch_tc_q<false, true>(tp, tm_q, tm_kv, grid, stream)
+                              : launch_tc_q<false, false>(tp, tm_q, tm_kv, grid, stream));
   return e == cudaSuccess ? launch_split_merge(p, grid, stream) : e;
 }
 

@@ -18,7 +18,7 @@ namespace mla {
 constexpr int kMergeWarps = 4;  // heads per CTA
 constexpr int kMergeBatch = 2;  // splits whose loads are in flight together
 
-__global__ void __launch_bounds__(kMergeWarps * 32, 8) split_merge_kernel(DecodeParams p, int grid) {
+__global__ void __launch_bounds__(kMergeWarps * 32, 7) split_merge_kernel(DecodeParams p, int grid) {
   // launched as a programmatic dependent of the decode kernel: wait until its
   // grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) split_merge_kernel(Decode
   // both loads in flight together: the record is only current for a request
   // with tiles (an empty one keeps whatever an earlier call left)
   const int4 info = info_ptr(p)[v];
-  if (request_tiles(p, v) == 0) return;
+  if ((p.q_len > 1 ? request_tiles<true>(p, v) : request_tiles<false>(p, v)) == 0) return;
   const int ns = info.y;
   // split k > 0 lives in slot 2 (first + k): never past the 2 x grid slots
   if (ns <= 1 || info.x < 0 || info.x + ns > grid) return;
@@ -53,8 +53,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) split_merge_kernel(Decode
   float mx = -INFINITY;
   for (int k = lane; k < ns; k += 32) mx = fmaxf(mx, lse_of(k));
   for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  // a query row that sees no token in any split (several query tokens per
+  // request) has mx = -inf: every weight is then 0 and the row the neutral pair
+  const float mref = mx == -INFINITY ? 0.f : mx;
   float sum = 0.f;
-  for (int k = lane; k < ns; k += 32) sum += exp2f(lse_of(k) - mx);
+  for (int k = lane; k < ns; k += 32) sum += exp2f(lse_of(k) - mref);
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
 
   float4 acc[4];
@@ -70,7 +73,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) split_merge_kernel(Decode
     }
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
-      const float w = k0 + u < ns ? exp2f(lse_of(k0 + u) - mx) : 0.f;
+      const float w = k0 + u < ns ? exp2f(lse_of(k0 + u) - mref) : 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc[i].x += w * x[u][i].x; acc[i].y += w * x[u][i].y;
@@ -78,7 +81,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) split_merge_kernel(Decode
       }
     }
   }
-  const float inv = 1.f / sum;
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
   uint32_t pk[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -91,7 +94,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) split_merge_kernel(Decode
   uint4 *dst = reinterpret_cast<uint4 *>(p.out + row * kDv + 16 * lane);
   dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-  if (lane == 0) p.lse[row] = lse_out(p, mx + log2f(sum));
+  if (lane == 0) p.lse[row] = sum > 0.f ? lse_out(p, mref + log2f(sum)) : -INFINITY;
 }
 
 cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream) {

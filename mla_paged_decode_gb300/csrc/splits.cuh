@@ -46,13 +46,13 @@ __device__ __forceinline__ float lse_out(const DecodeParams &p, float lse2) {
 
 // The neutral pair (0, -inf) for every virtual request with no owned token.
 // Virtual request v is handled by CTA v mod gridDim.x.  Block-wide.
+template <bool MULTI = false>
 __device__ inline void write_empty_requests(const DecodeParams &p) {
   const int V = p.batch * p.head_groups;
   int *err = error_word(p);
   for (int v = blockIdx.x; v < V; v += gridDim.x) {
     int b = v / p.head_groups, g = v % p.head_groups;  // b: output row
-    int L = checked_len(p, req_of(p, b), threadIdx.x == 0 ? err : nullptr);
-    if (local_len(L, p.num_parts, part_of(p, b)) != 0) continue;
+    if (request_len<MULTI>(p, v, threadIdx.x == 0 ? err : nullptr) != 0) continue;
     int h0 = g * p.heads_per_group;
     int hn = min(p.heads_per_group, p.heads - h0);
     uint4 *dst = reinterpret_cast<uint4 *>(p.out + (size_t(b) * p.heads + h0) * kDv);

@@ -67,7 +67,7 @@ def _partial(lib, d, *, part_id=0, num_parts=1, lse_base=0, sm_scale=0.1, q=FAKE
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(q_len=2), -2), (dict(q_len=0), -2), (dict(head_dim_qk=512), -2),
+    (dict(q_len=17), -2), (dict(q_len=0), -2), (dict(head_dim_qk=512), -2),
     (dict(head_dim_v=576), -2), (dict(page_size=32), -2), (dict(num_heads=0), -2),
     (dict(num_heads=129), -2), (dict(num_pages=0), -2), (dict(max_pages_per_seq=0), -2),
     (dict(batch=-1), -2), (dict(kv_dtype=7), -6), (dict(kv_dtype=1, kv_scale=0.0), -6),
@@ -103,7 +103,7 @@ def test_workspace_size_is_sane(lib):
     d = _desc(batch=64, num_heads=64)
     n = lib.mla_decode_workspace_size(ctypes.byref(d), 152)
     assert n > 0 and n % 256 == 0
-    assert lib.mla_decode_workspace_size(ctypes.byref(_desc(q_len=2)), 152) == 0
+    assert lib.mla_decode_workspace_size(ctypes.byref(_desc(q_len=17)), 152) == 0
     assert lib.mla_decode_workspace_size(None, 152) == 0
     more = lib.mla_decode_workspace_size(ctypes.byref(d), 304)
     assert more > n
@@ -178,7 +178,7 @@ def _dcp(lib, d, *, num_parts=2, partials=FAKE, out=FAKE, out_lse=None, ws=FAKE,
 
 
 def test_dcp_rejects_bad_arguments(lib):
-    assert _dcp(lib, _desc(q_len=2)) == -2
+    assert _dcp(lib, _desc(q_len=17)) == -2
     assert _dcp(lib, _desc(), num_parts=0) == -3
     assert _dcp(lib, _desc(), num_parts=257) == -3
     assert _dcp(lib, None) == -1
@@ -216,3 +216,9 @@ def test_dcp_metadata_rejects_bad_arguments(lib):
     assert _meta(lib, out=FAKE + 2) == -4
     assert _meta(lib, err=FAKE + 1) == -4
     assert _meta(lib, batch=0, seq=0, out=0) == 0
+
+
+def test_several_query_tokens_need_the_tensor_core_path(lib):
+    # num_parts = 3 runs the CUDA-core kernel, which takes one query token
+    assert _partial(lib, _desc(q_len=2), part_id=0, num_parts=3) == -2
+    assert _dcp(lib, _desc(q_len=4), num_parts=3) == -2

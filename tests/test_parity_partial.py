@@ -184,13 +184,15 @@ def test_bounds_are_checked_in_the_kernel():
     assert mla.check_workspace(ws) == 0
 
 
-def test_multi_token_query_is_rejected():
+def test_multi_token_query_is_rejected_off_the_tensor_core_path():
+    """Several query tokens run on the tensor-core kernel only (P | 8); with
+    P = 3 the call is refused before launching."""
     case = workloads.config_small(device="cuda")
     q2 = torch.zeros(1, 2, 16, 576, dtype=torch.bfloat16, device="cuda")
     out = torch.empty(1, 2, 16, 512, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(1, 2, 16, dtype=torch.float32, device="cuda")
     with pytest.raises(mla.MlaError) as e:
-        mla.decode_partial(q2, case.kv_pages, case.block_table, case.seq_lens, 0, 1,
+        mla.decode_partial(q2, case.kv_pages, case.block_table, case.seq_lens, 0, 3,
                            case.sm_scale, 0, out, lse, workspace=torch.zeros(
                                1 << 20, dtype=torch.uint8, device="cuda"))
     assert e.value.status == -2

@@ -114,7 +114,7 @@ def make_decode_case(name: str, heads: int, seq_lens: list[int], *,
                      pool_pages: int | None = None, kv_dtype: str = "bf16",
                      num_parts: int = 1, sm_scale: float = SM_SCALE_192,
                      seed: int = 0, device="cpu", tail_poison: bool = False,
-                     pad_value: int = 0) -> DecodeCase:
+                     pad_value: int = 0, q_len: int = 1) -> DecodeCase:
     """Build a paged decode batch.
 
     Each request's ceil(L/64) pages are drawn without replacement from a
@@ -122,7 +122,8 @@ def make_decode_case(name: str, heads: int, seq_lens: list[int], *,
     pages.  ``tail_poison`` fills the unused rows of every request's last page
     (and every page no request owns) with NaN bit patterns: a correct kernel
     never lets them reach its output.  Block-table entries past a request's
-    last page hold ``pad_value``.
+    last page hold ``pad_value``.  ``q_len`` query tokens per request (the
+    last q_len tokens of each length) give q [B, q_len, H, 576].
     """
     batch = len(seq_lens)
     need = [pages_for(L) for L in seq_lens]
@@ -136,7 +137,7 @@ def make_decode_case(name: str, heads: int, seq_lens: list[int], *,
         bt[b, :n] = perm[off:off + n].to(torch.int32)
         off += n
 
-    q = _randn_bf16((batch, 1, heads, D_QK), _gen(seed, "q", device), device)
+    q = _randn_bf16((batch, q_len, heads, D_QK), _gen(seed, "q", device), device)
     if kv_dtype == "bf16":
         kv = _randn_bf16((num_pages, PAGE_SIZE, D_QK), _gen(seed, "kv", device), device)
         kv_scale = 1.0
