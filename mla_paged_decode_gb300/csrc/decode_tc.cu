@@ -1,983 +1,17 @@
-// Tensor-core decode kernel for sm_103a: one CTA per SM walks its stream-K
-// range of 64-token tiles; TMA stages the partition's KV rows, tcgen05 MMAs
-// compute S = Q K^T (heads as M = 64) and O^T = V^T P^T (value dims as M =
-// 128, heads as N) with fp32 accumulators in TMEM, and a warpgroup runs the
-// online softmax between them.
-//
-// Roles (288 threads):
-//   warp 0          TMA producer: Q of each request (9 boxes of 64 dims) and,
-//                   per tile, one 4-D box per page holding the 64/P rows the
-//                   partition owns (lane k: page k), into a [atom][dim block]
-//                   [8 rows][128 B] swizzled layout that serves both MMAs.
-//   warp 1          TMEM owner (alloc/free).
-//   warps 1, 2      lane 0 issues half of the score MMAs (one accumulator each).
-//   warps 3, 8      lane 0 issues the PV MMAs of two of the four value chunks.
-//   warps 4..7      softmax and epilogue.  The S accumulator (M = 64) puts
-//                   head 16q + i in TMEM lane 32q + i (i < 16); read with the
-//                   16x256b shape, each lane of warp q gets 2 heads x 16 of the
-//                   64 tokens.  For the epilogue every thread owns TMEM lane
-//                   32q + lane of O^T: one value dimension.
-//
-// e4m3 caches (the same kernel with F8 = true, 384 threads): the producer
-// lands each owned fp8 row (576 B) in the upper half of its stage, and
-// warps 9..11 expand them in place into the same swizzled layout as f16 (an
-// exact conversion), converting the request's Q to f16 as well with one
-// power-of-two scale that keeps its largest element in [2^14, 2^15); the
-// MMAs then run with f16 operands, P is written as f16, and the scores carry
-// sm_scale * kv_scale / (that power of two).
-//
-// Pipeline per tile i (stage / S buffer i mod 2): producer -> kv_full ->
-// MMA S_i (36 MMAs, two interleaved accumulators so consecutive MMAs are
-// independent) -> s_full -> softmax reads S_i, frees it (s_free), waits for
-// PV_{i-1} (p_free), rescales O^T only when some head's running max grew by
-// more than 2^8, writes P_i (bf16) -> p_full -> MMA PV_i (4 independent
-// value-dim chunks) -> kv_empty + p_free.  The score issuers start S_{i+1} as
-// soon as tile i+1 lands, so the score MMAs of the next tile overlap this
-// tile's softmax, and the producer keeps the pages of the tile two ahead
-// streaming into L2.
-#include "common.cuh"
-#include "sm100.cuh"
-#include "splits.cuh"
+// Host entry of the tensor-core decode partial: picks the variant for the
+// cache dtype and queues the split merge behind it.  The kernel and its
+// variants are in decode_tc.cuh; the bf16 and e4m3 variants compile in
+// decode_tc_bf16.cu and decode_tc_e4m3.cu, side by side.
+#include "decode_tc.cuh"
 
 namespace mla {
-using namespace sm100;
 
-namespace tc {
-constexpr int kThreads = 288;                // bf16 cache
-constexpr int kThreadsF8 = 384;              // e4m3 cache: + 3 converter warps
-constexpr int kConvWarp0 = 9;
-constexpr int kConvThreads = 96;
-constexpr int kHeads = 64;                   // heads per virtual request (M of S)
-constexpr int kKb = kDqk / 64;               // 9 blocks of 64 bf16 = 128 B
-constexpr int kQBytes = kKb * 64 * 128;      // [kb][64 rows][128 B]
-constexpr int kAtomBytes = kKb * 1024;       // 8 tokens x 576 dims: [kb][8][128 B]
-constexpr int kStageBytes = 8 * kAtomBytes;  // 64 tokens
-// P [64 heads][64 tokens] bf16 reuses the rope block (dims 512..575) of the
-// tile's own stage, dead once S is computed: atom a at a * kAtomBytes + kPOff.
-constexpr int kPOff = 8 * 1024;
-constexpr int kOffQ = 0;
-constexpr int kOffKv = kOffQ + kQBytes;
-constexpr int kOffMisc = kOffKv + 2 * kStageBytes;
-constexpr int kSmemBytes = 232448;           // per-block maximum on sm_100 parts
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;                // O^T chunk c: columns [64c, 64c + npv)
-constexpr uint32_t kColS = 256;              // S(buffer s, chain k): 256 + 64 (2s + k)
-constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr uint64_t kDrainNs = 200000000ull;
-constexpr float kRescaleThreshold = 8.f;     // base-2 units
-constexpr int kRawOff = kStageBytes / 2;     // e4m3: raw [64 rows][576 B] in the stage's upper half
-constexpr int kRawRow = kDqk;                // bytes of one fp8 row
-}  // namespace tc
-
-struct TcParams {
-  DecodeParams p;
-  int npv;              // N of the PV MMA: heads rounded up to 16 (16..64)
-  int q_rows;           // rows of one Q box: min(64, H)
-  int groups_per_page;  // 8-row atoms one page holds for this partition: 8 / P
-};
-
-template <bool F8>
-constexpr int tc_threads() { return F8 ? tc::kThreadsF8 : tc::kThreads; }
-
-struct TcMisc {
-  uint64_t kv_full[2], kv_empty[2], q_full, q_empty, s_full[2], s_free[2];
-  uint64_t p_full[2], p_free, o_full, o_free, drain;
-  uint64_t kv_conv[2], q_ready;  // e4m3 only: stage / Q expanded to f16
-  uint32_t tmem_base;
-  int abort;
-  float alpha[2][64];
-  float ell[64];
-  float tscale[2];               // e4m3 only: score scale (base 2) of the tile in each stage
-  uint32_t vote[2][4];           // softmax: per-warp flags of the tile, by tile parity
-  alignas(16) unsigned char stage_out[4][2048];  // epilogue: per-warp transpose buffer
-  uint32_t conv_max[4];
-  CtaRange range;
-  long long scratch[tc::kThreadsF8 / 32 + 1];
-};
-static_assert(sizeof(TcMisc) + 1024 <= tc::kSmemBytes - tc::kOffMisc, "shared memory budget");
-
-// The requests (and tile ranges) this CTA owns, in order; every role walks it.
-// FUSED: all partitions in one launch (output row b = partition * B + input
-// request); otherwise one partition, p.part_id, and row b is request b.
-template <bool FUSED, bool MULTI>
-struct Walk {
-  const DecodeParams &p;
-  const CtaRange &r;
-  int V, v, b, g, n, tiles;
-  int rb, part, pc;  // input request of output row b, its partition, the map's partition coordinate
-  long long pv, t0, t1;
-  __device__ Walk(const DecodeParams &p_, const CtaRange &r_)
-      : p(p_), r(r_), V(p_.batch * p_.head_groups), v(r_.v_begin), pv(r_.p_begin) {}
-  __device__ bool next() {
-    while (v < V && pv < r.end) {
-      tiles = request_tiles<MULTI>(p, v);
-      if (tiles == 0) { ++v; continue; }
-      t0 = max(r.start, pv) - pv;
-      t1 = min(r.end, pv + tiles) - pv;
-      b = v / p.head_groups;
-      g = v % p.head_groups;
-      rb = FUSED ? b % p.req_batch : b;
-      part = FUSED ? b / p.req_batch : p.part_id;
-      pc = FUSED ? part : 0;
-      n = MULTI ? local_len(group_len(p, checked_len(p, rb, nullptr), g), p.num_parts, part)
-                : local_len(checked_len(p, rb, nullptr), p.num_parts, part);
-      return true;
-    }
-    return false;
-  }
-  __device__ void advance() { pv += request_cost(tiles); ++v; }
-};
-
-// One position in the walk: request + tile.
-template <bool FUSED, bool MULTI>
-struct TileCursor {
-  Walk<FUSED, MULTI> w;
-  long long t;
-  bool live;
-  __device__ TileCursor(const DecodeParams &p, const CtaRange &r) : w(p, r), t(0) {
-    live = w.next();
-    if (live) t = w.t0;
-  }
-  __device__ void step() {
-    if (++t >= w.t1) {
-      w.advance();
-      live = w.next();
-      if (live) t = w.t0;
-    }
-  }
-  __device__ bool first() const { return t == w.t0; }
-  __device__ bool last() const { return t == w.t1 - 1; }
-  __device__ int nv() const { return min(kTile, w.n - int(t) * kTile); }
-};
-
-__device__ __forceinline__ uint32_t bar_addr(uint64_t &b) { return smem_u32(&b); }
-
-// Logical pages [lp0, lp1] that hold tile t's owned tokens (n tokens owned by
-// partition `part`).
-__device__ __forceinline__ void tile_pages(const DecodeParams &p, int part, long long t, int n,
-                                           int *lp0, int *lp1) {
-  const int jl = min(int(t) * kTile + kTile, n) - 1;
-  *lp0 = int(t) * p.num_parts;
-  *lp1 = int((part + (long long)p.num_parts * jl) / kPage);
-}
-
-// ------------------------------------------------------------------ producer
-
-constexpr int kPrefetchAhead = 2;  // tiles whose pages are pulled into L2 ahead of the stage
-
-template <bool F8, bool FUSED, bool MULTI>
-__device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
-                            uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
-                            int *err) {
-  using namespace tc;
-  const DecodeParams &p = tp.p;
-  volatile int *abort = &m.abort;
-  const int lane = threadIdx.x & 31;
-  uint32_t kv_it = 0, q_it = 0;
-  int last_q = -1, last_kv[2] = {-1, -1};
-  // bf16: one 4-D box of groups_per_page swizzled atoms per page; e4m3: one
-  // 2-D box of the page's 8 * groups_per_page owned rows, 576 B each
-  const int rows_per_page = 8 * tp.groups_per_page;
-  const uint32_t page_bytes =
-      F8 ? uint32_t(rows_per_page * kRawRow) : uint32_t(tp.groups_per_page) * kAtomBytes;
-  const uint32_t dst0 = F8 ? sKv + kRawOff : sKv;
-  bool ok = true;
-
-  // The whole warp produces: lane k handles page k of a tile (a tile spans P
-  // pages), so the page-index loads, L2 prefetches and TMA boxes of a tile go
-  // out together rather than one after another.  A lane's page index is read
-  // kPrefetchAhead tiles early, when the page is prefetched into L2 (the
-  // 129 MB L2 gives the two shared-memory stages more HBM requests in
-  // flight), and carried in `ring` until its tile is loaded.
-  TileCursor<FUSED, MULTI> ahead(p, r);
-  auto next_ahead = [&]() {
-    int pg = -1;
-    if (ahead.live) {
-      int lp0, lp1;
-      tile_pages(p, ahead.w.part, ahead.t, ahead.w.n, &lp0, &lp1);
-      if (lane <= lp1 - lp0) {
-        pg = p.block_table[size_t(ahead.w.rb) * p.max_pages + lp0 + lane];
-        if (pg >= 0 && pg < p.num_pages) {
-          if (F8) {
-            if (FUSED)
-              tma_prefetch_3d(tm_kv, 0, pg * rows_per_page, ahead.w.pc);
-            else
-              tma_prefetch_2d(tm_kv, 0, pg * rows_per_page);
-          } else {
-            if (FUSED)
-              tma_prefetch_5d(tm_kv, 0, 0, 0, pg * tp.groups_per_page, ahead.w.pc);
-            else
-              tma_prefetch_4d(tm_kv, 0, 0, 0, pg * tp.groups_per_page);
-          }
-        }
-      }
-      ahead.step();
-    }
-    return pg;
-  };
-  int ring[kPrefetchAhead];
-#pragma unroll
-  for (int i = 0; i < kPrefetchAhead; ++i) ring[i] = next_ahead();
-
-  TileCursor<FUSED, MULTI> cur(p, r);
-  while (cur.live) {
-    if (cur.first()) {
-      checked_len(p, cur.w.rb, err);
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(m.q_empty), (q_it & 1) ^ 1, abort, kTimeoutNs))) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(bar_addr(m.q_full), uint32_t(kKb * tp.q_rows * 128));
-      __syncwarp();
-      if (lane < kKb)
-        tma_load_2d(sQ + lane * (64 * 128), tm_q, bar_addr(m.q_full), lane * 64,
-                    cur.w.rb * p.heads + cur.w.g * kHeads);
-      last_q = q_it & 1;
-      ++q_it;
-    }
-    const int s = kv_it & 1;
-    int lp0, lp1;
-    tile_pages(p, cur.w.part, cur.t, cur.w.n, &lp0, &lp1);
-    const bool mine = lane <= lp1 - lp0;
-    int pg = ring[0];
-    if (mine && (pg < 0 || pg >= p.num_pages)) {
-      atomicOr(err, kErrBadPage);
-      pg = -1;
-    }
-    const bool load = mine && pg >= 0;
-    const uint32_t bytes = uint32_t(__popc(__ballot_sync(0xffffffffu, load))) * page_bytes;
-    if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(m.kv_empty[s]), ((kv_it >> 1) & 1) ^ 1, abort,
-                                           kTimeoutNs))) {
-      ok = false;
-      break;
-    }
-    if (lane == 0) mbar_arrive_expect_tx(bar_addr(m.kv_full[s]), bytes);
-    __syncwarp();
-    if (load) {
-      const uint32_t dst = dst0 + s * kStageBytes + lane * page_bytes;
-      if (F8) {
-        if (FUSED)
-          tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, pg * rows_per_page, cur.w.pc);
-        else
-          tma_load_2d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, pg * rows_per_page);
-      } else {
-        if (FUSED)
-          tma_load_5d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, 0, 0, pg * tp.groups_per_page,
-                      cur.w.pc);
-        else
-          tma_load_4d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, 0, 0, pg * tp.groups_per_page);
-      }
-    }
-    last_kv[s] = (kv_it >> 1) & 1;
-    ++kv_it;
-#pragma unroll
-    for (int i = 0; i + 1 < kPrefetchAhead; ++i) ring[i] = ring[i + 1];
-    ring[kPrefetchAhead - 1] = next_ahead();
-    cur.step();
-  }
-  if (!ok && lane == 0) atomicOr(err, kErrTimeout);
-  // never leave the CTA with a copy still in flight into its shared memory
-  if (last_q >= 0) mbar_wait_drain(bar_addr(m.q_full), last_q, kDrainNs);
-  for (int s = 0; s < 2; ++s)
-    if (last_kv[s] >= 0) mbar_wait_drain(bar_addr(m.kv_full[s]), last_kv[s], kDrainNs);
-}
-
-// ------------------------------------------------------------------ MMA issuers
-//
-// A tcgen05.mma costs its issuing thread ~55 cycles whatever its size up to
-// N = 128 (measured on this GB300), so one thread cannot keep the tensor core
-// fed with M = 64 / N = 64 score MMAs.  Three warps issue: two split the 36
-// K-steps of S (one accumulator each), one issues PV.
-
-// Descriptors: an offset is added to the encoded start address (bits 0..13,
-// address >> 4), which never carries because shared addresses stay below 256 KB.
-template <bool F8, bool FUSED, bool MULTI>
-__device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
-                         uint32_t sKv, uint32_t tmem, int chain, int *err) {
-  using namespace tc;
-  const DecodeParams &p = tp.p;
-  volatile int *abort = &m.abort;
-  const uint32_t idesc_s = idesc_f32acc(64, 64, false, false, !F8);
-  // e4m3: the stage and Q are ready once the converter has expanded them
-  uint64_t *kv_ready = F8 ? m.kv_conv : m.kv_full;
-  uint64_t &q_ready = F8 ? m.q_ready : m.q_full;
-  const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);            // Q, K-major
-  const uint64_t dk0 = smem_desc_sw128(sKv, 16, kAtomBytes);    // K tile, K-major
-  constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
-  uint32_t s_it = 0, q_it = 0;
-  bool ok = true;
-  for (TileCursor<FUSED, MULTI> sc(p, r); sc.live; sc.step(), ++s_it) {
-    const int st = s_it & 1;
-    const uint32_t ph = (s_it >> 1) & 1;
-    if (!mbar_wait(bar_addr(kv_ready[st]), ph, abort, kTimeoutNs)) { ok = false; break; }
-    if (sc.first()) {
-      if (!mbar_wait(bar_addr(q_ready), q_it & 1, abort, kTimeoutNs)) { ok = false; break; }
-      ++q_it;
-    }
-    if (!mbar_wait(bar_addr(m.s_free[st]), ph ^ 1, abort, kTimeoutNs)) { ok = false; break; }
-    tc_fence_after();
-    const uint64_t dk = dk0 + st * kStageEnc;
-    const uint32_t d = tmem + kColS + 64 * (2 * st + chain);
-#pragma unroll
-    for (int i = 0; i < kKb * 2; ++i) {
-      const int ks = 2 * i + chain;
-      const int kb = ks >> 2, sub = ks & 3;
-      mma_bf16_ss(d, dq + ((kb * (64 * 128) + sub * 32) >> 4), dk + ((kb * 1024 + sub * 32) >> 4),
-                  idesc_s, i > 0);
-    }
-    mma_commit(bar_addr(m.s_full[st]));
-    if (sc.last()) mma_commit(bar_addr(m.q_empty));
-  }
-  if (!ok) atomicOr(err, kErrTimeout);
-  mma_commit(bar_addr(m.drain));
-  mbar_wait_drain(bar_addr(m.drain), 0, kDrainNs);
-}
-
-// O^T(chunk c) (+)= V^T(tile) P^T over ceil(nv/16) steps of 16 tokens; issuer
-// `half` takes value chunks 2 half and 2 half + 1.
-template <bool F8, bool FUSED, bool MULTI>
-__device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
-                          uint32_t tmem, int half, int *err) {
-  using namespace tc;
-  const DecodeParams &p = tp.p;
-  volatile int *abort = &m.abort;
-  const uint32_t idesc_o = idesc_f32acc(128, tp.npv, true, false, !F8);
-  const uint64_t dv0 = smem_desc_sw128(sKv, 1024, kAtomBytes);           // V^T, MN-major
-  const uint64_t dp0 = smem_desc_sw128(sKv + kPOff, 16, kAtomBytes);     // P, K-major
-  constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
-  uint32_t pv_it = 0, o_it = 0;
-  bool ok = true;
-  for (TileCursor<FUSED, MULTI> pc(p, r); pc.live; pc.step(), ++pv_it) {
-    if (!mbar_wait(bar_addr(m.p_full[pv_it & 1]), (pv_it >> 1) & 1, abort, kTimeoutNs)) {
-      ok = false;
-      break;
-    }
-    const bool fresh = pc.first();
-    if (fresh && !mbar_wait(bar_addr(m.o_free), (o_it & 1) ^ 1, abort, kTimeoutNs)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    const int st = pv_it & 1;
-    const uint64_t dv = dv0 + st * kStageEnc, dp = dp0 + st * kStageEnc;
-    const int ksteps = (pc.nv() + 15) >> 4;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      if (ks < ksteps) {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * half + cc;
-          mma_bf16_ss(tmem + kColO + 64 * c, dv + ((2 * ks * kAtomBytes + 2 * c * 1024) >> 4),
-                      dp + ((ks * 32) >> 4), idesc_o, !(fresh && ks == 0));
-        }
-      }
-    }
-    mma_commit(bar_addr(m.kv_empty[st]));
-    mma_commit(bar_addr(m.p_free));
-    if (pc.last()) {
-      mma_commit(bar_addr(m.o_full));
-      ++o_it;
-    }
-  }
-  if (!ok) atomicOr(err, kErrTimeout);
-  mma_commit(bar_addr(m.drain));
-  mbar_wait_drain(bar_addr(m.drain), 0, kDrainNs);
-}
-
-// ------------------------------------------------------------------ softmax + epilogue
-
-// O^T *= alpha per head (column), for this warp's 32 TMEM lanes.  Rare (a
-// head's running maximum grew by more than 2^8): kept out of line so that
-// the softmax loop's instruction stream stays short.
-__device__ __noinline__ void rescale_o(uint32_t tq, const float *al, int npv) {
-  using namespace tc;
-  for (int c = 0; c < 4; ++c)
-    for (int hb = 0; hb < npv / 16; ++hb) {
-      uint32_t o[16];
-      tmem_ld16(tq + kColO + 64 * c + 16 * hb, o);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al[16 * hb + i]);
-      tmem_st16(tq + kColO + 64 * c + 16 * hb, o);
-    }
-  tmem_wait_st();
-}
-
-// Packed fp32 pair arithmetic (one instruction per pair on sm_100 parts).
-__device__ __forceinline__ unsigned long long f2_bits(float2 a) {
-  return *reinterpret_cast<unsigned long long *>(&a);
-}
-__device__ __forceinline__ float2 bits_f2(unsigned long long b) {
-  return *reinterpret_cast<float2 *>(&b);
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  unsigned long long r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
-  return bits_f2(r);
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  unsigned long long r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(r);
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-// 2^x by the hardware approximation (relative error far below the bf16 / f16
-// rounding that follows); results below 2^-126 flush to zero.
-__device__ __forceinline__ float ex2(float x) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
-// Value rows [nv, roundup16(nv)) of a stage (the last tile of a request),
-// zeroed by the softmax warpgroup (rank gt): out of line, once per request.
-__device__ __noinline__ void zero_value_tail(unsigned char *stage, int nv, int gt) {
-  using namespace tc;
-  const int r0 = nv, nrow = ((nv + 15) & ~15) - nv;
-  for (int i = gt; i < nrow * 64; i += 128) {
-    const int rr = r0 + (i >> 6), kb = (i >> 3) & 7, ch = i & 7;
-    *reinterpret_cast<uint4 *>(stage + (rr >> 3) * kAtomBytes + kb * 1024 + (rr & 7) * 128 + ch * 16) =
-        make_uint4(0, 0, 0, 0);
-  }
-}
-
-template <bool F8, bool FUSED, bool MULTI>
-__device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
-                           unsigned char *smem, uint32_t tmem, int *err) {
-  using namespace tc;
-  const DecodeParams &p = tp.p;
-  volatile int *abort = &m.abort;
-  const int gt = int(threadIdx.x) - 128;  // rank in the warpgroup
-  const int q = gt >> 5, lane = gt & 31;
-  // 16x256b view of the M = 64 score accumulator: this lane holds heads
-  // row[0] = 16q + lane/4 and row[1] = row[0] + 8, and of every 8 tokens the
-  // pair 2 (lane % 4) + {0, 1}; four lanes share a head.
-  const int row[2] = {16 * q + (lane >> 2), 16 * q + (lane >> 2) + 8};
-  const int pair = 2 * (lane & 3);
-  const uint32_t tq = tmem + (uint32_t(32 * q) << 16);
-  float cs = p.score_scale_log2 * p.kv_scale;
-  uint32_t kv_it = 0, p_it = 0, o_it = 0;
-  bool ok = true;
-
-  Walk<FUSED, MULTI> w(p, r);
-  for (; ok && w.next(); w.advance()) {
-    const int hn = min(kHeads, p.heads - w.g * kHeads);
-    // owned tokens each of this lane's two rows sees (all w.n unless a request
-    // carries several query tokens, each with its own causal bound)
-    int nrow[2] = {w.n, w.n};
-    if (MULTI) {  // query token i of T sees the global tokens t < L - T + i + 1
-      const int L = checked_len(p, w.rb, nullptr);
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        nrow[h] = local_len(row_len(p, L, w.g * kHeads + row[h]), p.num_parts, w.part);
-    }
-    float mrun[2] = {-INFINITY, -INFINITY};  // running max (base-2 units) of each head
-    float ellp[2] = {0.f, 0.f};              // this lane's share of each head's sum
-    for (long long t = w.t0; t < w.t1; ++t, ++kv_it, ++p_it) {
-      const int s = kv_it & 1;
-      const uint32_t ph = (kv_it >> 1) & 1;
-      const int nv = min(kTile, w.n - int(t) * kTile);
-      // Every wait of the warpgroup is followed by a group vote, so that a
-      // wait that gave up in one warp never strands the others at a barrier.
-      bool got = __all_sync(0xffffffffu, mbar_wait(bar_addr(m.s_full[s]), ph, abort, kTimeoutNs));
-      if (F8 && got) {
-        // the converter's scale of this tile (Q's power of two folded in)
-        got = __all_sync(0xffffffffu, mbar_wait(bar_addr(m.kv_conv[s]), ph, abort, kTimeoutNs));
-        cs = m.tscale[s];
-      }
-      // unscaled scores in token pairs: xp[2j + h] = head row[h], tokens
-      // 8j + pair + {0, 1}
-      float2 xp[16];
-      if (got) {
-        tc_fence_after();
-        uint32_t ra[32], rb[32];
-        tmem_ld16x256b_x8(tq + kColS + 64 * (2 * s), ra);
-        tmem_ld16x256b_x8(tq + kColS + 64 * (2 * s + 1), rb);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          xp[k] = add2(make_float2(__uint_as_float(ra[2 * k]), __uint_as_float(ra[2 * k + 1])),
-                       make_float2(__uint_as_float(rb[2 * k]), __uint_as_float(rb[2 * k + 1])));
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_addr(m.s_free[s]));
-      }
-      const int nv0 = MULTI ? nrow[0] - int(t) * kTile : nv, nv1 = MULTI ? nrow[1] - int(t) * kTile : nv;
-      if ((MULTI ? min(nv0, nv1) : nv) < kTile) {  // the tile's tail: tokens past a row's last visible one
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int tok = 8 * (k >> 1) + pair, lim = (k & 1) ? nv1 : nv0;
-          xp[k].x = tok < lim ? xp[k].x : -INFINITY;
-          xp[k].y = tok + 1 < lim ? xp[k].y : -INFINITY;
-        }
-      }
-      float tmax[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float mx = max3(xp[h].x, xp[h].y, xp[2 + h].x);
-        mx = max3(mx, xp[2 + h].y, xp[4 + h].x);
-        mx = max3(mx, xp[4 + h].y, xp[6 + h].x);
-        mx = max3(mx, xp[6 + h].y, xp[8 + h].x);
-        mx = max3(mx, xp[8 + h].y, xp[10 + h].x);
-        mx = max3(mx, xp[10 + h].y, xp[12 + h].x);
-        mx = max3(mx, xp[12 + h].y, xp[14 + h].x);
-        tmax[h] = fmaxf(mx, xp[14 + h].y);
-      }
-      float mnew[2], alpha[2];
-      bool resc = false;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 1));
-        tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 2));
-        const float sm = tmax[h] * cs;  // cs > 0: the scaled maximum
-        mnew[h] = mrun[h];
-        alpha[h] = 1.f;
-        if (t == w.t0) {
-          mnew[h] = sm;
-        } else if (sm > mrun[h] + kRescaleThreshold) {
-          mnew[h] = sm;
-          alpha[h] = exp2f(mrun[h] - sm);
-          resc = true;
-        }
-      }
-      if ((lane & 3) == 0) {
-        m.alpha[p_it & 1][row[0]] = alpha[0];
-        m.alpha[p_it & 1][row[1]] = alpha[1];
-      }
-      // One plain group barrier per tile: each warp posts whether one of its
-      // heads needs an O rescale (bit 0) or a wait gave up (bit 1), and every
-      // branch below follows the OR of the four, so all 128 lanes take it
-      // together.  (Flags are double-buffered by tile parity: a warp cannot
-      // rewrite a buffer before every warp has passed the next barrier.)
-      {
-        const uint32_t flag = (__any_sync(0xffffffffu, resc) ? 1u : 0u) | (got ? 0u : 2u);
-        if (lane == 0) m.vote[p_it & 1][q] = flag;
-      }
-      named_sync(1, 128);
-      const uint32_t vote = m.vote[p_it & 1][0] | m.vote[p_it & 1][1] | m.vote[p_it & 1][2] |
-                            m.vote[p_it & 1][3];
-      if (vote & 2u) { ok = false; break; }
-      if (vote & 1u) {
-        // rescaling O^T needs the previous tile's PV to have finished
-        const bool pv_done = mbar_wait(bar_addr(m.p_free), (p_it - 1) & 1, abort, kTimeoutNs);
-        if (!named_sync_and(1, 128, pv_done)) { ok = false; break; }
-        tc_fence_after();
-        rescale_o(tq, m.alpha[p_it & 1], tp.npv);
-      }
-      // P = 2^(s cs - m) in bf16 (f16 for e4m3 caches), row-major
-      // [head][token] in the swizzled K-major layout: each lane writes 4-byte
-      // token pairs; the sum takes the rounded values the MMA will read
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        unsigned char *prow = smem + kOffKv + s * kStageBytes + (row[h] >> 3) * kAtomBytes + kPOff +
-                              (row[h] & 7) * 128 + (lane & 3) * 4;
-        // a row that has seen no token yet keeps a -inf max: its P is 0
-        const float mref = MULTI && mnew[h] == -INFINITY ? 0.f : mnew[h];
-        const float2 c2 = make_float2(cs, cs), m2 = make_float2(-mref, -mref);
-        float2 lsum = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float2 arg = fma2(xp[2 * j + h], c2, m2);
-          const float e0 = ex2(arg.x), e1 = ex2(arg.y);
-          float2 back;
-          uint32_t bits;
-          if (F8) {
-            __half2 v = __floats2half2_rn(e0, e1);
-            back = __half22float2(v);
-            bits = *reinterpret_cast<uint32_t *>(&v);
-          } else {
-            __nv_bfloat162 v = __floats2bfloat162_rn(e0, e1);
-            bits = *reinterpret_cast<uint32_t *>(&v);
-            back = make_float2(__uint_as_float(bits << 16), __uint_as_float(bits & 0xffff0000u));
-          }
-          lsum = add2(lsum, back);
-          *reinterpret_cast<uint32_t *>(prow + ((j ^ (row[h] & 7)) << 4)) = bits;
-        }
-        ellp[h] = ellp[h] * alpha[h] + (lsum.x + lsum.y);
-        mrun[h] = mnew[h];
-      }
-      // rows [nv, roundup16(nv)) of V are read by the last PV step but hold no
-      // owned token (stale or unowned data): zero their 512 value dims
-      if (nv & 15) zero_value_tail(smem + kOffKv + s * kStageBytes, nv, gt);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(m.p_full[s]));
-    }
-    if (!ok) break;
-
-    // the four lanes of a head hold parts of its sum
-    float ell[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      ell[h] = ellp[h] + __shfl_xor_sync(0xffffffffu, ellp[h], 1);
-      ell[h] += __shfl_xor_sync(0xffffffffu, ell[h], 2);
-    }
-    // ---- epilogue of this CTA's share of request v
-    if ((lane & 3) == 0) {  // per-head output scale: kv_scale / sum (0 for a row that saw nothing)
-      m.ell[row[0]] = !MULTI || ell[0] > 0.f ? p.kv_scale / ell[0] : 0.f;
-      m.ell[row[1]] = !MULTI || ell[1] > 0.f ? p.kv_scale / ell[1] : 0.f;
-    }
-    const bool got_o = mbar_wait(bar_addr(m.o_full), o_it & 1, abort, kTimeoutNs);
-    if (!named_sync_and(2, 128, got_o)) { ok = false; break; }
-    tc_fence_after();
-    const SplitInfo si = split_info(r, w.v, w.pv, w.tiles);
-    const bool split = si.nsplits > 1;
-    const size_t out_row0 = size_t(w.b) * p.heads + size_t(w.g) * kHeads;
-    // This warp owns value dims 128c + 32q .. + 31 of each chunk c (its TMEM
-    // lanes).  Values go through a 2 KB per-warp buffer, transposed to
-    // [head][dim], so that each lane stores 16-byte runs of dims: 8 (bf16)
-    // or 16 (fp32 slot) stores per chunk instead of 64.
-    unsigned char *stg = m.stage_out[q];
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t o[4][16];
-#pragma unroll
-      for (int hb = 0; hb < 4; ++hb) tmem_ld16(tq + kColO + 64 * c + 16 * hb, o[hb]);
-      tmem_wait_ld();
-      const int d0 = 128 * c + 32 * q;
-      if (!split) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {  // heads 32 half .. + 31
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int hb = 2 * half + hh;
-            float sc[16];  // the block's 16 output scales, read before its stores
-#pragma unroll
-            for (int i = 0; i < 16; ++i) sc[i] = m.ell[16 * hb + i];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              reinterpret_cast<__nv_bfloat16 *>(stg)[(16 * hh + i) * 32 + lane] =
-                  __float2bfloat16_rn(__uint_as_float(o[hb][i]) * sc[i]);
-          }
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {  // 32 heads x 4 runs of 8 dims
-            const int k = lane + 32 * j, hl = k >> 2, part = k & 3, h = 32 * half + hl;
-            const uint4 v = *reinterpret_cast<const uint4 *>(stg + k * 16);
-            if (h < hn)
-              *reinterpret_cast<uint4 *>(p.out + (out_row0 + h) * kDv + d0 + part * 8) = v;
-          }
-          __syncwarp();
-        }
-      } else {
-        float *slot = slot_out_ptr(p) + size_t(si.slot) * kSlotHeads * kDv;
-#pragma unroll
-        for (int hb = 0; hb < 4; ++hb) {  // heads 16 hb .. + 15
-          float sc[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) sc[i] = m.ell[16 * hb + i];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            reinterpret_cast<float *>(stg)[i * 32 + lane] = __uint_as_float(o[hb][i]) * sc[i];
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {  // 16 heads x 8 runs of 4 dims
-            const int k = lane + 32 * j, hl = k >> 3, part = k & 7, h = 16 * hb + hl;
-            const uint4 v = *reinterpret_cast<const uint4 *>(stg + k * 16);
-            // the merge reads it back after the rest of the KV stream
-            if (h < hn) st_global_keep_l2(slot + size_t(h) * kDv + d0 + part * 4, v);
-          }
-          __syncwarp();
-        }
-      }
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_addr(m.o_free));
-    ++o_it;
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-      if ((lane & 3) == 0 && row[h] < hn) {
-        const float lse2 = mrun[h] + log2f(ell[h]);
-        if (!split)
-          p.lse[out_row0 + row[h]] = lse_out(p, lse2);
-        else
-          slot_lse_ptr(p)[si.slot * kSlotHeads + row[h]] = lse2;
-      }
-    if (gt == 0) record_split(p, w.v, si);
-  }
-  if (!ok) atomicOr(err, kErrTimeout);
-}
-
-// ------------------------------------------------------------------ e4m3 converter
-//
-// Warps 9..11.  Q (bf16, as landed by TMA) becomes f16 scaled by 2^k, k chosen
-// from the largest |q| of the request so that it lies in [2^14, 2^15): every
-// bf16 value down to 2^-31 of that maximum is exact in f16 and nothing
-// overflows; the scores then carry 2^-k.  Each 8-byte chunk of fp8 values
-// (one row, 8 consecutive dims) becomes one 16-byte f16 chunk of the
-// swizzled [atom][dim block][8 rows][128 B] layout.
-
-// bf16 pair -> f16 pair, both scaled by the power of two `sc` (exact unless
-// the scaled value leaves f16's range, which the choice of k rules out).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc) {
-  const float lo = __uint_as_float(w << 16) * sc;
-  const float hi = __uint_as_float(w & 0xffff0000u) * sc;
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// 8 e4m3 values -> one 16-byte f16 chunk at `dst`.
-__device__ __forceinline__ void expand_fp8_store(unsigned char *dst, uint2 w) {
-  uint4 o;
-  o.x = e4m3x2_to_f16x2(uint16_t(w.x));
-  o.y = e4m3x2_to_f16x2(uint16_t(w.x >> 16));
-  o.z = e4m3x2_to_f16x2(uint16_t(w.y));
-  o.w = e4m3x2_to_f16x2(uint16_t(w.y >> 16));
-  *reinterpret_cast<uint4 *>(dst) = o;
-}
-
-// The request's Q (bf16, as landed) to f16 in place, scaled by 2^k; *qinv =
-// 2^-k.  Once per request piece: out of line.
-__device__ __noinline__ bool convert_q(const TcParams &tp, TcMisc &m, unsigned char *smem, int g,
-                                       uint32_t q_it, float *qinv) {
-  using namespace tc;
-  const DecodeParams &p = tp.p;
-  volatile int *abort = &m.abort;
-  const int ct = int(threadIdx.x) - kConvWarp0 * 32;
-  const int cw = ct >> 5, lane = ct & 31;
-  constexpr int kQPer = kQBytes / 16 / kConvThreads;  // 48 uint4 of Q per thread
-  static_assert(kQBytes / 16 % kConvThreads == 0 && kQPer % 8 == 0, "Q split");
-  const bool got = mbar_wait(bar_addr(m.q_full), q_it & 1, abort, kTimeoutNs);
-  if (!named_sync_and(3, kConvThreads, got)) return false;
-  uint4 *qv = reinterpret_cast<uint4 *>(smem + kOffQ);  // [kb][64 rows][8 chunks]
-  // the maximum over this request's heads; rows past them (zeros, or the
-  // next request's heads that the box also covers) only feed score rows
-  // the epilogue drops
-  const int hn = min(kHeads, p.heads - g * kHeads);
-  uint32_t mx = 0;
-#pragma unroll 8
-  for (int u = 0; u < kQPer; ++u) {
-    const int i = ct + u * kConvThreads;
-    if (((i >> 3) & 63) >= hn) continue;
-    const uint4 w = qv[i];
-    mx = __vmaxu2(mx, w.x & 0x7fff7fffu);
-    mx = __vmaxu2(mx, w.y & 0x7fff7fffu);
-    mx = __vmaxu2(mx, w.z & 0x7fff7fffu);
-    mx = __vmaxu2(mx, w.w & 0x7fff7fffu);
-  }
-  mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
-  if (lane == 0) m.conv_max[cw] = mx;
-  named_sync(3, kConvThreads);
-  mx = max(m.conv_max[0], max(m.conv_max[1], m.conv_max[2]));
-  // |q| bits are ordered like magnitudes; an Inf or NaN keeps k = 0
-  int k = 0;
-  if (mx < 0x7f80u) k = min(126, max(-126, 14 - (int(mx >> 7) - 127)));
-  const float sc = __int_as_float((127 + k) << 23);
-  *qinv = __int_as_float((127 - k) << 23);
-#pragma unroll 8
-  for (int u = 0; u < kQPer; ++u) {
-    uint4 w = qv[ct + u * kConvThreads];
-    w.x = bf16x2_to_f16x2_scaled(w.x, sc);
-    w.y = bf16x2_to_f16x2_scaled(w.y, sc);
-    w.z = bf16x2_to_f16x2_scaled(w.z, sc);
-    w.w = bf16x2_to_f16x2_scaled(w.w, sc);
-    qv[ct + u * kConvThreads] = w;
-  }
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar_addr(m.q_ready));
-  return true;
-}
-
-template <bool FUSED, bool MULTI>
-__device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r, TcMisc &m,
-                                           unsigned char *smem, int *err) {
-  using namespace tc;
-  const DecodeParams &p = tp.p;
-  volatile int *abort = &m.abort;
-  const int ct = int(threadIdx.x) - kConvWarp0 * 32;  // 0 .. 95
-  const int lane = ct & 31;
-  // Thread (tr, tc) = (ct / 24, ct % 24) converts, of rows 4k + tr, the 8-value
-  // chunks tc, tc + 24 and tc + 48: chunk c lands in dim block c / 8 at
-  // swizzled position (c % 8) ^ (row % 8), so the three chunks sit 3 blocks
-  // (3072 B) apart, and row 4k + tr has row % 8 = tr + 4 (k % 2), atom k / 2.
-  const int tr = ct / 24, tc = ct - 24 * (ct / 24);
-  const int src0 = tr * kRawRow + tc * 8;
-  const int dst0 = (tc >> 3) * 1024 + tr * 128 + (((tc & 7) ^ tr) << 4);
-  const int dst1 = (tc >> 3) * 1024 + (tr + 4) * 128 + (((tc & 7) ^ (tr + 4)) << 4);
-  static_assert(kConvThreads == 4 * 24 && kRawRow == 72 * 8, "converter split");
-  uint32_t kv_it = 0, q_it = 0;
-  float qinv = 1.f;
-  bool ok = true;
-  for (TileCursor<FUSED, MULTI> c(p, r); c.live; c.step(), ++kv_it) {
-    if (c.first()) {
-      if (!convert_q(tp, m, smem, c.w.g, q_it, &qinv)) { ok = false; break; }
-      ++q_it;
-    }
-    const int s = kv_it & 1;
-    const bool got = mbar_wait(bar_addr(m.kv_full[s]), (kv_it >> 1) & 1, abort, kTimeoutNs);
-    if (!named_sync_and(3, kConvThreads, got)) { ok = false; break; }
-    unsigned char *stage = smem + kOffKv + s * kStageBytes;
-    const unsigned char *raw = stage + kRawOff;
-    // Rows past the request's end stay unconverted: their scores are masked
-    // and the softmax zeroes the value rows the last PV step reads.
-    //
-    // Destination atom a (rows 8a .. 8a + 7) covers raw rows 16 (a - 4) ..
-    // 16 (a - 4) + 15 for a >= 4, so the rows go in four groups: 0..31 (below
-    // the raw rows), 32..47 (over raw rows 0..31), 48..55 (over 32..47), and
-    // 56..63, which overlaps its own raw rows: read first, written last.
-    const int nv = c.nv();
-    uint2 w[4][3];
-    // steps k0 .. k0 + n - 1: loads, then conversions and stores
-    auto load = [&](int k0, int n) {
-#pragma unroll
-      for (int k = 0; k < n; ++k)
-        if (4 * (k0 + k) + tr < nv)
-#pragma unroll
-          for (int e = 0; e < 3; ++e)
-            w[k][e] = *reinterpret_cast<const uint2 *>(raw + src0 + (k0 + k) * 4 * kRawRow + e * 192);
-    };
-    auto store = [&](int k0, int n) {
-#pragma unroll
-      for (int k = 0; k < n; ++k)
-        if (4 * (k0 + k) + tr < nv)
-#pragma unroll
-          for (int e = 0; e < 3; ++e)
-            expand_fp8_store(stage + ((k0 + k) >> 1) * kAtomBytes + (((k0 + k) & 1) ? dst1 : dst0) +
-                                 e * 3072,
-                             w[k][e]);
-    };
-    load(0, 4); store(0, 4);
-    load(4, 4); store(4, 4);
-    if (nv > 32) {
-      named_sync(3, kConvThreads);
-      load(8, 4); store(8, 4);
-      if (nv > 48) {
-        named_sync(3, kConvThreads);
-        load(12, 4);            // rows 48..63
-        store(12, 2);           // rows 48..55 over raw rows 32..47
-        if (nv > 56) {
-          named_sync(3, kConvThreads);
-#pragma unroll
-          for (int k = 0; k < 2; ++k) w[k][0] = w[k + 2][0], w[k][1] = w[k + 2][1], w[k][2] = w[k + 2][2];
-          store(14, 2);
-        }
-      }
-    }
-    if (ct == 0) m.tscale[s] = p.score_scale_log2 * p.kv_scale * qinv;
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_addr(m.kv_conv[s]));
-  }
-  if (!ok) atomicOr(err, kErrTimeout);
-}
-
-// ------------------------------------------------------------------ kernel
-
-template <bool F8, bool FUSED, bool MULTI>
-__global__ void __launch_bounds__(tc_threads<F8>(), 1)
-    decode_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_kv) {
-  using namespace tc;
-  extern __shared__ unsigned char smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
-  unsigned char *smem = smem_raw + pad;
-  const uint32_t sbase = raw + pad;
-  TcMisc &m = *reinterpret_cast<TcMisc *>(smem + kOffMisc);
-  const DecodeParams &p = tp.p;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int *err = error_word(p);
-
-  // Q rows past the request's heads are read by the MMAs but never loaded:
-  // they must hold finite values.  (P rows past them are written each tile.)
-  for (int i = tid; i < kQBytes / 16; i += tc_threads<F8>())
-    reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_addr(m.kv_full[s]), 1);
-      mbar_init(bar_addr(m.kv_empty[s]), 2);  // both PV issuers commit
-      mbar_init(bar_addr(m.s_full[s]), 2);   // both score issuers commit
-      mbar_init(bar_addr(m.s_free[s]), 4);
-    }
-    mbar_init(bar_addr(m.q_full), 1);
-    mbar_init(bar_addr(m.q_empty), 2);
-    // one per stage: the softmax runs ahead of the PV issuers, and tile k + 2
-    // (same stage) cannot reach the softmax before PV k has been issued
-    mbar_init(bar_addr(m.p_full[0]), 4);
-    mbar_init(bar_addr(m.p_full[1]), 4);
-    mbar_init(bar_addr(m.p_free), 2);
-    mbar_init(bar_addr(m.o_full), 2);
-    mbar_init(bar_addr(m.o_free), 4);
-    mbar_init(bar_addr(m.drain), 4);       // all four MMA issuers
-    mbar_init(bar_addr(m.kv_conv[0]), 3);  // one arrival per converter warp
-    mbar_init(bar_addr(m.kv_conv[1]), 3);
-    mbar_init(bar_addr(m.q_ready), 3);
-    m.abort = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
-    tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_kv);
-  }
-  fence_proxy_async_smem();
-  write_empty_requests<MULTI>(p);
-  cta_schedule<MULTI>(p, &m.range, m.scratch);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = m.tmem_base;
-  const CtaRange r = m.range;
-
-  if (r.start < r.end) {
-    if (warp == 0) {
-      tc_producer<F8, FUSED, MULTI>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
-    } else if (warp == 1 || warp == 2) {
-      if (lane == 0) tc_mma_s<F8, FUSED, MULTI>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
-    } else if (warp == 3 || warp == 8) {
-      if (lane == 0) tc_mma_pv<F8, FUSED, MULTI>(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
-    } else if (warp < 8) {
-      tc_softmax<F8, FUSED, MULTI>(tp, r, m, smem, tmem, err);
-    } else if (F8) {
-      tc_convert<FUSED, MULTI>(tp, r, m, smem, err);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
+extern template cudaError_t launch_tc_variants<false>(const TcParams &, const CUtensorMap &,
+                                                      const CUtensorMap &, int, cudaStream_t);
+extern template cudaError_t launch_tc_variants<true>(const TcParams &, const CUtensorMap &,
+                                                     const CUtensorMap &, int, cudaStream_t);
 
 int tc_smem_bytes() { return tc::kSmemBytes; }
-
-cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream);
-
-template <bool F8, bool FUSED, bool MULTI>
-static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
-                             int grid, cudaStream_t stream) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<F8, FUSED, MULTI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
-  decode_tc_kernel<F8, FUSED, MULTI>
-      <<<grid, tc_threads<F8>(), tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
-  return cudaGetLastError();
-}
-
-template <bool F8, bool FUSED>
-static cudaError_t launch_tc_q(const TcParams &tp, const CUtensorMap &tm_q,
-                               const CUtensorMap &tm_kv, int grid, cudaStream_t stream) {
-  return tp.p.q_len > 1 ? launch_tc<F8, FUSED, true>(tp, tm_q, tm_kv, grid, stream)
-                        : launch_tc<F8, FUSED, false>(tp, tm_q, tm_kv, grid, stream);
-}
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
                              const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
@@ -987,11 +21,8 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int gro
   tp.npv = npv;
   tp.q_rows = q_rows;
   tp.groups_per_page = groups_per_page;
-  const bool f8 = p.kv_e4m3 != 0, fused = p.fused != 0;
-  cudaError_t e = f8 ? (fused ? launch_tc_q<true, true>(tp, tm_q, tm_kv, grid, stream)
-                              : launch_tc_q<true, false>(tp, tm_q, tm_kv, grid, stream))
-                     : (fused ? launch_tc_q<false, true>(tp, tm_q, tm_kv, grid, stream)
-                              : launch_tc_q<false, false>(tp, tm_q, tm_kv, grid, stream));
+  cudaError_t e = p.kv_e4m3 ? launch_tc_variants<true>(tp, tm_q, tm_kv, grid, stream)
+                            : launch_tc_variants<false>(tp, tm_q, tm_kv, grid, stream);
   return e == cudaSuccess ? launch_split_merge(p, grid, stream) : e;
 }
 
