@@ -26,8 +26,8 @@ cudaError_t launch_kv_append(const void *kv_new, void *kv_pages, const int32_t *
                              int num_pages, int max_pages, int e4m3, float kv_scale,
                              int32_t *error_word, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
-                             const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
-                             cudaStream_t stream);
+                             const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
+                             const CUtensorMap &tm_kvg, int grid, cudaStream_t stream);
 cudaError_t launch_lse_combine(const void *partials, const float *lses, int num_parts, void *out,
                                float *out_lse, int rows, int dim, int base2, cudaStream_t stream);
 int combine_max_parts();
@@ -130,7 +130,8 @@ bool tensor_core_path(const mla_decode_desc *, int num_parts) {
 // faster boxes); for all P partitions (`all_parts`) it is added, with a stride
 // of one row (5-D / 3-D maps, coordinate r).
 int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, int part_id,
-                     int num_parts, bool all_parts, CUtensorMap *tm_q, CUtensorMap *tm_kv) {
+                     int num_parts, bool all_parts, CUtensorMap *tm_q, CUtensorMap *tm_kv,
+                     CUtensorMap *tm_kvg) {
   EncodeTiled enc = encode_tiled();
   if (!enc) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled unavailable");
@@ -162,6 +163,7 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3", r);
+    *tm_kvg = *tm_kv;  // unused: the e4m3 stage lands in one box per page
   } else {
     const cuuint64_t P = cuuint64_t(num_parts);
     const cuuint32_t G = cuuint32_t(8 / num_parts);
@@ -175,6 +177,14 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv", r);
+    // one column group (3 of the 9 dim blocks) of a page's atoms: the
+    // kernel's loads when a tile is one page (P = 1); the full-page box above
+    // serves the L2 prefetch and the loads of P > 1
+    box[2] = 3;
+    r = enc(tm_kvg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, all_parts ? 5 : 4, const_cast<char *>(base),
+            dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return tensor_map_fail("kv column group", r);
   }
   return MLA_OK;
 }
@@ -256,12 +266,12 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
   p.lse_base2 = lse_base == MLA_LSE_BASE2;
   cudaError_t e;
   if (tc) {
-    CUtensorMap tm_q, tm_kv;
-    int st = make_tensor_maps(q, kv_pages, d, part_id, num_parts, fused, &tm_q, &tm_kv);
+    CUtensorMap tm_q, tm_kv, tm_kvg;
+    int st = make_tensor_maps(q, kv_pages, d, part_id, num_parts, fused, &tm_q, &tm_kv, &tm_kvg);
     if (st != MLA_OK) return st;
     const int h = rows < kTcHeadsPerGroup ? rows : kTcHeadsPerGroup;
     const int npv = ((h + 15) / 16) * 16;
-    e = mla::launch_decode_tc(p, npv, h, 8 / num_parts, tm_q, tm_kv, grid, s);
+    e = mla::launch_decode_tc(p, npv, h, 8 / num_parts, tm_q, tm_kv, tm_kvg, grid, s);
   } else {
     e = mla::launch_decode_simt(p, grid, s);
   }

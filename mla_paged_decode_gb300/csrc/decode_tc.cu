@@ -6,23 +6,25 @@
 
 namespace mla {
 
-extern template cudaError_t launch_tc_variants<false>(const TcParams &, const CUtensorMap &,
-                                                      const CUtensorMap &, int, cudaStream_t);
-extern template cudaError_t launch_tc_variants<true>(const TcParams &, const CUtensorMap &,
-                                                     const CUtensorMap &, int, cudaStream_t);
+extern template cudaError_t launch_tc_variants<false>(
+    const TcParams &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, int,
+    cudaStream_t);
+extern template cudaError_t launch_tc_variants<true>(
+    const TcParams &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, int,
+    cudaStream_t);
 
 int tc_smem_bytes() { return tc::kSmemBytes; }
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
-                             const CUtensorMap &tm_q, const CUtensorMap &tm_kv, int grid,
-                             cudaStream_t stream) {
+                             const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
+                             const CUtensorMap &tm_kvg, int grid, cudaStream_t stream) {
   TcParams tp;
   tp.p = p;
   tp.npv = npv;
   tp.q_rows = q_rows;
   tp.groups_per_page = groups_per_page;
-  cudaError_t e = p.kv_e4m3 ? launch_tc_variants<true>(tp, tm_q, tm_kv, grid, stream)
-                            : launch_tc_variants<false>(tp, tm_q, tm_kv, grid, stream);
+  cudaError_t e = p.kv_e4m3 ? launch_tc_variants<true>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
+                            : launch_tc_variants<false>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
   return e == cudaSuccess ? launch_split_merge(p, grid, stream) : e;
 }
 

@@ -6,9 +6,11 @@
 //
 // Roles (288 threads):
 //   warp 0          TMA producer: Q of each request (9 boxes of 64 dims) and,
-//                   per tile, one 4-D box per page holding the 64/P rows the
-//                   partition owns (lane k: page k), into a [atom][dim block]
-//                   [8 rows][128 B] swizzled layout that serves both MMAs.
+//                   per tile, the 64/P rows the partition owns of each page
+//                   (lane k: page k) into a swizzled [column group][atom]
+//                   [dim block][8 rows][128 B] layout that serves both MMAs:
+//                   three boxes per page of three dim blocks each when P = 1
+//                   (the score MMAs start on the first), else one box.
 //   warp 1          TMEM owner (alloc/free).
 //   warps 1, 2      lane 0 issues half of the score MMAs (one accumulator each).
 //   warps 3, 8      lane 0 issues the PV MMAs of two of the four value chunks.
@@ -26,8 +28,8 @@
 // MMAs then run with f16 operands, P is written as f16, and the scores carry
 // sm_scale * kv_scale / (that power of two).
 //
-// Pipeline per tile i (stage / S buffer i mod 2): producer -> kv_full ->
-// MMA S_i (36 MMAs, two interleaved accumulators so consecutive MMAs are
+// Pipeline per tile i (stage / S buffer i mod 2): producer -> kv_full (per
+// column group) -> MMA S_i (36 MMAs, two interleaved accumulators so consecutive MMAs are
 // independent) -> s_full -> softmax reads S_i, frees it (s_free), waits for
 // PV_{i-1} (p_free), rescales O^T only when some head's running max grew by
 // more than 2^8, writes P_i (bf16) -> p_full -> MMA PV_i (4 independent
@@ -52,11 +54,30 @@ constexpr int kConvThreads = 96;
 constexpr int kHeads = 64;                   // heads per virtual request (M of S)
 constexpr int kKb = kDqk / 64;               // 9 blocks of 64 bf16 = 128 B
 constexpr int kQBytes = kKb * 64 * 128;      // [kb][64 rows][128 B]
-constexpr int kAtomBytes = kKb * 1024;       // 8 tokens x 576 dims: [kb][8][128 B]
+constexpr int kAtomBytes = kKb * 1024;       // 8 tokens x 576 dims
 constexpr int kStageBytes = 8 * kAtomBytes;  // 64 tokens
-// P [64 heads][64 tokens] bf16 reuses the rope block (dims 512..575) of the
-// tile's own stage, dead once S is computed: atom a at a * kAtomBytes + kPOff.
-constexpr int kPOff = 8 * 1024;
+// Stage layout: column groups of KBG dim blocks each,
+// [group][atom (8 rows)][dim block within the group][8 rows][128 B].
+// KBG = 3 (bf16 cache, P = 1: a tile is one page): three groups (dims
+// 0..191, 192..383, 384..575), each landed by its own TMA box and barrier,
+// so the score MMAs start on the first group while the others are in
+// flight.  KBG = 9 otherwise: one group, one box per page (a tile of P > 1
+// gathers P pages, and three boxes per page cost more than they gain; an
+// e4m3 stage is filled by the converter).  P [64 heads][64 tokens] reuses
+// the rope block (dims 512..575) of the tile's own stage, dead once S is
+// computed.
+template <bool F8, int AHEAD>
+constexpr int stage_kbg() { return !F8 && AHEAD == 1 ? 3 : kKb; }
+template <int KBG>
+constexpr int num_groups() { return kKb / KBG; }
+template <int KBG>
+constexpr uint32_t atom_stride() { return uint32_t(KBG) * 1024u; }
+// byte offset of dim block kb of atom 0 within a stage
+template <int KBG>
+__host__ __device__ constexpr uint32_t kb_off(int kb) {
+  return uint32_t(kb / KBG) * 8u * atom_stride<KBG>() + uint32_t(kb % KBG) * 1024u;
+}
+constexpr int kMaxGroups = 3;
 constexpr int kOffQ = 0;
 constexpr int kOffKv = kOffQ + kQBytes;
 constexpr int kOffMisc = kOffKv + 2 * kStageBytes;
@@ -82,7 +103,7 @@ template <bool F8>
 constexpr int tc_threads() { return F8 ? tc::kThreadsF8 : tc::kThreads; }
 
 struct TcMisc {
-  uint64_t kv_full[2], kv_empty[2], q_full, q_empty, s_full[2], s_free[2];
+  uint64_t kv_full[2][tc::kMaxGroups], kv_empty[2], q_full, q_empty, s_full[2], s_free[2];
   uint64_t p_full[2], p_free, o_full, o_free, drain;
   uint64_t kv_conv[2], q_ready;  // e4m3 only: stage / Q expanded to f16
   uint32_t tmem_base;
@@ -172,7 +193,7 @@ __device__ __forceinline__ void tile_pages(const DecodeParams &p, int part, long
 template <bool F8, bool FUSED, bool MULTI, int AHEAD>
 __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                             uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
-                            int *err) {
+                            const CUtensorMap *tm_kvg, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
@@ -182,8 +203,10 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   // bf16: one 4-D box of groups_per_page swizzled atoms per page; e4m3: one
   // 2-D box of the page's 8 * groups_per_page owned rows, 576 B each
   const int rows_per_page = 8 * tp.groups_per_page;
-  const uint32_t page_bytes =
-      F8 ? uint32_t(rows_per_page * kRawRow) : uint32_t(tp.groups_per_page) * kAtomBytes;
+  constexpr int KBG = stage_kbg<F8, AHEAD>(), kG = num_groups<KBG>();
+  // bytes one page lands per barrier: all its fp8 rows, or one column group
+  const uint32_t page_bytes = F8 ? uint32_t(rows_per_page * kRawRow)
+                                 : uint32_t(tp.groups_per_page) * atom_stride<KBG>();
   const uint32_t dst0 = F8 ? sKv + kRawOff : sKv;
   bool ok = true;
 
@@ -256,21 +279,27 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
       ok = false;
       break;
     }
-    if (lane == 0) mbar_arrive_expect_tx(bar_addr(m.kv_full[s]), bytes);
+    if (lane < kG) mbar_arrive_expect_tx(bar_addr(m.kv_full[s][lane]), bytes);
     __syncwarp();
     if (load) {
       const uint32_t dst = dst0 + s * kStageBytes + lane * page_bytes;
       if (F8) {
         if (FUSED)
-          tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, pg * rows_per_page, cur.w.pc);
+          tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, pg * rows_per_page, cur.w.pc);
         else
-          tma_load_2d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, pg * rows_per_page);
+          tma_load_2d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, pg * rows_per_page);
       } else {
-        if (FUSED)
-          tma_load_5d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, 0, 0, pg * tp.groups_per_page,
-                      cur.w.pc);
-        else
-          tma_load_4d(dst, tm_kv, bar_addr(m.kv_full[s]), 0, 0, 0, pg * tp.groups_per_page);
+        // group g: dim blocks [KBG g, KBG g + KBG) of the page's atoms
+        const CUtensorMap *tm = KBG == kKb ? tm_kv : tm_kvg;
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+          const uint32_t dg = dst + uint32_t(g) * 8u * atom_stride<KBG>();
+          if (FUSED)
+            tma_load_5d(dg, tm, bar_addr(m.kv_full[s][g]), 0, 0, KBG * g, pg * tp.groups_per_page,
+                        cur.w.pc);
+          else
+            tma_load_4d(dg, tm, bar_addr(m.kv_full[s][g]), 0, 0, KBG * g, pg * tp.groups_per_page);
+        }
       }
     }
     last_kv[s] = (kv_it >> 1) & 1;
@@ -284,7 +313,8 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   // never leave the CTA with a copy still in flight into its shared memory
   if (last_q >= 0) mbar_wait_drain(bar_addr(m.q_full), last_q, kDrainNs);
   for (int s = 0; s < 2; ++s)
-    if (last_kv[s] >= 0) mbar_wait_drain(bar_addr(m.kv_full[s]), last_kv[s], kDrainNs);
+    if (last_kv[s] >= 0)
+      for (int g = 0; g < kG; ++g) mbar_wait_drain(bar_addr(m.kv_full[s][g]), last_kv[s], kDrainNs);
 }
 
 // ------------------------------------------------------------------ MMA issuers
@@ -296,25 +326,28 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 
 // Descriptors: an offset is added to the encoded start address (bits 0..13,
 // address >> 4), which never carries because shared addresses stay below 256 KB.
-template <bool F8, bool FUSED, bool MULTI>
+template <bool F8, bool FUSED, bool MULTI, int KBG>
 __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                          uint32_t sKv, uint32_t tmem, int chain, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const uint32_t idesc_s = idesc_f32acc(64, 64, false, false, !F8);
-  // e4m3: the stage and Q are ready once the converter has expanded them
-  uint64_t *kv_ready = F8 ? m.kv_conv : m.kv_full;
+  // e4m3: the stage and Q are ready once the converter has expanded them;
+  // bf16: column group g of the stage once its own box has landed
   uint64_t &q_ready = F8 ? m.q_ready : m.q_full;
-  const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);            // Q, K-major
-  const uint64_t dk0 = smem_desc_sw128(sKv, 16, kAtomBytes);    // K tile, K-major
+  const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);                         // Q, K-major
+  const uint64_t dk0 = smem_desc_sw128(sKv + 32 * chain, 16, atom_stride<KBG>());  // K tile, K-major
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
   uint32_t s_it = 0, q_it = 0;
   bool ok = true;
   for (TileCursor<FUSED, MULTI> sc(p, r); sc.live; sc.step(), ++s_it) {
     const int st = s_it & 1;
     const uint32_t ph = (s_it >> 1) & 1;
-    if (!mbar_wait(bar_addr(kv_ready[st]), ph, abort, kTimeoutNs)) { ok = false; break; }
+    if (!mbar_wait(bar_addr(F8 ? m.kv_conv[st] : m.kv_full[st][0]), ph, abort, kTimeoutNs)) {
+      ok = false;
+      break;
+    }
     if (sc.first()) {
       if (!mbar_wait(bar_addr(q_ready), q_it & 1, abort, kTimeoutNs)) { ok = false; break; }
       ++q_it;
@@ -323,13 +356,21 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
     tc_fence_after();
     const uint64_t dk = dk0 + st * kStageEnc;
     const uint32_t d = tmem + kColS + 64 * (2 * st + chain);
+    // K-step ks = 2 i + chain: dim block i / 2, 16-dim slice 2 (i % 2) + chain
+    bool landed = true;
 #pragma unroll
     for (int i = 0; i < kKb * 2; ++i) {
-      const int ks = 2 * i + chain;
-      const int kb = ks >> 2, sub = ks & 3;
-      mma_bf16_ss(d, dq + ((kb * (64 * 128) + sub * 32) >> 4), dk + ((kb * 1024 + sub * 32) >> 4),
-                  idesc_s, i > 0);
+      const int kb = i >> 1;
+      if (!F8 && i > 0 && kb % KBG == 0 && (i & 1) == 0) {
+        landed = mbar_wait(bar_addr(m.kv_full[st][kb / KBG]), ph, abort, kTimeoutNs);
+        if (!landed) break;
+        tc_fence_after();
+      }
+      const uint32_t sub = 64u * uint32_t(i & 1) + 32u * uint32_t(chain);
+      mma_bf16_ss(d, dq + ((kb * (64 * 128) + sub) >> 4),
+                  dk + ((kb_off<KBG>(kb) + 64u * uint32_t(i & 1)) >> 4), idesc_s, i > 0);
     }
+    if (!landed) { ok = false; break; }
     mma_commit(bar_addr(m.s_full[st]));
     if (sc.last()) mma_commit(bar_addr(m.q_empty));
   }
@@ -340,15 +381,22 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
 
 // O^T(chunk c) (+)= V^T(tile) P^T over ceil(nv/16) steps of 16 tokens; issuer
 // `half` takes value chunks 2 half and 2 half + 1.
-template <bool F8, bool FUSED, bool MULTI>
+template <bool F8, bool FUSED, bool MULTI, int KBG>
 __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
                           uint32_t tmem, int half, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const uint32_t idesc_o = idesc_f32acc(128, tp.npv, true, false, !F8);
-  const uint64_t dv0 = smem_desc_sw128(sKv, 1024, kAtomBytes);           // V^T, MN-major
-  const uint64_t dp0 = smem_desc_sw128(sKv + kPOff, 16, kAtomBytes);     // P, K-major
+  // V^T of value chunk c (dim blocks 2c, 2c + 1), MN-major; P, K-major
+  uint64_t dv0[2];
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int c = 2 * half + cc;
+    dv0[cc] = smem_desc_sw128(sKv + kb_off<KBG>(2 * c), kb_off<KBG>(2 * c + 1) - kb_off<KBG>(2 * c),
+                              atom_stride<KBG>());
+  }
+  const uint64_t dp0 = smem_desc_sw128(sKv + kb_off<KBG>(8), 16, atom_stride<KBG>());
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
   uint32_t pv_it = 0, o_it = 0;
   bool ok = true;
@@ -364,7 +412,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
     }
     tc_fence_after();
     const int st = pv_it & 1;
-    const uint64_t dv = dv0 + st * kStageEnc, dp = dp0 + st * kStageEnc;
+    const uint64_t dp = dp0 + st * kStageEnc;
     const int ksteps = (pc.nv() + 15) >> 4;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
@@ -372,7 +420,8 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int c = 2 * half + cc;
-          mma_bf16_ss(tmem + kColO + 64 * c, dv + ((2 * ks * kAtomBytes + 2 * c * 1024) >> 4),
+          mma_bf16_ss(tmem + kColO + 64 * c,
+                      dv0[cc] + st * kStageEnc + ((2 * ks * atom_stride<KBG>()) >> 4),
                       dp + ((ks * 32) >> 4), idesc_o, !(fresh && ks == 0));
         }
       }
@@ -440,17 +489,18 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Value rows [nv, roundup16(nv)) of a stage (the last tile of a request),
 // zeroed by the softmax warpgroup (rank gt): out of line, once per request.
+template <int KBG>
 static __device__ __noinline__ void zero_value_tail(unsigned char *stage, int nv, int gt) {
   using namespace tc;
   const int r0 = nv, nrow = ((nv + 15) & ~15) - nv;
   for (int i = gt; i < nrow * 64; i += 128) {
     const int rr = r0 + (i >> 6), kb = (i >> 3) & 7, ch = i & 7;
-    *reinterpret_cast<uint4 *>(stage + (rr >> 3) * kAtomBytes + kb * 1024 + (rr & 7) * 128 + ch * 16) =
-        make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4 *>(stage + kb_off<KBG>(kb) + (rr >> 3) * atom_stride<KBG>() +
+                               (rr & 7) * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
   }
 }
 
-template <bool F8, bool FUSED, bool MULTI>
+template <bool F8, bool FUSED, bool MULTI, int KBG>
 __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
                            unsigned char *smem, uint32_t tmem, int *err) {
   using namespace tc;
@@ -578,8 +628,8 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
       // token pairs; the sum takes the rounded values the MMA will read
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        unsigned char *prow = smem + kOffKv + s * kStageBytes + (row[h] >> 3) * kAtomBytes + kPOff +
-                              (row[h] & 7) * 128 + (lane & 3) * 4;
+        unsigned char *prow = smem + kOffKv + s * kStageBytes + kb_off<KBG>(8) +
+                              (row[h] >> 3) * atom_stride<KBG>() + (row[h] & 7) * 128 + (lane & 3) * 4;
         // a row that has seen no token yet keeps a -inf max: its P is 0
         const float mref = MULTI && mnew[h] == -INFINITY ? 0.f : mnew[h];
         const float2 c2 = make_float2(cs, cs), m2 = make_float2(-mref, -mref);
@@ -607,7 +657,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
       }
       // rows [nv, roundup16(nv)) of V are read by the last PV step but hold no
       // owned token (stale or unowned data): zero their 512 value dims
-      if (nv & 15) zero_value_tail(smem + kOffKv + s * kStageBytes, nv, gt);
+      if (nv & 15) zero_value_tail<KBG>(smem + kOffKv + s * kStageBytes, nv, gt);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -816,7 +866,7 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
       ++q_it;
     }
     const int s = kv_it & 1;
-    const bool got = mbar_wait(bar_addr(m.kv_full[s]), (kv_it >> 1) & 1, abort, kTimeoutNs);
+    const bool got = mbar_wait(bar_addr(m.kv_full[s][0]), (kv_it >> 1) & 1, abort, kTimeoutNs);
     if (!named_sync_and(3, kConvThreads, got)) { ok = false; break; }
     unsigned char *stage = smem + kOffKv + s * kStageBytes;
     const unsigned char *raw = stage + kRawOff;
@@ -878,7 +928,8 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
 template <bool F8, bool FUSED, bool MULTI, int AHEAD>
 __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     decode_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_kv) {
+                     const __grid_constant__ CUtensorMap tm_kv,
+                     const __grid_constant__ CUtensorMap tm_kvg) {
   using namespace tc;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -889,6 +940,7 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
   const DecodeParams &p = tp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int *err = error_word(p);
+  constexpr int KBG = stage_kbg<F8, AHEAD>();
 
   // Q rows past the request's heads are read by the MMAs but never loaded:
   // they must hold finite values.  (P rows past them are written each tile.)
@@ -896,7 +948,7 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_addr(m.kv_full[s]), 1);
+      for (int g = 0; g < kMaxGroups; ++g) mbar_init(bar_addr(m.kv_full[s][g]), 1);
       mbar_init(bar_addr(m.kv_empty[s]), 2);  // both PV issuers commit
       mbar_init(bar_addr(m.s_full[s]), 2);   // both score issuers commit
       mbar_init(bar_addr(m.s_free[s]), 4);
@@ -924,6 +976,7 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
+    if (KBG != kKb) tma_prefetch_desc(&tm_kvg);
   }
   fence_proxy_async_smem();
   write_empty_requests<MULTI>(p);
@@ -936,13 +989,14 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
 
   if (r.start < r.end) {
     if (warp == 0) {
-      tc_producer<F8, FUSED, MULTI, AHEAD>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, err);
+      tc_producer<F8, FUSED, MULTI, AHEAD>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, &tm_kvg,
+                                           err);
     } else if (warp == 1 || warp == 2) {
-      if (lane == 0) tc_mma_s<F8, FUSED, MULTI>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
+      if (lane == 0) tc_mma_s<F8, FUSED, MULTI, KBG>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
     } else if (warp == 3 || warp == 8) {
-      if (lane == 0) tc_mma_pv<F8, FUSED, MULTI>(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
+      if (lane == 0) tc_mma_pv<F8, FUSED, MULTI, KBG>(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
     } else if (warp < 8) {
-      tc_softmax<F8, FUSED, MULTI>(tp, r, m, smem, tmem, err);
+      tc_softmax<F8, FUSED, MULTI, KBG>(tp, r, m, smem, tmem, err);
     } else if (F8) {
       tc_convert<FUSED, MULTI>(tp, r, m, smem, err);
     }
@@ -959,7 +1013,7 @@ cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t str
 
 template <bool F8, bool FUSED, bool MULTI, int AHEAD>
 static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
-                             int grid, cudaStream_t stream) {
+                             const CUtensorMap &tm_kvg, int grid, cudaStream_t stream) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -971,7 +1025,7 @@ static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const 
     configured[dev] = 1;
   }
   decode_tc_kernel<F8, FUSED, MULTI, AHEAD>
-      <<<grid, tc_threads<F8>(), tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv);
+      <<<grid, tc_threads<F8>(), tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv, tm_kvg);
   return cudaGetLastError();
 }
 
@@ -980,16 +1034,17 @@ static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const 
 // in one launch (distance 2); each with one query token or several.
 template <bool F8>
 cudaError_t launch_tc_variants(const TcParams &tp, const CUtensorMap &tm_q,
-                               const CUtensorMap &tm_kv, int grid, cudaStream_t stream) {
+                               const CUtensorMap &tm_kv, const CUtensorMap &tm_kvg, int grid,
+                               cudaStream_t stream) {
   const bool multi = tp.p.q_len > 1;
   if (tp.p.fused)
-    return multi ? launch_tc<F8, true, true, 2>(tp, tm_q, tm_kv, grid, stream)
-                 : launch_tc<F8, true, false, 2>(tp, tm_q, tm_kv, grid, stream);
+    return multi ? launch_tc<F8, true, true, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
+                 : launch_tc<F8, true, false, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
   if (tp.p.num_parts == 1)
-    return multi ? launch_tc<F8, false, true, 1>(tp, tm_q, tm_kv, grid, stream)
-                 : launch_tc<F8, false, false, 1>(tp, tm_q, tm_kv, grid, stream);
-  return multi ? launch_tc<F8, false, true, 2>(tp, tm_q, tm_kv, grid, stream)
-               : launch_tc<F8, false, false, 2>(tp, tm_q, tm_kv, grid, stream);
+    return multi ? launch_tc<F8, false, true, 1>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
+                 : launch_tc<F8, false, false, 1>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
+  return multi ? launch_tc<F8, false, true, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
+               : launch_tc<F8, false, false, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
 }
 
 }  // namespace mla
