@@ -22,11 +22,6 @@ __device__ __forceinline__ SplitInfo split_info(const CtaRange &r, int v, long l
   return s;
 }
 
-// Slot CTA c used for request v (which starts at tile pv).
-__device__ __forceinline__ int slot_of(const CtaRange &r, int c, int c_first, long long pv) {
-  return 2 * c + ((c == c_first && sched_start(c, r.total, r.g_eff) < pv) ? 1 : 0);
-}
-
 __device__ __forceinline__ float *slot_lse_ptr(const DecodeParams &p) {
   return reinterpret_cast<float *>(p.ws + p.wl.slot_lse);
 }
