@@ -979,6 +979,12 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     if (KBG != kKb) tma_prefetch_desc(&tm_kvg);
   }
   fence_proxy_async_smem();
+  // Launched as a programmatic dependent of the stream's previous kernel, so
+  // that this prologue overlaps its tail: everything above touches only this
+  // CTA's own resources.  Wait for that kernel's completion (and its writes)
+  // before reading any input or writing any output.  (Releasing this
+  // launch's own dependent, the split merge, early as well measured slower.)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   write_empty_requests<MULTI>(p);
   cta_schedule<MULTI>(p, &m.range, m.scratch);
   tc_fence_before();
@@ -1024,9 +1030,17 @@ static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const 
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  decode_tc_kernel<F8, FUSED, MULTI, AHEAD>
-      <<<grid, tc_threads<F8>(), tc::kSmemBytes, stream>>>(tp, tm_q, tm_kv, tm_kvg);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(tc_threads<F8>());
+  cfg.dynamicSmemBytes = tc::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<F8, FUSED, MULTI, AHEAD>, tp, tm_q, tm_kv, tm_kvg);
 }
 
 // The variants of one cache dtype: one partition alone with P = 1 (a tile is
