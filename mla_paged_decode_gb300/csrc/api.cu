@@ -280,6 +280,18 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
 
 }  // namespace
 
+namespace mla {
+// The decode partial of one partition on a caller-chosen workspace and grid
+// (arguments already validated): the path of the allocation-free entry point.
+int enqueue_partial(const void *q, const void *kv_pages, const int32_t *block_table,
+                    const int32_t *seq_lens, int part_id, int num_parts, float sm_scale,
+                    int lse_base, void *out, float *lse, const mla_decode_desc *d,
+                    void *workspace, int grid, cudaStream_t s) {
+  return enqueue_decode(q, kv_pages, block_table, seq_lens, part_id, num_parts, false, sm_scale,
+                        lse_base, out, lse, d, workspace, grid, s);
+}
+}  // namespace mla
+
 extern "C" {
 
 int mla_version(void) { return 100; }

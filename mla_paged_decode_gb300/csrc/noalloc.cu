@@ -21,12 +21,15 @@
 #include "common.cuh"
 
 namespace mla {
-cudaError_t launch_decode_simt(const DecodeParams &p, int grid, cudaStream_t stream);
+int enqueue_partial(const void *q, const void *kv_pages, const int32_t *block_table,
+                    const int32_t *seq_lens, int part_id, int num_parts, float sm_scale,
+                    int lse_base, void *out, float *lse, const mla_decode_desc *d,
+                    void *workspace, int grid, cudaStream_t s);
 }
 
 namespace {
 
-constexpr int kNoAllocHeadsPerGroup = 32;   // the CUDA-core decode kernel's head group
+constexpr int kNoAllocHeadsPerGroup = 32;   // the smaller head group of the two decode kernels
 constexpr int kNoAllocMaxVirtual = 16384;   // batch * ceil(heads / 32)
 constexpr int kNoAllocMaxGrid = 152;        // CTAs (GPUs with more SMs use 152)
 
@@ -113,27 +116,8 @@ extern "C" int mla_decode_partial_noalloc(const void *q, const void *kv_pages,
   // The scratch keeps the previous call's contents: the error word must start
   // at zero (every other part is rewritten before it is read).
   if (cudaMemsetAsync(dev.scratch, 0, 256, s) != cudaSuccess) return MLA_ERR_CUDA;
-
-  mla::DecodeParams p;
-  p.q = static_cast<const __nv_bfloat16 *>(q);
-  p.kv = kv_pages;
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
-  p.out = static_cast<__nv_bfloat16 *>(out);
-  p.lse = lse;
-  p.ws = static_cast<unsigned char *>(dev.scratch);
-  p.wl = wl;
-  p.batch = d->batch;
-  p.heads = d->num_heads;
-  p.head_groups = groups;
-  p.heads_per_group = kNoAllocHeadsPerGroup;
-  p.num_pages = d->num_pages;
-  p.max_pages = d->max_pages_per_seq;
-  p.part_id = part_id;
-  p.num_parts = num_parts;
-  p.kv_e4m3 = d->kv_dtype == MLA_KV_E4M3;
-  p.kv_scale = p.kv_e4m3 ? d->kv_scale : 1.f;
-  p.score_scale_log2 = sm_scale * mla::kLog2e;
-  p.lse_base2 = lse_base == MLA_LSE_BASE2;
-  return mla::launch_decode_simt(p, grid, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  // the kernels of mla_decode_partial (tensor-core when num_parts divides 8)
+  // on the built-in scratch
+  return mla::enqueue_partial(q, kv_pages, block_table, seq_lens, part_id, num_parts, sm_scale,
+                              lse_base, out, lse, d, dev.scratch, grid, s);
 }

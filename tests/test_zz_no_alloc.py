@@ -5,8 +5,8 @@ loops that cannot take an allocation's device synchronisation, C hosts with
 no allocator).  mla_decode_partial_noalloc serves them from scratch built into
 the library.  This checks, on two calls in a row (the second one finds the
 first one's leftovers in the shared scratch), that its outputs match those of
-mla_decode_partial within the parity tolerances, and that a batch beyond the
-built-in limit is refused without a launch.  The file is named so that pytest
+mla_decode_partial (bitwise: the same kernels run), and that a batch beyond
+the built-in limit is refused without a launch.  The file is named so that pytest
 collects it last.
 """
 import ctypes
@@ -60,6 +60,9 @@ def test_noalloc_matches_the_workspace_entry_point_twice_in_a_row(lib):
         ref = ref_out.double().cpu().numpy()
         assert_out_close(out, ref, what=f"no-alloc call {call}")
         assert_lse_close(lse, ref_lse.double().cpu().numpy(), base, what=f"no-alloc call {call}")
+        # num_parts = 2 runs the same tensor-core kernels on the same grid
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), call
+        assert torch.equal(lse, ref_lse), call
 
 
 def test_noalloc_refuses_batches_beyond_its_scratch(lib):
