@@ -200,7 +200,8 @@ def cpu_baseline(case, seconds: float):
     while spent < seconds and done < case.batch:
         q, kv, bt, lens = subcase_bits(case, [done])
         t0 = time.perf_counter()
-        oracle.decode_partial(q, kv, bt, lens, 0, 1, case.sm_scale, 0)
+        oracle.decode_partial(q, kv, bt, lens, 0, 1, case.sm_scale, 0, kv_dtype=case.kv_dtype,
+                              kv_scale=case.kv_scale)
         spent += time.perf_counter() - t0
         tokens += int(lens[0])
         done += 1
@@ -698,25 +699,136 @@ def run_dcp8(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def run_fp8(args, world, rank, local):
+    """--op fp8: the e4m3-cache workload (B=128, H=128, lognormal lengths with
+    median 8192, per-tensor scale, P=1) through mla_decode_partial.  Its
+    roofline is the tensor pipe: the MMAs run on f16 operands expanded from
+    the cache, and each 64-head group reads the cache again."""
+    import mla_paged_decode_gb300 as mla
+    from mla_paged_decode_gb300 import build
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    if rank == 0 or not os.path.exists(mla.library_path()):
+        build.build()
+    barrier(world)
+    mla.load_library()
+    case = workloads.config_fp8(device=dev, seed=args.seed, batch=args.batch)
+    if args.batch != 128:
+        case.name += f"_b{args.batch}"
+    B, H = case.batch, case.heads
+    n_tok = int(case.seq_lens.sum().item())
+    kv_bytes = n_tok * ROW_BYTES[case.kv_dtype]
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table, case.kv_scale)
+    out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q=case.q, bt=case.block_table, sl=case.seq_lens):
+        mla.decode_partial(q, case.kv_pages, bt, sl, 0, 1, case.sm_scale, 0, out, lse,
+                           kv_scale=case.kv_scale, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = ClockSampler(local)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    assert mla.check_workspace(ws) == 0
+    q_h, bt_h, sl_h = (case.q.cpu().pin_memory(), case.block_table.cpu().pin_memory(),
+                       case.seq_lens.cpu().pin_memory())
+    q_d, bt_d, sl_d = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        step(q_d, bt_d, sl_d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    per_s = ms / 1e3 / args.steps
+    peak, peak_kind = measured_peaks()
+    tpeak, tpeak_kind = measured_bf16_tflops()
+    flops = float(n_tok) * H * (2 * 576 + 2 * 512)
+    line = {
+        "metric": "MLA decode tokens/s and KV-read HBM GB/s (fraction of roofline) on 1 GB300",
+        "value": aggregate(ms, args.steps, B, world), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": case.name, "batch": B, "heads": H, "q_len": 1, "num_parts": 1,
+                   "seq_lens": "lognormal, median 8192, sigma 1, clipped to [1024, 65536] (seed %d)"
+                               % args.seed,
+                   "page_size": 64, "pool_pages": case.num_pages, "kv_dtype": "e4m3",
+                   "kv_bytes_per_step": kv_bytes,
+                   "l2": "%.2f GB of e4m3 KV per step; each of the two 64-head groups reads it"
+                         % (kv_bytes / 1e9),
+                   "parallelism": "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": flops / per_s / 1e12, "peak": tpeak,
+                     "unit": "TFLOP/s", "frac": flops / per_s / 1e12 / tpeak,
+                     "peak_source": tpeak_kind, "traffic": None,
+                     "kernel": "mla_decode_partial on an e4m3 cache: decode kernel + split merge, "
+                               "timed together per call (f16 MMAs on the expanded cache; real "
+                               "heads' flops, QK^T over 576 dims and PV over 512)",
+                     "hbm_achieved_gbs": kv_bytes / per_s / 1e9, "hbm_peak_gbs": peak,
+                     "hbm_frac": kv_bytes / per_s / 1e9 / peak, "hbm_peak_source": peak_kind},
+        "e2e": {"value": aggregate(e_ms, args.steps, B, world), "unit": "tokens/s",
+                "h2d_bytes_per_step": q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4,
+                "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clock_info,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["decode", "dcp8", "kv_append"], default="decode",
+    ap.add_argument("--op", choices=["decode", "dcp8", "fp8", "kv_append"], default="decode",
                     help="decode (the headline), dcp8 (the 8-partition DCP workload in one "
-                         "mla_decode_dcp call), or the KV append of one row per request")
+                         "mla_decode_dcp call), fp8 (the e4m3-cache workload), or the KV "
+                         "append of one row per request")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batch", type=int, default=64,
-                    help="requests per step (64 = the headline workload; smaller only for profiling)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="requests per step (default: the workload's own, 64 for decode and "
+                         "128 for fp8; smaller only for profiling)")
     ap.add_argument("--pool-pages", type=int, default=40000,
                     help="cache pool size in pages (40000 = the headline workload)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.batch is None:
+        args.batch = 128 if args.op == "fp8" else 64
     world, rank, local = dist_env()
     if args.op == "kv_append":
         if args.impl == "reference":
@@ -724,6 +836,12 @@ def main(argv=None):
                               "the append's CPU oracle is reported as cpu_baseline of --op kv_append"}))
             return
         run_append(args, world, rank, local)
+    elif args.op == "fp8":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the fp8 workload's CPU oracle is reported as cpu_baseline of --op fp8"}))
+            return
+        run_fp8(args, world, rank, local)
     elif args.op == "dcp8":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
