@@ -76,6 +76,9 @@ SHAPES = [
     (48, [64, 96, 31, 2049], 1, "e4m3"),
     (80, [300, 900, 1], 2, "e4m3"),
     (80, [700, 5], 1, "bf16"),
+    (128, [1300, 64, 1, 0, 511], 1, "bf16"),   # one page per tile, two head groups
+    (1, [77, 3000, 2, 65], 1, "bf16"),
+    (7, [129, 2, 1000], 1, "bf16"),
 ]
 
 
@@ -88,6 +91,15 @@ def test_random_shapes_with_poisoned_tails(heads, lens, num_parts, kv_dtype):
                                       device="cuda", tail_poison=True, pool_pages=sum(
                                           (L + 63) // 64 for L in lens) + 3)
     _check_all(case, atol=FP8_ATOL if kv_dtype == "e4m3" else None)
+
+
+def test_many_short_requests():
+    """600 requests of 1..300 tokens: every CTA walks several requests, and
+    many of them end mid-tile."""
+    lens = [int(x) for x in torch.randint(1, 301, (600,), generator=torch.Generator().manual_seed(3))]
+    case = workloads.make_decode_case("many_short", 16, lens, seed=3, device="cuda",
+                                      tail_poison=True, pool_pages=sum((L + 63) // 64 for L in lens) + 3)
+    _check_all(case, bases=(0,))
 
 
 def test_single_request_spread_over_every_cta():
