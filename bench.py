@@ -666,14 +666,15 @@ def run_dcp8(args, world, rank, local):
                      "unit": "GB/s", "frac": kv_bytes / per_s / 1e9 / peak,
                      "peak_source": peak_kind, "frac_of_8tbs": kv_bytes / per_s / 1e9 / 8000.0,
                      "traffic": None,
-                     "kernel": "mla_decode_dcp: one decode launch over the 8 partitions, split "
-                               "merge and LSE combine, timed together per call",
+                     "kernel": "mla_decode_dcp: one decode launch over the 8 partitions and "
+                               "one split merge with the LSE combine fused, timed together "
+                               "per call",
                      "tensor_tflops": flops / per_s / 1e12, "tensor_peak_tflops": tpeak,
                      "tensor_frac": flops / per_s / 1e12 / tpeak, "tensor_peak_source": tpeak_kind},
         "e2e": {"value": aggregate(e_ms, args.steps, B, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4,
                 "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clock_info,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:

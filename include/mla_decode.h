@@ -164,7 +164,8 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
  *               rules as for mla_decode_partial.
  *
  * num_parts in {1, 2, 4, 8}: one decode launch covers every (partition,
- * request) pair, then one split merge and the combine (three kernels).
+ * request) pair, then one kernel merges the requests the decode's schedule
+ * split across SMs and combines the partitions (two kernels).
  * Other num_parts (up to 256): one decode call per partition, then the
  * combine.  Errors and bounds reporting as for mla_decode_partial.
  */

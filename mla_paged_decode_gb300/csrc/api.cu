@@ -231,7 +231,8 @@ int head_groups_of(const mla_decode_desc *d) {
 int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_table,
                    const int32_t *seq_lens, int part_id, int num_parts, bool fused,
                    float sm_scale, int lse_base, void *out, float *lse, const mla_decode_desc *d,
-                   void *workspace, int grid, cudaStream_t s) {
+                   void *workspace, int grid, cudaStream_t s, void *comb_out = nullptr,
+                   float *comb_lse = nullptr) {
   const bool tc = tensor_core_path(d, num_parts);
   if (fused && !tc) return MLA_ERR_ARG;
   if (d->q_len > 1 && !tc) return MLA_ERR_SHAPE;
@@ -260,6 +261,8 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
   p.num_parts = num_parts;
   p.fused = fused ? 1 : 0;
   p.req_batch = d->batch;
+  p.comb_out = static_cast<__nv_bfloat16 *>(comb_out);
+  p.comb_lse = comb_lse;
   p.kv_e4m3 = d->kv_dtype == MLA_KV_E4M3;
   p.kv_scale = p.kv_e4m3 ? d->kv_scale : 1.f;
   p.score_scale_log2 = sm_scale * mla::kLog2e;
@@ -393,10 +396,11 @@ int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_tab
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t rows = size_t(d->batch) * rows_of(d);
   if (tensor_core_path(d, num_parts)) {
-    // every partition in one decode launch (and one split merge)
-    st = enqueue_decode(q, kv_pages, block_table, seq_lens, 0, num_parts, true, sm_scale,
-                        lse_base, partials, partial_lses, d, workspace, f.sms, s);
-    if (st != MLA_OK) return st;
+    // every partition in one decode launch, then one kernel that merges the
+    // splits and combines the partitions
+    return enqueue_decode(q, kv_pages, block_table, seq_lens, 0, num_parts, true, sm_scale,
+                          lse_base, partials, partial_lses, d, workspace, f.sms, s, out,
+                          out_lse);
   } else {
     for (int r = 0; r < num_parts; ++r) {
       st = enqueue_decode(q, kv_pages, block_table, seq_lens, r, num_parts, false, sm_scale,

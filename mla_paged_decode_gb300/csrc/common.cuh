@@ -58,6 +58,10 @@ struct DecodeParams {
   // partition bv / req_batch; out / lse are then [P, B, ...].  Otherwise
   // fused = 0 and req_batch = batch.
   int fused = 0, req_batch = 0;
+  // fused only: the partitions' LSE combine, written by the merge kernel
+  // ([B, rows, 512] bf16 and, optionally, [B, rows] fp32 in the lse base)
+  __nv_bfloat16 *comb_out = nullptr;
+  float *comb_lse = nullptr;
   // Query tokens per request (tensor-core kernel only; 1 elsewhere): the
   // `heads` rows of a request are then q_len x q_heads, row i * q_heads + h
   // for query token i, and token i of T sees the global tokens t < L - T + i + 1.

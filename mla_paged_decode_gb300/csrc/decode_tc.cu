@@ -25,7 +25,10 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int gro
   tp.groups_per_page = groups_per_page;
   cudaError_t e = p.kv_e4m3 ? launch_tc_variants<true>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
                             : launch_tc_variants<false>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
-  return e == cudaSuccess ? launch_split_merge(p, grid, stream) : e;
+  if (e != cudaSuccess) return e;
+  // all partitions in one launch: the split merge also combines the partitions
+  return p.fused && p.comb_out ? launch_dcp_merge_combine(p, grid, stream)
+                               : launch_split_merge(p, grid, stream);
 }
 
 }  // namespace mla

@@ -1016,6 +1016,7 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
 }
 
 cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_dcp_merge_combine(const DecodeParams &p, int grid, cudaStream_t stream);
 
 template <bool F8, bool FUSED, bool MULTI, int AHEAD>
 static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
