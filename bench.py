@@ -189,6 +189,33 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+GRAPH_CALLS = 20  # calls captured in one graph
+
+
+def graph_time(call, dev, stream, steps: int) -> float:
+    """Milliseconds for `steps` calls of call(stream) replayed from CUDA
+    graphs of GRAPH_CALLS calls each (3 replays of warm-up first)."""
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for _ in range(GRAPH_CALLS):
+            call(cap)
+    stream.wait_stream(cap)
+    replays = max(1, steps // GRAPH_CALLS)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) * steps / (replays * GRAPH_CALLS)
+
+
 def cpu_baseline(case, seconds: float):
     """The fp64 oracle, as it stands, on whole requests of the same workload
     until ``seconds`` of CPU time have passed."""
@@ -268,6 +295,14 @@ def run_ours(args, world, rank, local):
     clock_info = clocks.stop()
     ms = t_start.elapsed_time(t_end)
     ms_max = max_over_ranks(ms, world, dev)
+    assert mla.check_workspace(ws) == 0
+
+    # The same calls replayed from a CUDA graph (reported separately): the
+    # host's launch work leaves the timed region.
+    graph_ms = graph_time(lambda st: mla.decode_partial(
+        case.q, case.kv_pages, case.block_table, case.seq_lens, 0, 1, case.sm_scale, 0, out, lse,
+        workspace=ws, stream=st), dev, stream, args.steps)
+    graph_ms_max = max_over_ranks(graph_ms, world, dev)
     assert mla.check_workspace(ws) == 0
 
     # end to end through the C ABI with host buffers: pinned H2D inputs, D2H results
@@ -399,6 +434,9 @@ def run_ours(args, world, rank, local):
                         "copies double-buffered on two copy streams, overlapping the "
                         "neighbouring steps' decode (a serving loop); serial_value: every "
                         "copy and the decode in sequence on one stream"},
+        "graph": {"value": aggregate(graph_ms_max, args.steps, B, world), "unit": "tokens/s",
+                  "ms_per_step": graph_ms_max / args.steps, "calls_per_graph": GRAPH_CALLS,
+                  "note": "the same calls replayed from CUDA graphs (not the headline)"},
         # each mla_decode_partial call launches the decode kernel and the split merge
         "gpu_launches": 2 * args.steps,
         "clocks": clock_info,
@@ -807,13 +845,72 @@ def run_fp8(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def run_combine(args, world, rank, local):
+    """--op combine: mla_lse_combine alone on the micro-benchmark shapes (P=8,
+    H=16, D=512, T in {1, 8, 16, 32, 64, 128} tokens; partials N(0, 1) bf16,
+    lse N(5, 3), one partition per token holding the neutral pair), each
+    call replayed from CUDA graphs so that the small launches are timed on
+    the device.  value: GB/s at T = 128; every T in `points`."""
+    import mla_paged_decode_gb300 as mla
+    from mla_paged_decode_gb300 import build
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    if rank == 0 or not os.path.exists(mla.library_path()):
+        build.build()
+    barrier(world)
+    mla.load_library()
+    stream = torch.cuda.current_stream(dev)
+    P, H, D = 8, 16, 512
+    points = []
+    for T in (1, 8, 16, 32, 64, 128):
+        c = workloads.combine_case(T, num_parts=P, heads=H, dim=D, seed=args.seed, device=dev)
+        out = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+        out_lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+
+        def call(st, c=c, out=out, out_lse=out_lse):
+            mla.lse_combine(c.partials, c.lses, P, out, lse_base=mla.LSE_NATURAL,
+                            out_lse=out_lse, stream=st)
+
+        for _ in range(args.warmup):
+            call(stream)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(graph_time(call, dev, stream, args.steps), world, dev)
+        us = ms * 1e3 / args.steps
+        nbytes = c.partials.numel() * 2 + c.lses.numel() * 4 + out.numel() * 2 + out_lse.numel() * 4
+        points.append({"tokens": T, "us_per_call": us, "gbs": nbytes / us / 1e3,
+                       "bytes_per_call": nbytes})
+    peak, peak_kind = measured_peaks()
+    top = points[-1]
+    line = {
+        "metric": "MLA LSE combine GB/s (P=8, H=16, D=512) on 1 GB300",
+        "value": top["gbs"] * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": top["us_per_call"] / 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "combine_p8_h16_d512", "points": points,
+                   "timing": "CUDA graphs of %d calls, replayed" % GRAPH_CALLS},
+        "roofline": {"bound": "hbm", "achieved": top["gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": top["gbs"] / peak, "peak_source": peak_kind, "traffic": None,
+                     "kernel": "lse_combine_kernel at T = 128 (latency-bound below)"},
+        "e2e": {"value": None, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "note": "a device-only micro-benchmark"},
+        "gpu_launches": args.steps * len(points),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["decode", "dcp8", "fp8", "kv_append"], default="decode",
+    ap.add_argument("--op", choices=["decode", "dcp8", "fp8", "kv_append", "combine"],
+                    default="decode",
                     help="decode (the headline), dcp8 (the 8-partition DCP workload in one "
                          "mla_decode_dcp call), fp8 (the e4m3-cache workload), or the KV "
                          "append of one row per request")
@@ -837,6 +934,12 @@ def main(argv=None):
                               "the append's CPU oracle is reported as cpu_baseline of --op kv_append"}))
             return
         run_append(args, world, rank, local)
+    elif args.op == "combine":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the combine's oracle is pinned in tests/test_oracle_pins.py"}))
+            return
+        run_combine(args, world, rank, local)
     elif args.op == "fp8":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
