@@ -189,6 +189,51 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def gpu_setup(world: int, rank: int, local: int):
+    """This rank's device and current stream, the process group, and the
+    in-tree library (built by rank 0, or by any rank that finds it missing)."""
+    import mla_paged_decode_gb300 as mla
+    from mla_paged_decode_gb300 import build
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    if rank == 0 or not os.path.exists(mla.library_path()):
+        build.build()
+    barrier(world)
+    mla.load_library()
+    return mla, dev, torch.cuda.current_stream(dev)
+
+
+def timed_steps(step, steps: int, warmup: int, world: int, dev, stream, sample_clocks=False,
+                side_streams=(), tail=None):
+    """`warmup` untimed calls of step(), then exactly `steps` timed ones,
+    bracketed by a barrier and a synchronize on both sides and timed with CUDA
+    events on `stream` (which side streams wait for before their first copy;
+    `tail` runs after the last step, inside the region).  Returns the
+    milliseconds (max over ranks) and the clock record (or None)."""
+    for _ in range(warmup):
+        step()
+    if tail:
+        tail()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index) if sample_clocks else None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for st in side_streams:
+        st.wait_event(e0)
+    for _ in range(steps):
+        step()
+    if tail:
+        tail()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    info = clocks.stop() if clocks else None
+    return max_over_ranks(e0.elapsed_time(e1), world, dev), info
+
+
 GRAPH_CALLS = 20  # calls captured in one graph
 
 
@@ -253,16 +298,7 @@ def _oracle_threads() -> int:
 # ---------------------------------------------------------------- the two arms
 
 def run_ours(args, world, rank, local):
-    import mla_paged_decode_gb300 as mla
-    from mla_paged_decode_gb300 import build
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    init_dist(world, "nccl")
-    if rank == 0 or not os.path.exists(mla.library_path()):
-        build.build()
-    barrier(world)
-    mla.load_library()
-
+    mla, dev, stream = gpu_setup(world, rank, local)
     case = workloads.config_long32k(device=dev, seed=args.seed, batch=args.batch,
                                     pool_pages=args.pool_pages)
     if args.batch != 64 or args.pool_pages != 40000:
@@ -272,29 +308,13 @@ def run_ours(args, world, rank, local):
     out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
     ws = mla.make_workspace(case.q, case.kv_pages, case.block_table)
-    stream = torch.cuda.current_stream(dev)
 
     def step():
         mla.decode_partial(case.q, case.kv_pages, case.block_table, case.seq_lens, 0, 1,
                            case.sm_scale, 0, out, lse, workspace=ws, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for _ in range(args.steps):
-        step()
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clock_info = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
-    ms_max = max_over_ranks(ms, world, dev)
+    ms_max, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
+                                     sample_clocks=True)
     assert mla.check_workspace(ws) == 0
 
     # The same calls replayed from a CUDA graph (reported separately): the
@@ -324,29 +344,9 @@ def run_ours(args, world, rank, local):
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
-    def timed(step_fn, tail=None, side_streams=()):
-        for _ in range(max(3, args.warmup)):
-            step_fn()
-        if tail:
-            tail()
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for st in side_streams:  # no copy starts before the region does
-            st.wait_event(e0)
-        for _ in range(args.steps):
-            step_fn()
-        if tail:
-            tail()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        return max_over_ranks(e0.elapsed_time(e1), world, dev)
-
     with torch.cuda.stream(stream):
-        e_serial_ms = timed(e2e_step)
+        e_serial_ms, _ = timed_steps(e2e_step, args.steps, max(3, args.warmup), world, dev,
+                                     stream)
     assert torch.isfinite(out_h.float()).all()
 
     # The same steps as a serving loop runs them: double-buffered device inputs
@@ -390,12 +390,13 @@ def run_ours(args, world, rank, local):
         for bb in bufs:
             stream.wait_event(bb["ev_out"])
 
-    e_ms_max = timed(e2e_pipelined_step, drain, (h2d_s, d2h_s))
+    e_ms_max, _ = timed_steps(e2e_pipelined_step, args.steps, max(3, args.warmup), world, dev,
+                              stream, side_streams=(h2d_s, d2h_s), tail=drain)
     for bb in bufs:
         assert torch.equal(bb["out_h"].view(torch.int16), out_h.view(torch.int16))
 
     value = aggregate(ms_max, args.steps, B, world)
-    avg_launch_s = ms / 1e3 / args.steps
+    avg_launch_s = ms_max / 1e3 / args.steps
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / avg_launch_s / 1e9
     flops = float(case.seq_lens.sum().item()) * H * (2 * 576 + 2 * 512)
@@ -518,15 +519,7 @@ def _append_subcache(case_bits_, B):
 def run_append(args, world, rank, local):
     """--op kv_append: one new cache row per request of the headline batch
     (each request's last token rewritten, so its table needs no new page)."""
-    import mla_paged_decode_gb300 as mla
-    from mla_paged_decode_gb300 import build
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    init_dist(world, "nccl")
-    if rank == 0 or not os.path.exists(mla.library_path()):
-        build.build()
-    barrier(world)
-    mla.load_library()
+    mla, dev, stream = gpu_setup(world, rank, local)
     case = workloads.config_long32k(device=dev, seed=args.seed, batch=args.batch,
                                     pool_pages=args.pool_pages)
     B = case.batch
@@ -534,25 +527,13 @@ def run_append(args, world, rank, local):
     g = torch.Generator().manual_seed(args.seed + 1)
     new = torch.randn(B, 576, generator=g).to(torch.bfloat16).to(dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
     def step():
         mla.kv_append(new, case.kv_pages, case.block_table, pos, 0, 1, error_word=err,
                       stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clocks = ClockSampler(local)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    clock_info = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
+                                 sample_clocks=True)
     assert int(err.item()) == 0
     # end to end: the new rows and positions from pinned host memory, the error word back
     new_h, pos_h = new.cpu().pin_memory(), pos.cpu().pin_memory()
@@ -566,16 +547,7 @@ def run_append(args, world, rank, local):
                       stream=stream)
         err_h.copy_(err, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e_ms, _ = timed_steps(e2e_step, args.steps, 3, world, dev, stream)
     per_s = ms / 1e3 / args.steps
     byts = B * (1152 + 1152 + 8)   # new row read, cache row written, position + table entry
     peak, peak_kind = measured_peaks()
@@ -624,15 +596,7 @@ def run_dcp8(args, world, rank, local):
     """--op dcp8: the decode-context-parallel workload (B=64, H=16, P=8; 60
     requests of 131072 tokens and four of 1, 3, 5, 7) as one mla_decode_dcp
     call per step: every partition's (out, lse) and their combine."""
-    import mla_paged_decode_gb300 as mla
-    from mla_paged_decode_gb300 import build
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    init_dist(world, "nccl")
-    if rank == 0 or not os.path.exists(mla.library_path()):
-        build.build()
-    barrier(world)
-    mla.load_library()
+    mla, dev, stream = gpu_setup(world, rank, local)
     case = workloads.config_dcp8(device=dev, seed=args.seed)
     B, H, P = case.batch, case.heads, case.num_parts
     kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
@@ -641,25 +605,13 @@ def run_dcp8(args, world, rank, local):
     plse = torch.empty(P, B, 1, H, dtype=torch.float32, device=dev)
     out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
     out_lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
     def step(q=case.q, bt=case.block_table, sl=case.seq_lens):
         mla.decode_dcp(q, case.kv_pages, bt, sl, P, case.sm_scale, 1, partials=parts,
                        partial_lses=plse, out=out, out_lse=out_lse, workspace=ws, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clocks = ClockSampler(local)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    clock_info = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
+                                 sample_clocks=True)
     assert mla.check_workspace(ws) == 0
     q_h, bt_h, sl_h = (case.q.cpu().pin_memory(), case.block_table.cpu().pin_memory(),
                        case.seq_lens.cpu().pin_memory())
@@ -675,16 +627,7 @@ def run_dcp8(args, world, rank, local):
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(out_lse, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e_ms, _ = timed_steps(e2e_step, args.steps, 3, world, dev, stream)
     per_s = ms / 1e3 / args.steps
     peak, peak_kind = measured_peaks()
     tpeak, tpeak_kind = measured_bf16_tflops()
@@ -743,15 +686,7 @@ def run_fp8(args, world, rank, local):
     median 8192, per-tensor scale, P=1) through mla_decode_partial.  Its
     roofline is the tensor pipe: the MMAs run on f16 operands expanded from
     the cache, and each 64-head group reads the cache again."""
-    import mla_paged_decode_gb300 as mla
-    from mla_paged_decode_gb300 import build
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    init_dist(world, "nccl")
-    if rank == 0 or not os.path.exists(mla.library_path()):
-        build.build()
-    barrier(world)
-    mla.load_library()
+    mla, dev, stream = gpu_setup(world, rank, local)
     case = workloads.config_fp8(device=dev, seed=args.seed, batch=args.batch)
     if args.batch != 128:
         case.name += f"_b{args.batch}"
@@ -761,25 +696,13 @@ def run_fp8(args, world, rank, local):
     ws = mla.make_workspace(case.q, case.kv_pages, case.block_table, case.kv_scale)
     out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
     def step(q=case.q, bt=case.block_table, sl=case.seq_lens):
         mla.decode_partial(q, case.kv_pages, bt, sl, 0, 1, case.sm_scale, 0, out, lse,
                            kv_scale=case.kv_scale, workspace=ws, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clocks = ClockSampler(local)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    clock_info = clocks.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
+                                 sample_clocks=True)
     assert mla.check_workspace(ws) == 0
     q_h, bt_h, sl_h = (case.q.cpu().pin_memory(), case.block_table.cpu().pin_memory(),
                        case.seq_lens.cpu().pin_memory())
@@ -795,16 +718,7 @@ def run_fp8(args, world, rank, local):
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e_ms, _ = timed_steps(e2e_step, args.steps, 3, world, dev, stream)
     per_s = ms / 1e3 / args.steps
     peak, peak_kind = measured_peaks()
     tpeak, tpeak_kind = measured_bf16_tflops()
@@ -851,16 +765,7 @@ def run_combine(args, world, rank, local):
     lse N(5, 3), one partition per token holding the neutral pair), each
     call replayed from CUDA graphs so that the small launches are timed on
     the device.  value: GB/s at T = 128; every T in `points`."""
-    import mla_paged_decode_gb300 as mla
-    from mla_paged_decode_gb300 import build
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    init_dist(world, "nccl")
-    if rank == 0 or not os.path.exists(mla.library_path()):
-        build.build()
-    barrier(world)
-    mla.load_library()
-    stream = torch.cuda.current_stream(dev)
+    mla, dev, stream = gpu_setup(world, rank, local)
     P, H, D = 8, 16, 512
     points = []
     for T in (1, 8, 16, 32, 64, 128):
