@@ -204,6 +204,23 @@ int mla_decode_partial_noalloc(const void *q, const void *kv_pages, const int32_
                                const mla_decode_desc *d, mla_stream_t stream);
 
 /*
+ * Self-test of the bounded waits every kernel here uses (no GPU fault
+ * involved): launches one CTA whose two warps wait on shared-memory barriers
+ * that nothing completes.  Warp 0 gives up after `timeout_ns` (1 us .. 0.1 s)
+ * and raises the CTA's abort flag; warp 1, whose own limit is ten times
+ * longer, must give up as soon as it sees the flag.  Each warp that gave up
+ * sets bit 8 + warp of the workspace's error word, and MLA_ERR_TIMEOUT is
+ * reported by mla_decode_check_workspace, which also clears the word.
+ *
+ *  workspace   any decode workspace (256-byte aligned); only its error word
+ *              is written.
+ *
+ * Returns MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_ARG (timeout out of range),
+ * MLA_ERR_CUDA, or MLA_OK once the kernel is enqueued.
+ */
+int mla_selftest_bounded_wait(void *workspace, int64_t timeout_ns, mla_stream_t stream);
+
+/*
  * Waits for `stream`, reads and clears the device error word of `workspace`.
  * Returns MLA_OK, MLA_ERR_TIMEOUT, MLA_ERR_BOUNDS, or MLA_ERR_CUDA.  (The one call that
  * synchronises; meant for tests and debugging.)

@@ -96,6 +96,8 @@ def load_library():
         lib.mla_last_cuda_error.restype = ctypes.c_char_p
         lib.mla_version.argtypes = []
         lib.mla_version.restype = i32
+        lib.mla_selftest_bounded_wait.argtypes = [vp, ctypes.c_int64, vp]
+        lib.mla_selftest_bounded_wait.restype = i32
         _lib = lib
         return lib
 
@@ -344,6 +346,15 @@ def check_workspace(workspace: torch.Tensor, stream=None) -> int:
     if st not in (0, -9):
         _check(st)
     return st
+
+
+def selftest_bounded_wait(workspace: torch.Tensor, timeout_ns: int, stream=None) -> None:
+    """mla_selftest_bounded_wait: two warps wait on barriers that nothing
+    completes; the waits give up (after timeout_ns, and on the abort flag)
+    and report MLA_ERR_TIMEOUT in the workspace's error word."""
+    with torch.cuda.device(workspace.device):
+        _check(load_library().mla_selftest_bounded_wait(
+            workspace.data_ptr(), int(timeout_ns), _stream_ptr(stream, workspace.device)))
 
 
 def lse_combine(partials, lses, num_parts: int, out, *, lse_base: int = LSE_NATURAL,

@@ -23,7 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libmla_decode.so")
 SOURCES = ["api.cu", "decode_simt.cu", "decode_tc.cu", "decode_tc_bf16.cu", "decode_tc_e4m3.cu",
-           "split_merge.cu", "lse_combine.cu", "noalloc.cu", "kv_append.cu", "dcp_metadata.cu"]
+           "split_merge.cu", "lse_combine.cu", "noalloc.cu", "kv_append.cu", "dcp_metadata.cu",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

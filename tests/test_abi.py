@@ -222,3 +222,11 @@ def test_several_query_tokens_need_the_tensor_core_path(lib):
     # num_parts = 3 runs the CUDA-core kernel, which takes one query token
     assert _partial(lib, _desc(q_len=2), part_id=0, num_parts=3) == -2
     assert _dcp(lib, _desc(q_len=4), num_parts=3) == -2
+
+
+def test_selftest_rejects_bad_arguments(lib):
+    lib.mla_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    assert lib.mla_selftest_bounded_wait(None, 10**6, None) == -1
+    assert lib.mla_selftest_bounded_wait(FAKE + 16, 10**6, None) == -4
+    assert lib.mla_selftest_bounded_wait(FAKE, 10, None) == -6
+    assert lib.mla_selftest_bounded_wait(FAKE, 2 * 10**8, None) == -6
