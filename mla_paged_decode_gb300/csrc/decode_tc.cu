@@ -13,8 +13,6 @@ extern template cudaError_t launch_tc_variants<true>(
     const TcParams &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, int,
     cudaStream_t);
 
-int tc_smem_bytes() { return tc::kSmemBytes; }
-
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
                              const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
                              const CUtensorMap &tm_kvg, int grid, cudaStream_t stream) {

@@ -52,17 +52,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking: has the phase of parity `parity` completed?
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits for the phase of parity `parity` to complete.  Gives up after
 // `timeout_ns` or as soon as *abort is set; on a timeout it sets *abort.
 // Returns false if it gave up.
@@ -284,17 +273,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 // Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Named barrier of `count` threads that also ORs `pred` over them.
-__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, %2, %3, pi; selp.u32 %0, 1, 0, po; }"
-      : "=r"(r)
-      : "r"(uint32_t(pred)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
 }
 
 // Named barrier of `count` threads that ANDs `pred` over them.
