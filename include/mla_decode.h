@@ -51,7 +51,8 @@ typedef struct CUstream_st *mla_stream_t; /* == cudaStream_t */
 enum mla_status {
   MLA_OK = 0,
   MLA_ERR_NULL = -1,      /* a required pointer is NULL                           */
-  MLA_ERR_SHAPE = -2,     /* unsupported size: q_len != 1, Dqk != 576, Dv != 512,
+  MLA_ERR_SHAPE = -2,     /* unsupported size: q_len outside 1..16 (or > 1 off the
+                             tensor-core path), Dqk != 576, Dv != 512,
                              page_size != 64, heads not in [1, 128], ...          */
   MLA_ERR_PARTITION = -3, /* num_parts < 1 or part_id outside [0, num_parts)      */
   MLA_ERR_ALIGN = -4,     /* q / kv_pages / out / partials not 16-byte aligned,
@@ -81,7 +82,7 @@ enum mla_kv_dtype {
 typedef struct mla_decode_desc {
   int32_t batch;             /* B, number of requests (0 is a no-op)              */
   int32_t num_heads;         /* H, query heads per request, 1..128                */
-  int32_t q_len;             /* query tokens per request; must be 1               */
+  int32_t q_len;             /* query tokens per request, 1..16 (see below)       */
   int32_t head_dim_qk;       /* must be 576 (512 latent + 64 rope)                */
   int32_t head_dim_v;        /* must be 512 (the latent)                          */
   int32_t page_size;         /* tokens per cache page; must be 64                 */
@@ -104,7 +105,7 @@ size_t mla_decode_workspace_size(const mla_decode_desc *d, int num_sms);
 /*
  * Partition `part_id` of `num_parts` of MLA absorbed decode attention.
  *
- *  q           bf16 [B, 1, H, 576], contiguous.  Dims 0..511 latent, 512..575 rope.
+ *  q           bf16 [B, q_len, H, 576], contiguous.  Dims 0..511 latent, 512..575 rope.
  *  kv_pages    [num_pages, 64, 576] rows of the GLOBAL paged cache, contiguous,
  *              bf16 or e4m3 bytes per d->kv_dtype.  Row dims 0..511 are also
  *              the value (the latent).
@@ -119,19 +120,25 @@ size_t mla_decode_workspace_size(const mla_decode_desc *d, int num_sms);
  *              local pages and local lengths.
  *  sm_scale    softmax scale applied to q.k (finite).
  *  lse_base    enum mla_lse_base of the returned lse.
- *  out         bf16 [B, 1, H, 512]: softmax(sm_scale q K^T) V over the owned
+ *  out         bf16 [B, q_len, H, 512]: softmax(sm_scale q K^T) V over the owned
  *              tokens, rounded to nearest even.  All of it is written.
- *  lse         fp32 [B, 1, H]: log-sum-exp of the scaled scores in `lse_base`.
+ *  lse         fp32 [B, q_len, H]: log-sum-exp of the scaled scores in `lse_base`.
  *              A request for which the partition owns no token gets out = 0 and
  *              lse = -inf (the neutral pair of the LSE merge).
  *  workspace   scratch of >= mla_decode_workspace_size(d, 0) bytes, 256-byte
  *              aligned, its first 256 bytes zero before first use (see above).
  *
  * Enqueues two kernels on `stream`: the decode kernel and the merge of the
- * requests its schedule split across SMs.
+ * requests its schedule split across SMs.  The tensor-core kernel serves
+ * every num_parts with num_parts / gcd(num_parts, 8) <= 16: it gathers
+ * partition part_id mod g of g = gcd(num_parts, 8) and, when g < num_parts,
+ * drops the tokens the other partitions own (reading num_parts / g times
+ * the partition's own bytes).  Larger ratios run a CUDA-core kernel.
  *
- * Single-token decode only: q_len != 1 is rejected with MLA_ERR_SHAPE, the
- * analogue of the DCP kernel gate that refuses multi-token (causal) requests.
+ * Several query tokens (q_len = T > 1; tensor-core path only, else
+ * MLA_ERR_SHAPE): the request's queries are its last T tokens, and query
+ * token i attends causally to the owned tokens t < L_b - T + i + 1; a query
+ * row that sees no owned token gets the neutral pair.
  * Block-table entries outside [0, num_pages) and lengths outside
  * [0, 64 * max_pages_per_seq] are not dereferenced: the kernel skips them and
  * records MLA_ERR_BOUNDS in the workspace (read it with
@@ -185,7 +192,8 @@ int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_tab
  * device synchronisation an allocation may cause, and plain-C hosts with no
  * allocator of their own.
  *
- * Same arguments, layouts and results as mla_decode_partial.  Its scratch is
+ * Same arguments, layouts and results as mla_decode_partial, for one query
+ * token per request (q_len = 1; other values return MLA_ERR_SHAPE).  Its scratch is
  * a ~40 MB array built into the library, which every GPU that loads the
  * library keeps until the process exits; it calls no cudaMalloc, cudaFree or
  * other allocating routine.  The first call on a device takes that device's

@@ -116,9 +116,23 @@ constexpr int kTcHeadsPerGroup = 64;
 
 // The tensor-core kernel takes partitions whose owned rows of a page form
 // whole 8-row groups (P | 8), for bf16 and e4m3 caches alike.
-bool tensor_core_path(const mla_decode_desc *, int num_parts) {
-  return num_parts == 1 || num_parts == 2 || num_parts == 4 || num_parts == 8;
+// The tensor-core kernel gathers partition r mod g of g = gcd(P, 8) (g divides
+// a page's 8 atoms) and, when g < P, drops the tokens other partitions own:
+// it reads P / g times the partition's own bytes at the tensor-core rate,
+// which beats the CUDA-core kernel while P / g stays small.
+int gather_parts(int num_parts) {
+  int g = 8, a = num_parts;
+  while (a) { const int t = g % a; g = a; a = t; }
+  return g;
 }
+constexpr int kMaxOwnerRatio = 16;  // P / gather_parts(P) served by the tensor cores
+
+bool tensor_core_path(const mla_decode_desc *, int num_parts) {
+  return num_parts >= 1 && num_parts / gather_parts(num_parts) <= kMaxOwnerRatio;
+}
+
+// all partitions in one decode launch: P divides 8 (no owner mask)
+bool fused_path(int num_parts) { return num_parts >= 1 && 8 % num_parts == 0; }
 
 // Q as [B*H rows, 576] bf16, one 64-column swizzled box of min(64, H) rows;
 // partition rows of a bf16 cache as a 5-D view (64 dims, 8 rows of stride P,
@@ -234,7 +248,7 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
                    void *workspace, int grid, cudaStream_t s, void *comb_out = nullptr,
                    float *comb_lse = nullptr) {
   const bool tc = tensor_core_path(d, num_parts);
-  if (fused && !tc) return MLA_ERR_ARG;
+  if (fused && !fused_path(num_parts)) return MLA_ERR_ARG;
   if (d->q_len > 1 && !tc) return MLA_ERR_SHAPE;
   const int per_group = tc ? kTcHeadsPerGroup : kSimtHeadsPerGroup;
   const int rows = rows_of(d);
@@ -259,6 +273,13 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
   p.max_pages = d->max_pages_per_seq;
   p.part_id = fused ? 0 : part_id;
   p.num_parts = num_parts;
+  const int gp = tc ? gather_parts(num_parts) : num_parts;
+  if (gp < num_parts) {  // owner mask over the gather of partition part_id mod gp of gp
+    p.num_parts = gp;
+    p.part_id = part_id % gp;
+    p.own_parts = num_parts;
+    p.own_part = part_id;
+  }
   p.fused = fused ? 1 : 0;
   p.req_batch = d->batch;
   p.comb_out = static_cast<__nv_bfloat16 *>(comb_out);
@@ -270,11 +291,12 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
   cudaError_t e;
   if (tc) {
     CUtensorMap tm_q, tm_kv, tm_kvg;
-    int st = make_tensor_maps(q, kv_pages, d, part_id, num_parts, fused, &tm_q, &tm_kv, &tm_kvg);
+    int st = make_tensor_maps(q, kv_pages, d, p.part_id, p.num_parts, fused, &tm_q, &tm_kv,
+                              &tm_kvg);
     if (st != MLA_OK) return st;
     const int h = rows < kTcHeadsPerGroup ? rows : kTcHeadsPerGroup;
     const int npv = ((h + 15) / 16) * 16;
-    e = mla::launch_decode_tc(p, npv, h, 8 / num_parts, tm_q, tm_kv, tm_kvg, grid, s);
+    e = mla::launch_decode_tc(p, npv, h, 8 / p.num_parts, tm_q, tm_kv, tm_kvg, grid, s);
   } else {
     e = mla::launch_decode_simt(p, grid, s);
   }
@@ -303,7 +325,7 @@ const char *mla_status_string(int status) {
   switch (status) {
     case MLA_OK: return "ok";
     case MLA_ERR_NULL: return "a required pointer is NULL";
-    case MLA_ERR_SHAPE: return "unsupported shape (q_len 1..16, and 1 unless num_parts divides 8; Dqk 576, Dv 512, page 64, heads 1..128)";
+    case MLA_ERR_SHAPE: return "unsupported shape (q_len 1..16, and 1 off the tensor-core path: num_parts / gcd(num_parts, 8) > 16; Dqk 576, Dv 512, page 64, heads 1..128)";
     case MLA_ERR_PARTITION: return "bad partition (need num_parts >= 1 and 0 <= part_id < num_parts)";
     case MLA_ERR_ALIGN: return "misaligned pointer (16 B for tensors, 256 B for the workspace)";
     case MLA_ERR_WORKSPACE: return "workspace too small";
@@ -395,7 +417,7 @@ int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_tab
     return MLA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t rows = size_t(d->batch) * rows_of(d);
-  if (tensor_core_path(d, num_parts)) {
+  if (fused_path(num_parts)) {
     // every partition in one decode launch, then one kernel that merges the
     // splits and combines the partitions
     return enqueue_decode(q, kv_pages, block_table, seq_lens, 0, num_parts, true, sm_scale,

@@ -66,6 +66,12 @@ struct DecodeParams {
   // `heads` rows of a request are then q_len x q_heads, row i * q_heads + h
   // for query token i, and token i of T sees the global tokens t < L - T + i + 1.
   int q_len = 1, q_heads = 0;
+  // Owner mask (tensor-core kernel only): when own_parts > num_parts the call
+  // computes partition own_part of own_parts through the gather of partition
+  // part_id = own_part mod num_parts of num_parts (num_parts divides both 8
+  // and own_parts), and the softmax drops every gathered token whose global
+  // index is not own_part mod own_parts.  Otherwise own_parts = 0.
+  int own_parts = 0, own_part = 0;
   int kv_e4m3;
   float kv_scale;             // 1 for bf16
   float score_scale_log2;     // sm_scale * log2(e): scores kept in the base-2 domain
@@ -116,7 +122,38 @@ __device__ __forceinline__ int request_len(const DecodeParams &p, int v, int *er
   int bv = v / p.head_groups;
   int L = checked_len(p, req_of(p, bv), err);
   if (MULTI) L = group_len(p, L, v % p.head_groups);
+  // under an owner mask, a request the real partition owns no token of is
+  // empty (the neutral pair), however many the gathered partition holds
+  if (MULTI && p.own_parts > p.num_parts && local_len(L, p.own_parts, p.own_part) == 0) return 0;
   return local_len(L, p.num_parts, part_of(p, bv));
+}
+
+// Kernels whose rows may differ in the tokens they see: several query
+// tokens per request, or an owner mask.
+__host__ __device__ __forceinline__ bool multi_rows(const DecodeParams &p) {
+  return p.q_len > 1 || p.own_parts > p.num_parts;
+}
+
+// Owner mask of the gathered partition's tiles.  Local token j of partition
+// part_id of num_parts is global token part_id + j * num_parts; with
+// Q = own_parts / num_parts it belongs to own_part when j = c mod Q,
+// c = own_part / num_parts.  bits(t): bit i set when local token 64t + i is
+// owned.
+struct OwnerMask {
+  unsigned long long comb;  // bits 0, Q, 2Q, ... below 64
+  int q, c;
+  __device__ __forceinline__ unsigned long long bits(long long t) const {
+    return comb << int(((long long)c - (64 * t) % q + q) % q);
+  }
+};
+
+__device__ inline OwnerMask owner_mask_of(const DecodeParams &p) {
+  OwnerMask o;
+  o.q = p.own_parts / p.num_parts;
+  o.c = p.own_part / p.num_parts;
+  o.comb = 0;
+  for (int j = 0; j < 64; j += o.q) o.comb |= 1ull << j;
+  return o;
 }
 
 template <bool MULTI = false>

@@ -517,6 +517,10 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
   float cs = p.score_scale_log2 * p.kv_scale;
   uint32_t kv_it = 0, p_it = 0, o_it = 0;
   bool ok = true;
+  // an owner mask: the gathered tiles hold other partitions' tokens too
+  const bool masked = MULTI && p.own_parts > p.num_parts;
+  OwnerMask own{};
+  if (masked) own = owner_mask_of(p);
 
   Walk<FUSED, MULTI> w(p, r);
   for (; ok && w.next(); w.advance()) {
@@ -568,6 +572,15 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
           const int tok = 8 * (k >> 1) + pair, lim = (k & 1) ? nv1 : nv0;
           xp[k].x = tok < lim ? xp[k].x : -INFINITY;
           xp[k].y = tok + 1 < lim ? xp[k].y : -INFINITY;
+        }
+      }
+      if (MULTI && masked) {  // tokens another partition owns
+        const unsigned long long ob = own.bits(t);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int tok = 8 * (k >> 1) + pair;
+          xp[k].x = (ob >> tok) & 1ull ? xp[k].x : -INFINITY;
+          xp[k].y = (ob >> (tok + 1)) & 1ull ? xp[k].y : -INFINITY;
         }
       }
       float tmax[2];
@@ -1051,7 +1064,7 @@ template <bool F8>
 cudaError_t launch_tc_variants(const TcParams &tp, const CUtensorMap &tm_q,
                                const CUtensorMap &tm_kv, const CUtensorMap &tm_kvg, int grid,
                                cudaStream_t stream) {
-  const bool multi = tp.p.q_len > 1;
+  const bool multi = multi_rows(tp.p);
   if (tp.p.fused)
     return multi ? launch_tc<F8, true, true, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
                  : launch_tc<F8, true, false, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream);

@@ -219,9 +219,11 @@ def test_dcp_metadata_rejects_bad_arguments(lib):
 
 
 def test_several_query_tokens_need_the_tensor_core_path(lib):
-    # num_parts = 3 runs the CUDA-core kernel, which takes one query token
-    assert _partial(lib, _desc(q_len=2), part_id=0, num_parts=3) == -2
-    assert _dcp(lib, _desc(q_len=4), num_parts=3) == -2
+    # num_parts / gcd(num_parts, 8) > 16 runs the CUDA-core kernel, which
+    # takes one query token (17 / 1, 136 / 8); 3 and 48 / 8 stay on the tensor cores
+    assert _partial(lib, _desc(q_len=2), part_id=0, num_parts=17) == -2
+    assert _partial(lib, _desc(q_len=2), part_id=5, num_parts=136) == -2
+    assert _dcp(lib, _desc(q_len=4), num_parts=17) == -2
 
 
 def test_selftest_rejects_bad_arguments(lib):

@@ -43,6 +43,8 @@ CASES = [
     (128, 2, [800, 2, 65], 1, "bf16"),
     (8, 8, [8, 9, 200, 63], 2, "bf16"),
     (16, 4, [4, 900, 70, 1], 4, "e4m3"),
+    (32, 2, [3, 500, 90, 7], 3, "bf16"),               # owner mask: gather 1, keep 1 of 3
+    (16, 3, [1, 2, 5, 300, 130], 6, "e4m3"),           # gather 2, keep 1 of 3
 ]
 
 

@@ -79,6 +79,11 @@ SHAPES = [
     (128, [1300, 64, 1, 0, 511], 1, "bf16"),   # one page per tile, two head groups
     (1, [77, 3000, 2, 65], 1, "bf16"),
     (7, [129, 2, 1000], 1, "bf16"),
+    # P not dividing 8: gather partition r mod gcd(P, 8), drop other owners' tokens
+    (16, [1, 3, 5, 7, 511, 1025, 2049], 16, "bf16"),  # gather 8, keep 1 of 2
+    (32, [300, 2049, 17, 0], 6, "bf16"),              # gather 2, keep 1 of 3
+    (64, [700, 65, 1300], 12, "e4m3"),                # gather 4, keep 1 of 3
+    (16, [40, 999, 3, 70], 17, "bf16"),               # 17 / 1 > 16: the CUDA-core kernel
 ]
 
 
@@ -197,16 +202,17 @@ def test_bounds_are_checked_in_the_kernel():
 
 
 def test_multi_token_query_is_rejected_off_the_tensor_core_path():
-    """Several query tokens run on the tensor-core kernel only (P | 8); with
-    P = 3 the call is refused before launching."""
+    """Several query tokens run on the tensor-core kernel only; with P = 17
+    (17 / gcd(17, 8) > 16: the CUDA-core kernel) the call is refused before
+    launching."""
     case = workloads.config_small(device="cuda")
     q2 = torch.zeros(1, 2, 16, 576, dtype=torch.bfloat16, device="cuda")
     out = torch.empty(1, 2, 16, 512, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(1, 2, 16, dtype=torch.float32, device="cuda")
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table)
     with pytest.raises(mla.MlaError) as e:
-        mla.decode_partial(q2, case.kv_pages, case.block_table, case.seq_lens, 0, 3,
-                           case.sm_scale, 0, out, lse, workspace=torch.zeros(
-                               1 << 20, dtype=torch.uint8, device="cuda"))
+        mla.decode_partial(q2, case.kv_pages, case.block_table, case.seq_lens, 0, 17,
+                           case.sm_scale, 0, out, lse, workspace=ws)
     assert e.value.status == -2
 
 
