@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -759,6 +760,108 @@ def run_fp8(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def _line(args, world, ms, units, unit, config, roofline, e2e, launches, clock_info,
+          metric="MLA decode tokens/s and KV-read HBM GB/s (fraction of roofline) on 1 GB300"):
+    """The JSON line's common keys for `units` processed per step per rank."""
+    return {"metric": metric, "value": aggregate(ms, args.steps, units, world), "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clock_info}
+
+
+def _hbm_roofline(kv_bytes, ms, steps, kernel):
+    peak, peak_kind = measured_peaks()
+    gbs = kv_bytes / (ms / 1e3 / steps) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+            "peak_source": peak_kind, "frac_of_8tbs": gbs / 8000.0, "traffic": None,
+            "kernel": kernel}
+
+
+def run_dcp_parts(args, world, rank, local):
+    """--op dcp --parts P: the 32K-context batch (B=64, H=64, bf16) as P
+    round-robin partitions and their merge, one mla_decode_dcp call per step
+    (the tensor-core kernel: one launch for all partitions when P divides 8,
+    else one launch per partition with the owner mask when P / gcd(P, 8) <= 16,
+    else the CUDA-core kernel).  KV GB/s counts each cached row once."""
+    mla, dev, stream = gpu_setup(world, rank, local)
+    P = args.parts
+    case = workloads.config_long32k(device=dev, seed=args.seed)
+    B, H = case.batch, case.heads
+    kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
+    ws = mla.make_dcp_workspace(case.q, case.kv_pages, case.block_table, P)
+    parts = torch.empty(P, B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+    plse = torch.empty(P, B, 1, H, dtype=torch.float32, device=dev)
+    out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        mla.decode_dcp(case.q, case.kv_pages, case.block_table, case.seq_lens, P, case.sm_scale,
+                       0, partials=parts, partial_lses=plse, out=out, workspace=ws, stream=stream)
+
+    ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
+                                 sample_clocks=True)
+    assert mla.check_workspace(ws) == 0
+    g = math.gcd(P, 8)
+    path = ("one launch for all partitions" if 8 % P == 0 else
+            "one launch per partition, owner mask over the gather of partition r mod %d" % g
+            if P // g <= 16 else "the CUDA-core kernel, one launch per partition")
+    line = _line(args, world, ms, B, "tokens/s",
+                 {"workload": "long32k_b64_h64_bf16_p%d" % P, "batch": B, "heads": H, "q_len": 1,
+                  "num_parts": P, "path": path, "kv_bytes_per_step": kv_bytes,
+                  "l2": "inputs larger than L2: %.2f GB of KV per step" % (kv_bytes / 1e9),
+                  "parallelism": "DCP partitions emulated on one GPU"},
+                 _hbm_roofline(kv_bytes, ms, args.steps,
+                               "mla_decode_dcp: every partition's decode and the merge, timed "
+                               "together per call (rows gathered P / gcd(P, 8) times when P "
+                               "does not divide 8)"),
+                 {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0, "note": "device-only: see the decode op's e2e"},
+                 (2 if 8 % P == 0 else 2 * P + 1) * args.steps, clock_info)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_mtp(args, world, rank, local):
+    """--op mtp --q-len T: T query tokens per request (multi-token prediction
+    or target verify) on the 32K-context lengths, B=64, H=64, P=1; query token
+    i attends to the tokens before L - T + i + 1.  One 64-row group per query
+    token: the cache is walked once per group."""
+    mla, dev, stream = gpu_setup(world, rank, local)
+    T = args.q_len
+    case = workloads.config_long32k(device=dev, seed=args.seed, q_len=T)
+    B, H = case.batch, case.heads
+    kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table)
+    out = torch.empty(B, T, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, T, H, dtype=torch.float32, device=dev)
+
+    def step():
+        mla.decode_partial(case.q, case.kv_pages, case.block_table, case.seq_lens, 0, 1,
+                           case.sm_scale, 0, out, lse, workspace=ws, stream=stream)
+
+    ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
+                                 sample_clocks=True)
+    assert mla.check_workspace(ws) == 0
+    groups = -(-T * H // 64)
+    line = _line(args, world, ms, B * T, "query tokens/s",
+                 {"workload": "long32k_b64_h64_bf16_q%d" % T, "batch": B, "heads": H, "q_len": T,
+                  "num_parts": 1, "row_groups_per_request": groups, "kv_bytes_per_step": kv_bytes,
+                  "l2": "inputs larger than L2: %.2f GB of KV per step" % (kv_bytes / 1e9),
+                  "parallelism": "single GPU"},
+                 _hbm_roofline(kv_bytes * groups, ms, args.steps,
+                               "mla_decode_partial with %d query tokens: decode kernel + split "
+                               "merge; bytes = the KV once per 64-row group (%d)" % (T, groups)),
+                 {"value": None, "unit": "query tokens/s", "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0, "note": "device-only: see the decode op's e2e"},
+                 2 * args.steps, clock_info)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def run_combine(args, world, rank, local):
     """--op combine: mla_lse_combine alone on the micro-benchmark shapes (P=8,
     H=16, D=512, T in {1, 8, 16, 32, 64, 128} tokens; partials N(0, 1) bf16,
@@ -814,12 +917,14 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["decode", "dcp8", "fp8", "kv_append", "combine"],
+    ap.add_argument("--op", choices=["decode", "dcp8", "fp8", "kv_append", "combine", "dcp", "mtp"],
                     default="decode",
                     help="decode (the headline), dcp8 (the 8-partition DCP workload in one "
                          "mla_decode_dcp call), fp8 (the e4m3-cache workload), or the KV "
                          "append of one row per request")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--parts", type=int, default=3, help="partitions for --op dcp")
+    ap.add_argument("--q-len", type=int, default=2, help="query tokens per request for --op mtp")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
@@ -839,6 +944,12 @@ def main(argv=None):
                               "the append's CPU oracle is reported as cpu_baseline of --op kv_append"}))
             return
         run_append(args, world, rank, local)
+    elif args.op in ("dcp", "mtp"):
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the oracle of these workloads is the decode op's reference arm"}))
+            return
+        (run_dcp_parts if args.op == "dcp" else run_mtp)(args, world, rank, local)
     elif args.op == "combine":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
