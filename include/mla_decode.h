@@ -212,6 +212,14 @@ int mla_decode_partial_noalloc(const void *q, const void *kv_pages, const int32_
                                const mla_decode_desc *d, mla_stream_t stream);
 
 /*
+ * 1 if the library's kernels run on a GPU of compute capability
+ * major.minor (they are built for sm_103a only), else 0.  Every entry point
+ * that launches returns MLA_ERR_DEVICE on a device this refuses, before
+ * launching anything.
+ */
+int mla_arch_supported(int major, int minor);
+
+/*
  * Self-test of the bounded waits every kernel here uses (no GPU fault
  * involved): launches one CTA whose two warps wait on shared-memory barriers
  * that nothing completes.  Warp 0 gives up after `timeout_ns` (1 us .. 0.1 s)

@@ -79,7 +79,7 @@ DeviceFacts current_device(int *st, int *dev_out = nullptr) {
     f.major = mj;
     f.minor = mn;
   }
-  *st = (f.major == 10 && f.minor == 3) ? MLA_OK : MLA_ERR_DEVICE;
+  *st = mla_arch_supported(f.major, f.minor) ? MLA_OK : MLA_ERR_DEVICE;
   return f;
 }
 
@@ -320,6 +320,10 @@ int enqueue_partial(const void *q, const void *kv_pages, const int32_t *block_ta
 extern "C" {
 
 int mla_version(void) { return 100; }
+
+// The kernels are built for sm_103a only (arch-specific tcgen05 and TMA
+// forms): any other compute capability, sm_100 included, is refused.
+int mla_arch_supported(int major, int minor) { return major == 10 && minor == 3 ? 1 : 0; }
 
 const char *mla_status_string(int status) {
   switch (status) {

@@ -232,3 +232,25 @@ def test_selftest_rejects_bad_arguments(lib):
     assert lib.mla_selftest_bounded_wait(FAKE + 16, 10**6, None) == -4
     assert lib.mla_selftest_bounded_wait(FAKE, 10, None) == -6
     assert lib.mla_selftest_bounded_wait(FAKE, 2 * 10**8, None) == -6
+
+
+def test_arch_gate_takes_sm103_only(lib):
+    """The kernels are built for sm_103a: every other compute capability of the
+    family or around it is refused (MLA_ERR_DEVICE before any launch)."""
+    lib.mla_arch_supported.argtypes = [ctypes.c_int, ctypes.c_int]
+    assert lib.mla_arch_supported(10, 3) == 1
+    for major, minor in [(10, 0), (10, 1), (10, 2), (11, 0), (12, 0), (12, 1), (9, 0), (8, 9)]:
+        assert lib.mla_arch_supported(major, minor) == 0, (major, minor)
+
+
+def test_a_valid_call_without_a_gpu_returns_an_error():
+    """With every argument valid, a machine without a usable GPU gets a
+    status, not a crash (the device query fails before any launch)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the fake pointers must never reach a real launch")
+    lib = mla.load_library() if os.path.exists(mla.library_path()) else None
+    if lib is None:
+        pytest.skip("library not built")
+    st = _partial(lib, _desc())
+    assert st in (-7, -8), st   # MLA_ERR_CUDA or MLA_ERR_DEVICE
