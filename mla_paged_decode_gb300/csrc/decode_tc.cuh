@@ -28,15 +28,23 @@
 // MMAs then run with f16 operands, P is written as f16, and the scores carry
 // sm_scale * kv_scale / (that power of two).
 //
+// Partitions: P divides 8 here (64/P owned rows per page); a call for
+// another P runs the gather of P' = gcd(P, 8) with an owner mask in the
+// softmax (DecodeParams::own_parts), through the several-query-token
+// variants, which carry the per-row bounds and guards that mask needs.
+//
 // Pipeline per tile i (stage / S buffer i mod 2): producer -> kv_full (per
-// column group) -> MMA S_i (36 MMAs, two interleaved accumulators so consecutive MMAs are
-// independent) -> s_full -> softmax reads S_i, frees it (s_free), waits for
+// column group) -> MMA S_i (36 MMAs, two interleaved accumulators so
+// consecutive MMAs are independent) -> s_full -> softmax reads S_i, frees it (s_free), waits for
 // PV_{i-1} (p_free), rescales O^T only when some head's running max grew by
 // more than 2^8, writes P_i (bf16) -> p_full -> MMA PV_i (4 independent
 // value-dim chunks) -> kv_empty + p_free.  The score issuers start S_{i+1} as
 // soon as tile i+1 lands, so the score MMAs of the next tile overlap this
 // tile's softmax, and the producer keeps the pages of the next tile (two
-// ahead when a tile gathers several pages) streaming into L2.
+// ahead when a tile gathers several pages) streaming into L2.  The kernel is
+// launched as a programmatic dependent of the stream's previous kernel: its
+// prologue overlaps that kernel's tail, and griddepcontrol.wait precedes
+// every read of an input.
 #pragma once
 
 #include "common.cuh"
