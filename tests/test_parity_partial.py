@@ -260,3 +260,17 @@ def test_fp8_query_far_outside_f16_range(q_shift, num_parts):
     case.q = (case.q.float() * 2.0 ** q_shift).to(torch.bfloat16)
     case.sm_scale = case.sm_scale * 2.0 ** -q_shift
     _check_all(case, bases=(0,), atol=FP8_ATOL)
+
+
+@pytest.mark.parametrize("num_parts", [1, 3])
+def test_fp8_cache_of_subnormal_codes(num_parts):
+    """Every cached code has a zero exponent field: OCP e4m3 subnormals,
+    (m / 8) * 2^-6 times the scale.  With a scale of 64 they are ordinary
+    keys and values, and the kernel's f16 expansion must keep them exact; a
+    flush to zero anywhere would show in the relative-norm bound, which
+    holds for outputs of any magnitude."""
+    case = workloads.make_decode_case("fp8_subnormal", 64, [700, 65, 1300], seed=41,
+                                      device="cuda", kv_dtype="e4m3", num_parts=num_parts)
+    case.kv_pages &= 0x87
+    case.kv_scale = 64.0
+    _check_all(case, bases=(0, 1), atol=FP8_ATOL)
