@@ -107,6 +107,21 @@ def test_many_short_requests():
     _check_all(case, bases=(0,))
 
 
+@pytest.mark.parametrize("num_parts,kv_dtype", [(1, "bf16"), (2, "bf16"), (3, "bf16"), (8, "e4m3")])
+def test_requests_sharing_cache_pages(num_parts, kv_dtype):
+    """Block tables that alias physical pages, as a shared prompt prefix
+    does: requests 1 and 2 reuse request 0's first 40 and 39 pages, and
+    request 3 maps both of its logical pages to one physical page."""
+    lens = [3000, 3100, 2600, 128, 700]
+    case = workloads.make_decode_case("shared", 64, lens, seed=61, device="cuda",
+                                      kv_dtype=kv_dtype, num_parts=num_parts)
+    bt = case.block_table
+    bt[1, :40] = bt[0, :40]
+    bt[2, :39] = bt[0, :39]
+    bt[3, 1] = bt[3, 0]
+    _check_all(case, bases=(0,), atol=FP8_ATOL if kv_dtype == "e4m3" else None)
+
+
 def test_single_request_spread_over_every_cta():
     """One long request: every CTA holds a split, the last one merges them."""
     case = workloads.make_decode_case("one_long", 64, [150000], seed=21, device="cuda")
