@@ -131,8 +131,24 @@ bool tensor_core_path(const mla_decode_desc *, int num_parts) {
   return num_parts >= 1 && num_parts / gather_parts(num_parts) <= kMaxOwnerRatio;
 }
 
-// all partitions in one decode launch: P divides 8 (no owner mask)
-bool fused_path(int num_parts) { return num_parts >= 1 && 8 % num_parts == 0; }
+// A bf16 cache with one query token and P in {3, 5, 6, 7}: the tensor-core
+// kernel gathers exactly the partition's rows, with a TMA traversal stride of
+// P rows (at most 8), `strided_apg(P)` atoms of 8 rows per page.  Other P not
+// dividing 8 (and e4m3 caches, or several query tokens) take the owner mask.
+bool strided_path(const mla_decode_desc *d, int num_parts) {
+  return d->kv_dtype == MLA_KV_BF16 && d->q_len == 1 && num_parts > 1 && num_parts < 8 &&
+         8 % num_parts != 0;
+}
+int strided_apg(int num_parts) {
+  const int rows = (mla::kPage + num_parts - 1) / num_parts;  // a partition's rows of a page, at most
+  return (rows + 7) / 8;
+}
+
+// all partitions in one decode launch: P divides 8 (no owner mask), or the
+// strided gather
+bool fused_path(const mla_decode_desc *d, int num_parts) {
+  return num_parts >= 1 && (8 % num_parts == 0 || strided_path(d, num_parts));
+}
 
 // Q as [B*H rows, 576] bf16, one 64-column swizzled box of min(64, H) rows;
 // partition rows of a bf16 cache as a 5-D view (64 dims, 8 rows of stride P,
@@ -144,8 +160,8 @@ bool fused_path(int num_parts) { return num_parts >= 1 && 8 % num_parts == 0; }
 // faster boxes); for all P partitions (`all_parts`) it is added, with a stride
 // of one row (5-D / 3-D maps, coordinate r).
 int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, int part_id,
-                     int num_parts, bool all_parts, CUtensorMap *tm_q, CUtensorMap *tm_kv,
-                     CUtensorMap *tm_kvg) {
+                     int num_parts, bool all_parts, bool strided, CUtensorMap *tm_q,
+                     CUtensorMap *tm_kv, CUtensorMap *tm_kvg) {
   EncodeTiled enc = encode_tiled();
   if (!enc) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled unavailable");
@@ -178,6 +194,22 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3", r);
     *tm_kvg = *tm_kv;  // unused: the e4m3 stage lands in one box per page
+  } else if (strided) {
+    // (64 dims, 64 page rows, 9 blocks of 64 dims, pages): one box is one
+    // atom, rows c, c + P, ..., c + 7P of a page (traversal stride P), which
+    // lands as [9 blocks][8 rows][128 B]; rows past the page are out of
+    // bounds and read as zeros.  The partition is in the row coordinate.
+    const cuuint32_t P = cuuint32_t(num_parts);
+    cuuint64_t dims[4] = {64, cuuint64_t(mla::kPage), cuuint64_t(mla::kDqk / 64),
+                          cuuint64_t(d->num_pages)};
+    cuuint64_t strides[3] = {row, 128, cuuint64_t(mla::kPage) * row};
+    cuuint32_t box[4] = {64, 8 * P, cuuint32_t(mla::kDqk / 64), 1};
+    cuuint32_t es[4] = {1, P, 1, 1};
+    CUresult r = enc(tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(kv), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return tensor_map_fail("kv strided", r);
+    *tm_kvg = *tm_kv;  // unused: one column group
   } else {
     const cuuint64_t P = cuuint64_t(num_parts);
     const cuuint32_t G = cuuint32_t(8 / num_parts);
@@ -248,7 +280,7 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
                    void *workspace, int grid, cudaStream_t s, void *comb_out = nullptr,
                    float *comb_lse = nullptr) {
   const bool tc = tensor_core_path(d, num_parts);
-  if (fused && !fused_path(num_parts)) return MLA_ERR_ARG;
+  if (fused && !fused_path(d, num_parts)) return MLA_ERR_ARG;
   if (d->q_len > 1 && !tc) return MLA_ERR_SHAPE;
   const int per_group = tc ? kTcHeadsPerGroup : kSimtHeadsPerGroup;
   const int rows = rows_of(d);
@@ -273,8 +305,15 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
   p.max_pages = d->max_pages_per_seq;
   p.part_id = fused ? 0 : part_id;
   p.num_parts = num_parts;
-  const int gp = tc ? gather_parts(num_parts) : num_parts;
-  if (gp < num_parts) {  // owner mask over the gather of partition part_id mod gp of gp
+  const bool strided = tc && strided_path(d, num_parts);
+  const int gp = tc && !strided ? gather_parts(num_parts) : num_parts;
+  if (strided) {
+    p.strided = 1;
+    p.apg = strided_apg(num_parts);
+    p.s_q63 = (mla::kPage - 1) / num_parts;
+    p.s_r63 = (mla::kPage - 1) % num_parts;
+    p.s_c64 = mla::kPage % num_parts;
+  } else if (gp < num_parts) {  // owner mask over the gather of partition part_id mod gp of gp
     p.num_parts = gp;
     p.part_id = part_id % gp;
     p.own_parts = num_parts;
@@ -291,12 +330,12 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
   cudaError_t e;
   if (tc) {
     CUtensorMap tm_q, tm_kv, tm_kvg;
-    int st = make_tensor_maps(q, kv_pages, d, p.part_id, p.num_parts, fused, &tm_q, &tm_kv,
-                              &tm_kvg);
+    int st = make_tensor_maps(q, kv_pages, d, p.part_id, p.num_parts, fused, strided, &tm_q,
+                              &tm_kv, &tm_kvg);
     if (st != MLA_OK) return st;
     const int h = rows < kTcHeadsPerGroup ? rows : kTcHeadsPerGroup;
     const int npv = ((h + 15) / 16) * 16;
-    e = mla::launch_decode_tc(p, npv, h, 8 / p.num_parts, tm_q, tm_kv, tm_kvg, grid, s);
+    e = mla::launch_decode_tc(p, npv, h, strided ? 1 : 8 / p.num_parts, tm_q, tm_kv, tm_kvg, grid, s);
   } else {
     e = mla::launch_decode_simt(p, grid, s);
   }
@@ -421,7 +460,7 @@ int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_tab
     return MLA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t rows = size_t(d->batch) * rows_of(d);
-  if (fused_path(num_parts)) {
+  if (fused_path(d, num_parts)) {
     // every partition in one decode launch, then one kernel that merges the
     // splits and combines the partitions
     return enqueue_decode(q, kv_pages, block_table, seq_lens, 0, num_parts, true, sm_scale,

@@ -72,6 +72,15 @@ struct DecodeParams {
   // and own_parts), and the softmax drops every gathered token whose global
   // index is not own_part mod own_parts.  Otherwise own_parts = 0.
   int own_parts = 0, own_part = 0;
+  // Strided gather (tensor-core kernel, bf16 cache, one query token, P in
+  // {3, 5, 6, 7}): partition r's rows of page lp are y0 + kP (y0 = (r - 64 lp)
+  // mod P), landed by TMA with a traversal stride of P in atoms of 8 rows,
+  // `apg` atoms per page.  The tile walk then runs over slots: page lp holds
+  // slots [8 apg lp, 8 apg (lp + 1)), slot 8 apg lp + k is row y0 + kP when
+  // that row is below 64 (else the slot is empty), and a request's length in
+  // slots ends just past its last owned token.  Otherwise strided = 0.
+  int strided = 0, apg = 0;
+  int s_q63 = 0, s_r63 = 0, s_c64 = 0;  // strided: 63 / P, 63 mod P, 64 mod P
   int kv_e4m3;
   float kv_scale;             // 1 for bf16
   float score_scale_log2;     // sm_scale * log2(e): scores kept in the base-2 domain
@@ -81,7 +90,7 @@ struct DecodeParams {
 // ---------------------------------------------------------------- partition rule
 
 // Tokens owned by partition r of P out of a global length L: t < L, t mod P == r.
-__device__ __forceinline__ int local_len(int L, int P, int r) {
+__host__ __device__ __forceinline__ int local_len(int L, int P, int r) {
   return L / P + (r < L % P ? 1 : 0);
 }
 
@@ -114,6 +123,48 @@ __device__ __forceinline__ int group_len(const DecodeParams &p, int L, int g) {
   return p.q_len <= 1 ? L : row_len(p, L, min(p.heads, (g + 1) * p.heads_per_group) - 1);
 }
 
+// Strided gather: the first row partition `part` owns in logical page lp,
+// and the slots of a request of length L (see DecodeParams::strided).
+__host__ __device__ __forceinline__ int strided_y0(int part, int P, int lp) {
+  return ((part - (kPage % P) * (lp % P)) % P + P) % P;
+}
+__host__ __device__ __forceinline__ int strided_slots(int L, int P, int r, int apg) {
+  const int n = local_len(L, P, r);
+  if (n == 0) return 0;
+  const int t_last = r + P * (n - 1);
+  const int lp = t_last / kPage;
+  const int y0 = strided_y0(r, P, lp);
+  return 8 * apg * lp + (t_last - kPage * lp - y0) / P + 1;
+}
+// The slots of consecutive tiles that hold a row (below 64 within its page),
+// walked atom by atom without a division: page lp + 1 starts at
+// y0 - (64 mod P) (mod P), and a page with start y0 holds 63 / P + 1 rows of
+// the partition, one fewer when y0 > 63 mod P.
+struct StridedMask {
+  int ap, y0;  // the next atom: its index within its page, its page's first row
+  __device__ void start(const DecodeParams &p, int part, long long t) {
+    const int a = int(8 * t), lp = a / p.apg;
+    ap = a - lp * p.apg;
+    y0 = strided_y0(part, p.num_parts, lp);
+  }
+  // bit i set when slot i of the next tile holds a row; moves to the tile after
+  __device__ __forceinline__ unsigned long long next(const DecodeParams &p) {
+    unsigned long long m = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int rows = p.s_q63 + 1 - (y0 > p.s_r63 ? 1 : 0);
+      const int v = min(8, max(0, rows - 8 * ap));
+      m |= ((1ull << v) - 1ull) << (8 * k);
+      if (++ap == p.apg) {
+        ap = 0;
+        y0 -= p.s_c64;
+        if (y0 < 0) y0 += p.num_parts;
+      }
+    }
+    return m;
+  }
+};
+
 // Owned tokens of virtual request v (its group's widest row).
 // MULTI: requests may carry several query tokens (a compile-time switch, so
 // that single-token kernels keep the plain length rule in their code).
@@ -125,13 +176,15 @@ __device__ __forceinline__ int request_len(const DecodeParams &p, int v, int *er
   // under an owner mask, a request the real partition owns no token of is
   // empty (the neutral pair), however many the gathered partition holds
   if (MULTI && p.own_parts > p.num_parts && local_len(L, p.own_parts, p.own_part) == 0) return 0;
+  // strided gather: the length in slots
+  if (MULTI && p.strided) return strided_slots(L, p.num_parts, part_of(p, bv), p.apg);
   return local_len(L, p.num_parts, part_of(p, bv));
 }
 
 // Kernels whose rows may differ in the tokens they see: several query
 // tokens per request, or an owner mask.
 __host__ __device__ __forceinline__ bool multi_rows(const DecodeParams &p) {
-  return p.q_len > 1 || p.own_parts > p.num_parts;
+  return p.q_len > 1 || p.own_parts > p.num_parts || p.strided;
 }
 
 // Owner mask of the gathered partition's tiles.  Local token j of partition

@@ -150,8 +150,10 @@ struct Walk {
       rb = FUSED ? b % p.req_batch : b;
       part = FUSED ? b / p.req_batch : p.part_id;
       pc = FUSED ? part : 0;
-      n = MULTI ? local_len(group_len(p, checked_len(p, rb, nullptr), g), p.num_parts, part)
-                : local_len(checked_len(p, rb, nullptr), p.num_parts, part);
+      const int L = checked_len(p, rb, nullptr);
+      n = !MULTI ? local_len(L, p.num_parts, part)
+          : p.strided ? strided_slots(L, p.num_parts, part, p.apg)  // slots, not tokens
+                      : local_len(group_len(p, L, g), p.num_parts, part);
       return true;
     }
     return false;
@@ -192,6 +194,27 @@ __device__ __forceinline__ void tile_pages(const DecodeParams &p, int part, long
   *lp1 = int((part + (long long)p.num_parts * jl) / kPage);
 }
 
+// The logical page that producer lane `lane` loads for tile t, and the first
+// page row of its box: lane k loads page lp0 + k of the tile's pages, or, for
+// the strided gather, atom 8t + k (rows row0 + iP, i < 8, of its page).
+// False when the lane loads nothing.
+template <bool MULTI>
+__device__ __forceinline__ bool lane_page(const DecodeParams &p, int part, long long t, int n, int lane,
+                                          int *lp, int *row0) {
+  if (MULTI && p.strided) {
+    const int a = int(8 * t) + lane;
+    if (lane >= 8 || 8 * a >= n) return false;
+    *lp = a / p.apg;
+    *row0 = strided_y0(part, p.num_parts, *lp) + 8 * p.num_parts * (a - *lp * p.apg);
+    return true;
+  }
+  int lp0, lp1;
+  tile_pages(p, part, t, n, &lp0, &lp1);
+  *lp = lp0 + lane;
+  *row0 = 0;
+  return lane <= lp1 - lp0;
+}
+
 // ------------------------------------------------------------------ producer
 
 // AHEAD: tiles whose pages are pulled into L2 ahead of the stage.  1 when a
@@ -228,16 +251,17 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   auto next_ahead = [&]() {
     int pg = -1;
     if (ahead.live) {
-      int lp0, lp1;
-      tile_pages(p, ahead.w.part, ahead.t, ahead.w.n, &lp0, &lp1);
-      if (lane <= lp1 - lp0) {
-        pg = p.block_table[size_t(ahead.w.rb) * p.max_pages + lp0 + lane];
+      int lp, row0;
+      if (lane_page<MULTI>(p, ahead.w.part, ahead.t, ahead.w.n, lane, &lp, &row0)) {
+        pg = p.block_table[size_t(ahead.w.rb) * p.max_pages + lp];
         if (pg >= 0 && pg < p.num_pages) {
           if (F8) {
             if (FUSED)
               tma_prefetch_3d(tm_kv, 0, pg * rows_per_page, ahead.w.pc);
             else
               tma_prefetch_2d(tm_kv, 0, pg * rows_per_page);
+          } else if (MULTI && p.strided) {
+            tma_prefetch_4d(tm_kv, 0, row0, 0, pg);
           } else {
             if (FUSED)
               tma_prefetch_5d(tm_kv, 0, 0, 0, pg * tp.groups_per_page, ahead.w.pc);
@@ -272,9 +296,8 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
       ++q_it;
     }
     const int s = kv_it & 1;
-    int lp0, lp1;
-    tile_pages(p, cur.w.part, cur.t, cur.w.n, &lp0, &lp1);
-    const bool mine = lane <= lp1 - lp0;
+    int lp, row0;
+    const bool mine = lane_page<MULTI>(p, cur.w.part, cur.t, cur.w.n, lane, &lp, &row0);
     int pg = ring[0];
     if (mine && (pg < 0 || pg >= p.num_pages)) {
       atomicOr(err, kErrBadPage);
@@ -296,6 +319,9 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
           tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, pg * rows_per_page, cur.w.pc);
         else
           tma_load_2d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, pg * rows_per_page);
+      } else if (MULTI && p.strided) {
+        // one atom: rows row0 + iP (traversal stride P) of page pg, all dims
+        tma_load_4d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, row0, 0, pg);
       } else {
         // group g: dim blocks [KBG g, KBG g + KBG) of the page's atoms
         const CUtensorMap *tm = KBG == kKb ? tm_kv : tm_kvg;
@@ -536,12 +562,14 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
     // owned tokens each of this lane's two rows sees (all w.n unless a request
     // carries several query tokens, each with its own causal bound)
     int nrow[2] = {w.n, w.n};
-    if (MULTI) {  // query token i of T sees the global tokens t < L - T + i + 1
+    if (MULTI && !p.strided) {  // query token i of T sees the global tokens t < L - T + i + 1
       const int L = checked_len(p, w.rb, nullptr);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
         nrow[h] = local_len(row_len(p, L, w.g * kHeads + row[h]), p.num_parts, w.part);
     }
+    StridedMask smask;  // strided gather: the slots of each tile that hold a row
+    if (MULTI && p.strided) smask.start(p, w.part, w.t0);
     float mrun[2] = {-INFINITY, -INFINITY};  // running max (base-2 units) of each head
     float ellp[2] = {0.f, 0.f};              // this lane's share of each head's sum
     for (long long t = w.t0; t < w.t1; ++t, ++kv_it, ++p_it) {
@@ -582,8 +610,8 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
           xp[k].y = tok + 1 < lim ? xp[k].y : -INFINITY;
         }
       }
-      if (MULTI && masked) {  // tokens another partition owns
-        const unsigned long long ob = own.bits(t);
+      if (MULTI && (masked || p.strided)) {  // tokens another partition owns; empty strided slots
+        const unsigned long long ob = p.strided ? smask.next(p) : own.bits(t);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int tok = 8 * (k >> 1) + pair;

@@ -79,7 +79,11 @@ SHAPES = [
     (128, [1300, 64, 1, 0, 511], 1, "bf16"),   # one page per tile, two head groups
     (1, [77, 3000, 2, 65], 1, "bf16"),
     (7, [129, 2, 1000], 1, "bf16"),
-    # P not dividing 8: gather partition r mod gcd(P, 8), drop other owners' tokens
+    # P in {3, 5, 6, 7} with a bf16 cache: the strided gather (rows y0 + kP of each page)
+    (64, [1300, 5, 4097, 70], 5, "bf16"),
+    (16, [1, 2, 3, 4, 5, 6, 7, 64, 65, 2000], 7, "bf16"),
+    (128, [700, 64, 1, 0, 191, 192, 193], 3, "bf16"),   # two head groups; page-edge lengths
+    # other P not dividing 8: gather partition r mod gcd(P, 8), drop other owners' tokens
     (16, [1, 3, 5, 7, 511, 1025, 2049], 16, "bf16"),  # gather 8, keep 1 of 2
     (32, [300, 2049, 17, 0], 6, "bf16"),              # gather 2, keep 1 of 3
     (64, [700, 65, 1300], 12, "e4m3"),                # gather 4, keep 1 of 3
