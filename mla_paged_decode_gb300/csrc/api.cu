@@ -114,9 +114,9 @@ int tensor_map_fail(const char *what, CUresult r) {
 
 constexpr int kTcHeadsPerGroup = 64;
 
-// The tensor-core kernel takes partitions whose owned rows of a page form
-// whole 8-row groups (P | 8), for bf16 and e4m3 caches alike.
-// The tensor-core kernel gathers partition r mod g of g = gcd(P, 8) (g divides
+// The tensor-core kernel reads exactly a partition's rows when they form whole
+// 8-row groups of a page (P | 8), or through the strided gather below.
+// Otherwise it gathers partition r mod g of g = gcd(P, 8) (g divides
 // a page's 8 atoms) and, when g < P, drops the tokens other partitions own:
 // it reads P / g times the partition's own bytes at the tensor-core rate,
 // which beats the CUDA-core kernel while P / g stays small.

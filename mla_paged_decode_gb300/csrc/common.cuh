@@ -166,9 +166,10 @@ struct StridedMask {
 };
 
 // Owned tokens of virtual request v (its group's widest row).
-// MULTI: requests may carry several query tokens (a compile-time switch, so
-// that single-token kernels keep the plain length rule in their code).
-template <bool MULTI = false>
+// MULTI: rows may differ in the tokens they see (several query tokens, or an
+// owner mask); MULTI == 2: the strided gather, whose lengths count slots.  A
+// compile-time switch, so that each kernel keeps only its own length rule.
+template <int MULTI = 0>
 __device__ __forceinline__ int request_len(const DecodeParams &p, int v, int *err) {
   int bv = v / p.head_groups;
   int L = checked_len(p, req_of(p, bv), err);
@@ -176,8 +177,8 @@ __device__ __forceinline__ int request_len(const DecodeParams &p, int v, int *er
   // under an owner mask, a request the real partition owns no token of is
   // empty (the neutral pair), however many the gathered partition holds
   if (MULTI && p.own_parts > p.num_parts && local_len(L, p.own_parts, p.own_part) == 0) return 0;
-  // strided gather: the length in slots
-  if (MULTI && p.strided) return strided_slots(L, p.num_parts, part_of(p, bv), p.apg);
+  // strided gather (MULTI == 2): the length in slots
+  if (MULTI == 2) return strided_slots(L, p.num_parts, part_of(p, bv), p.apg);
   return local_len(L, p.num_parts, part_of(p, bv));
 }
 
@@ -209,7 +210,7 @@ __device__ inline OwnerMask owner_mask_of(const DecodeParams &p) {
   return o;
 }
 
-template <bool MULTI = false>
+template <int MULTI = 0>
 __device__ __forceinline__ int request_tiles(const DecodeParams &p, int v) {
   return (request_len<MULTI>(p, v, nullptr) + kTile - 1) / kTile;
 }
@@ -253,7 +254,7 @@ __device__ __forceinline__ long long request_cost(int tiles) {
 
 // Block-wide: computes this CTA's range.  All threads must call it.
 // `scratch` needs blockDim.x / 32 + 1 long longs of shared memory.
-template <bool MULTI = false>
+template <int MULTI = 0>
 __device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long long *scratch) {
   const int V = p.batch * p.head_groups;
   const int tid = threadIdx.x, nw = blockDim.x / 32, lane = tid & 31, warp = tid >> 5;

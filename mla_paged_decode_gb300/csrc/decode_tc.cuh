@@ -28,8 +28,11 @@
 // MMAs then run with f16 operands, P is written as f16, and the scores carry
 // sm_scale * kv_scale / (that power of two).
 //
-// Partitions: P divides 8 here (64/P owned rows per page); a call for
-// another P runs the gather of P' = gcd(P, 8) with an owner mask in the
+// Partitions: P divides 8 here (64/P owned rows per page), or P in
+// {3, 5, 6, 7} with a bf16 cache and one query token: the strided gather
+// (DecodeParams::strided; one box per 8-row atom, rows y0 + kP of a page,
+// through the several-row variants, which mask a tile's empty slots).  A
+// call for another P runs the gather of P' = gcd(P, 8) with an owner mask in the
 // softmax (DecodeParams::own_parts), through the several-query-token
 // variants, which carry the per-row bounds and guards that mask needs.
 //
@@ -130,7 +133,7 @@ static_assert(sizeof(TcMisc) + 1024 <= tc::kSmemBytes - tc::kOffMisc, "shared me
 // The requests (and tile ranges) this CTA owns, in order; every role walks it.
 // FUSED: all partitions in one launch (output row b = partition * B + input
 // request); otherwise one partition, p.part_id, and row b is request b.
-template <bool FUSED, bool MULTI>
+template <bool FUSED, int MULTI>
 struct Walk {
   const DecodeParams &p;
   const CtaRange &r;
@@ -151,9 +154,9 @@ struct Walk {
       part = FUSED ? b / p.req_batch : p.part_id;
       pc = FUSED ? part : 0;
       const int L = checked_len(p, rb, nullptr);
-      n = !MULTI ? local_len(L, p.num_parts, part)
-          : p.strided ? strided_slots(L, p.num_parts, part, p.apg)  // slots, not tokens
-                      : local_len(group_len(p, L, g), p.num_parts, part);
+      n = MULTI == 2 ? strided_slots(L, p.num_parts, part, p.apg)  // slots, not tokens
+          : MULTI      ? local_len(group_len(p, L, g), p.num_parts, part)
+                       : local_len(L, p.num_parts, part);
       return true;
     }
     return false;
@@ -162,7 +165,7 @@ struct Walk {
 };
 
 // One position in the walk: request + tile.
-template <bool FUSED, bool MULTI>
+template <bool FUSED, int MULTI>
 struct TileCursor {
   Walk<FUSED, MULTI> w;
   long long t;
@@ -198,10 +201,10 @@ __device__ __forceinline__ void tile_pages(const DecodeParams &p, int part, long
 // page row of its box: lane k loads page lp0 + k of the tile's pages, or, for
 // the strided gather, atom 8t + k (rows row0 + iP, i < 8, of its page).
 // False when the lane loads nothing.
-template <bool MULTI>
+template <bool STRIDED>
 __device__ __forceinline__ bool lane_page(const DecodeParams &p, int part, long long t, int n, int lane,
                                           int *lp, int *row0) {
-  if (MULTI && p.strided) {
+  if (STRIDED) {
     const int a = int(8 * t) + lane;
     if (lane >= 8 || 8 * a >= n) return false;
     *lp = a / p.apg;
@@ -221,11 +224,12 @@ __device__ __forceinline__ bool lane_page(const DecodeParams &p, int part, long 
 // tile is one page (P = 1), 2 when it gathers P pages of 64/P rows (each the
 // measured best of 0..4).  It is a template parameter because the same choice
 // made at run time costs more than it gains.
-template <bool F8, bool FUSED, bool MULTI, int AHEAD>
+template <bool F8, bool FUSED, int MULTI, int AHEAD>
 __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                             uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
                             const CUtensorMap *tm_kvg, int *err) {
   using namespace tc;
+  constexpr bool STRIDED = MULTI == 2;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const int lane = threadIdx.x & 31;
@@ -252,7 +256,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
     int pg = -1;
     if (ahead.live) {
       int lp, row0;
-      if (lane_page<MULTI>(p, ahead.w.part, ahead.t, ahead.w.n, lane, &lp, &row0)) {
+      if (lane_page<STRIDED>(p, ahead.w.part, ahead.t, ahead.w.n, lane, &lp, &row0)) {
         pg = p.block_table[size_t(ahead.w.rb) * p.max_pages + lp];
         if (pg >= 0 && pg < p.num_pages) {
           if (F8) {
@@ -260,7 +264,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
               tma_prefetch_3d(tm_kv, 0, pg * rows_per_page, ahead.w.pc);
             else
               tma_prefetch_2d(tm_kv, 0, pg * rows_per_page);
-          } else if (MULTI && p.strided) {
+          } else if (STRIDED) {
             tma_prefetch_4d(tm_kv, 0, row0, 0, pg);
           } else {
             if (FUSED)
@@ -297,7 +301,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
     }
     const int s = kv_it & 1;
     int lp, row0;
-    const bool mine = lane_page<MULTI>(p, cur.w.part, cur.t, cur.w.n, lane, &lp, &row0);
+    const bool mine = lane_page<STRIDED>(p, cur.w.part, cur.t, cur.w.n, lane, &lp, &row0);
     int pg = ring[0];
     if (mine && (pg < 0 || pg >= p.num_pages)) {
       atomicOr(err, kErrBadPage);
@@ -319,7 +323,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
           tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, pg * rows_per_page, cur.w.pc);
         else
           tma_load_2d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, pg * rows_per_page);
-      } else if (MULTI && p.strided) {
+      } else if (STRIDED) {
         // one atom: rows row0 + iP (traversal stride P) of page pg, all dims
         tma_load_4d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, row0, 0, pg);
       } else {
@@ -360,7 +364,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 
 // Descriptors: an offset is added to the encoded start address (bits 0..13,
 // address >> 4), which never carries because shared addresses stay below 256 KB.
-template <bool F8, bool FUSED, bool MULTI, int KBG>
+template <bool F8, bool FUSED, int MULTI, int KBG>
 __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
                          uint32_t sKv, uint32_t tmem, int chain, int *err) {
   using namespace tc;
@@ -415,7 +419,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
 
 // O^T(chunk c) (+)= V^T(tile) P^T over ceil(nv/16) steps of 16 tokens; issuer
 // `half` takes value chunks 2 half and 2 half + 1.
-template <bool F8, bool FUSED, bool MULTI, int KBG>
+template <bool F8, bool FUSED, int MULTI, int KBG>
 __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
                           uint32_t tmem, int half, int *err) {
   using namespace tc;
@@ -534,10 +538,11 @@ static __device__ __noinline__ void zero_value_tail(unsigned char *stage, int nv
   }
 }
 
-template <bool F8, bool FUSED, bool MULTI, int KBG>
+template <bool F8, bool FUSED, int MULTI, int KBG>
 __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
                            unsigned char *smem, uint32_t tmem, int *err) {
   using namespace tc;
+  constexpr bool STRIDED = MULTI == 2;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const int gt = int(threadIdx.x) - 128;  // rank in the warpgroup
@@ -562,14 +567,14 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
     // owned tokens each of this lane's two rows sees (all w.n unless a request
     // carries several query tokens, each with its own causal bound)
     int nrow[2] = {w.n, w.n};
-    if (MULTI && !p.strided) {  // query token i of T sees the global tokens t < L - T + i + 1
+    if (MULTI && !STRIDED) {  // query token i of T sees the global tokens t < L - T + i + 1
       const int L = checked_len(p, w.rb, nullptr);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
         nrow[h] = local_len(row_len(p, L, w.g * kHeads + row[h]), p.num_parts, w.part);
     }
     StridedMask smask;  // strided gather: the slots of each tile that hold a row
-    if (MULTI && p.strided) smask.start(p, w.part, w.t0);
+    if (STRIDED) smask.start(p, w.part, w.t0);
     float mrun[2] = {-INFINITY, -INFINITY};  // running max (base-2 units) of each head
     float ellp[2] = {0.f, 0.f};              // this lane's share of each head's sum
     for (long long t = w.t0; t < w.t1; ++t, ++kv_it, ++p_it) {
@@ -610,8 +615,10 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
           xp[k].y = tok + 1 < lim ? xp[k].y : -INFINITY;
         }
       }
-      if (MULTI && (masked || p.strided)) {  // tokens another partition owns; empty strided slots
-        const unsigned long long ob = p.strided ? smask.next(p) : own.bits(t);
+      if (STRIDED || (MULTI && masked)) {  // empty strided slots; tokens another partition owns
+        unsigned long long ob;
+        if constexpr (STRIDED) ob = smask.next(p);
+        else ob = own.bits(t);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int tok = 8 * (k >> 1) + pair;
@@ -889,7 +896,7 @@ static __device__ __noinline__ bool convert_q(const TcParams &tp, TcMisc &m, uns
   return true;
 }
 
-template <bool FUSED, bool MULTI>
+template <bool FUSED, int MULTI>
 __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r, TcMisc &m,
                                            unsigned char *smem, int *err) {
   using namespace tc;
@@ -974,7 +981,7 @@ __device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r
 
 // ------------------------------------------------------------------ kernel
 
-template <bool F8, bool FUSED, bool MULTI, int AHEAD>
+template <bool F8, bool FUSED, int MULTI, int AHEAD>
 __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     decode_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_kv,
@@ -1067,7 +1074,7 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
 cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream);
 cudaError_t launch_dcp_merge_combine(const DecodeParams &p, int grid, cudaStream_t stream);
 
-template <bool F8, bool FUSED, bool MULTI, int AHEAD>
+template <bool F8, bool FUSED, int MULTI, int AHEAD>
 static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
                              const CUtensorMap &tm_kvg, int grid, cudaStream_t stream) {
   static int configured[64] = {0};
@@ -1095,11 +1102,17 @@ static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const 
 
 // The variants of one cache dtype: one partition alone with P = 1 (a tile is
 // one page: prefetch distance 1), one partition of P > 1, or all P partitions
-// in one launch (distance 2); each with one query token or several.
+// in one launch (distance 2); each with one query token or several, and the
+// strided gather of a bf16 cache (one partition or all).
 template <bool F8>
 cudaError_t launch_tc_variants(const TcParams &tp, const CUtensorMap &tm_q,
                                const CUtensorMap &tm_kv, const CUtensorMap &tm_kvg, int grid,
                                cudaStream_t stream) {
+  if constexpr (!F8) {
+    if (tp.p.strided)
+      return tp.p.fused ? launch_tc<F8, true, 2, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
+                        : launch_tc<F8, false, 2, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
+  }
   const bool multi = multi_rows(tp.p);
   if (tp.p.fused)
     return multi ? launch_tc<F8, true, true, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)

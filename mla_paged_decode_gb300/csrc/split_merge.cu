@@ -94,7 +94,9 @@ __device__ __forceinline__ void store_row(__nv_bfloat16 *row, const uint32_t (&p
 // one keeps whatever an earlier call left); split k > 0 lives in slot
 // 2 (first + k): never past the 2 x grid slots
 __device__ __forceinline__ bool is_split(const DecodeParams &p, int v, int4 info, int grid) {
-  const int tiles = multi_rows(p) ? request_tiles<true>(p, v) : request_tiles<false>(p, v);
+  const int tiles = p.strided       ? request_tiles<2>(p, v)
+                    : multi_rows(p) ? request_tiles<1>(p, v)
+                                    : request_tiles<0>(p, v);
   return tiles > 0 && info.y > 1 && info.x >= 0 && info.x + info.y <= grid;
 }
 

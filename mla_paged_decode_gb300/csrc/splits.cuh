@@ -41,7 +41,7 @@ __device__ __forceinline__ float lse_out(const DecodeParams &p, float lse2) {
 
 // The neutral pair (0, -inf) for every virtual request with no owned token.
 // Virtual request v is handled by CTA v mod gridDim.x.  Block-wide.
-template <bool MULTI = false>
+template <int MULTI = 0>
 __device__ inline void write_empty_requests(const DecodeParams &p) {
   const int V = p.batch * p.head_groups;
   int *err = error_word(p);
