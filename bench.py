@@ -781,9 +781,10 @@ def _hbm_roofline(kv_bytes, ms, steps, kernel):
 def run_dcp_parts(args, world, rank, local):
     """--op dcp --parts P: the 32K-context batch (B=64, H=64, bf16) as P
     round-robin partitions and their merge, one mla_decode_dcp call per step
-    (the tensor-core kernel: one launch for all partitions when P divides 8,
-    else one launch per partition with the owner mask when P / gcd(P, 8) <= 16,
-    else the CUDA-core kernel).  KV GB/s counts each cached row once."""
+    (the tensor-core kernel: one launch for all partitions when P divides 8 or
+    P is 3, 5, 6 or 7 (the strided gather), else one launch per partition with
+    the owner mask when P / gcd(P, 8) <= 16, else the CUDA-core kernel).  KV
+    GB/s counts each cached row once."""
     mla, dev, stream = gpu_setup(world, rank, local)
     P = args.parts
     case = workloads.config_long32k(device=dev, seed=args.seed)
