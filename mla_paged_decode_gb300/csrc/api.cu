@@ -131,13 +131,13 @@ bool tensor_core_path(const mla_decode_desc *, int num_parts) {
   return num_parts >= 1 && num_parts / gather_parts(num_parts) <= kMaxOwnerRatio;
 }
 
-// A bf16 cache with one query token and P in {3, 5, 6, 7}: the tensor-core
-// kernel gathers exactly the partition's rows, with a TMA traversal stride of
-// P rows (at most 8), `strided_apg(P)` atoms of 8 rows per page.  Other P not
-// dividing 8 (and e4m3 caches, or several query tokens) take the owner mask.
+// One query token and P in {3, 5, 6, 7}: the tensor-core kernel gathers
+// exactly the partition's rows, with a TMA traversal stride of P rows (at
+// most 8), `strided_apg(P)` atoms of 8 rows per page, for bf16 and e4m3
+// caches alike.  Other P not dividing 8 (or several query tokens) take the
+// owner mask.
 bool strided_path(const mla_decode_desc *d, int num_parts) {
-  return d->kv_dtype == MLA_KV_BF16 && d->q_len == 1 && num_parts > 1 && num_parts < 8 &&
-         8 % num_parts != 0;
+  return d->q_len == 1 && num_parts > 1 && num_parts < 8 && 8 % num_parts != 0;
 }
 int strided_apg(int num_parts) {
   const int rows = (mla::kPage + num_parts - 1) / num_parts;  // a partition's rows of a page, at most
@@ -179,7 +179,22 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("q", r);
   }
-  if (d->kv_dtype == MLA_KV_E4M3) {
+  if (d->kv_dtype == MLA_KV_E4M3 && strided) {
+    // (144 words of 4 fp8 values, 64 page rows, pages): one box is one atom,
+    // raw rows c, c + P, ..., c + 7P of a page (traversal stride P), landing
+    // as 8 consecutive 576-byte rows; rows past the page read as zeros
+    const cuuint32_t P = cuuint32_t(num_parts);
+    const cuuint64_t row8 = cuuint64_t(mla::kDqk);
+    cuuint64_t dims[3] = {row8 / 4, cuuint64_t(mla::kPage), cuuint64_t(d->num_pages)};
+    cuuint64_t strides[2] = {row8, cuuint64_t(mla::kPage) * row8};
+    cuuint32_t box[3] = {cuuint32_t(row8 / 4), 8 * P, 1};
+    cuuint32_t es[3] = {1, P, 1};
+    CUresult r = enc(tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(kv), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 strided", r);
+    *tm_kvg = *tm_kv;
+  } else if (d->kv_dtype == MLA_KV_E4M3) {
     const cuuint64_t P = cuuint64_t(num_parts);
     const cuuint32_t R = cuuint32_t(mla::kPage / num_parts);
     const cuuint64_t row8 = cuuint64_t(mla::kDqk);

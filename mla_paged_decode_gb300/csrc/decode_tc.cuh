@@ -29,7 +29,7 @@
 // sm_scale * kv_scale / (that power of two).
 //
 // Partitions: P divides 8 here (64/P owned rows per page), or P in
-// {3, 5, 6, 7} with a bf16 cache and one query token: the strided gather
+// {3, 5, 6, 7} with one query token: the strided gather
 // (DecodeParams::strided; one box per 8-row atom, rows y0 + kP of a page,
 // through the several-row variants, which mask a tile's empty slots).  A
 // call for another P runs the gather of P' = gcd(P, 8) with an owner mask in the
@@ -259,7 +259,9 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
       if (lane_page<STRIDED>(p, ahead.w.part, ahead.t, ahead.w.n, lane, &lp, &row0)) {
         pg = p.block_table[size_t(ahead.w.rb) * p.max_pages + lp];
         if (pg >= 0 && pg < p.num_pages) {
-          if (F8) {
+          if (F8 && STRIDED) {
+            tma_prefetch_3d(tm_kv, 0, row0, pg);
+          } else if (F8) {
             if (FUSED)
               tma_prefetch_3d(tm_kv, 0, pg * rows_per_page, ahead.w.pc);
             else
@@ -318,7 +320,10 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
     __syncwarp();
     if (load) {
       const uint32_t dst = dst0 + s * kStageBytes + lane * page_bytes;
-      if (F8) {
+      if (F8 && STRIDED) {
+        // one atom: raw rows row0 + iP (traversal stride P) of page pg
+        tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, row0, pg);
+      } else if (F8) {
         if (FUSED)
           tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, pg * rows_per_page, cur.w.pc);
         else
@@ -1103,16 +1108,14 @@ static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const 
 // The variants of one cache dtype: one partition alone with P = 1 (a tile is
 // one page: prefetch distance 1), one partition of P > 1, or all P partitions
 // in one launch (distance 2); each with one query token or several, and the
-// strided gather of a bf16 cache (one partition or all).
+// strided gather (one partition or all).
 template <bool F8>
 cudaError_t launch_tc_variants(const TcParams &tp, const CUtensorMap &tm_q,
                                const CUtensorMap &tm_kv, const CUtensorMap &tm_kvg, int grid,
                                cudaStream_t stream) {
-  if constexpr (!F8) {
-    if (tp.p.strided)
-      return tp.p.fused ? launch_tc<F8, true, 2, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
-                        : launch_tc<F8, false, 2, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
-  }
+  if (tp.p.strided)
+    return tp.p.fused ? launch_tc<F8, true, 2, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
+                      : launch_tc<F8, false, 2, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
   const bool multi = multi_rows(tp.p);
   if (tp.p.fused)
     return multi ? launch_tc<F8, true, true, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)

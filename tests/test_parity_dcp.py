@@ -32,11 +32,12 @@ CASES = [
     (64, [64, 200, 1000, 4097, 1], 4, "bf16"),
     (128, [700, 65, 2, 0], 2, "bf16"),
     (32, [77, 3000, 9], 1, "bf16"),
-    (16, [40, 999, 3], 3, "bf16"),            # P not dividing 8, bf16: the strided gather, one launch
+    (16, [40, 999, 3], 3, "bf16"),            # P in {3, 5, 6, 7}: the strided gather, one launch
     (64, [1300, 5, 4097, 70], 5, "bf16"),
     (16, [333, 6, 65, 0], 6, "bf16"),
     (32, [2049, 7, 700], 7, "bf16"),
-    (16, [40, 999, 3], 3, "e4m3"),            # e4m3: the owner mask, one call per partition
+    (16, [40, 999, 3], 3, "e4m3"),            # e4m3, the strided gather too
+    (64, [700, 2, 1500], 7, "e4m3"),
     (64, [1500, 33, 640, 0], 4, "e4m3"),
     (16, [1, 2, 3, 900, 2049], 8, "e4m3"),
 ]

@@ -79,7 +79,9 @@ SHAPES = [
     (128, [1300, 64, 1, 0, 511], 1, "bf16"),   # one page per tile, two head groups
     (1, [77, 3000, 2, 65], 1, "bf16"),
     (7, [129, 2, 1000], 1, "bf16"),
-    # P in {3, 5, 6, 7} with a bf16 cache: the strided gather (rows y0 + kP of each page)
+    # P in {3, 5, 6, 7}, one query token: the strided gather (rows y0 + kP of each page)
+    (64, [1, 63, 64, 65, 3000], 6, "e4m3"),
+    (128, [2049, 7, 640], 7, "e4m3"),
     (64, [1300, 5, 4097, 70], 5, "bf16"),
     (16, [1, 2, 3, 4, 5, 6, 7, 64, 65, 2000], 7, "bf16"),
     (128, [700, 64, 1, 0, 191, 192, 193], 3, "bf16"),   # two head groups; page-edge lengths
