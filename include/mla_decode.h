@@ -16,8 +16,7 @@
  *                      sglang pull 33926, implementation steps 3 (FP8 KV path)
  *                      and 4 (under DCP the fused KV write is off and the
  *                      pool's own write stores the rank's rows).
- *  mla_decode_dcp      all P partitions in one call (one decode launch for P | 8, and
- *                      for P <= 8 with one query token)
+ *  mla_decode_dcp      all P partitions in one call (one decode launch for P <= 8)
  *                      and their merge: the DCP ranks emulated on one GPU.
  *  mla_lse_combine     the LSE-weighted softmax merge of P partial results.
  *                      sglang pull 33364 ([Attention][DCP] Add symm_a2a ...),
@@ -133,8 +132,8 @@ size_t mla_decode_workspace_size(const mla_decode_desc *d, int num_sms);
  * requests its schedule split across SMs.  The tensor-core kernel serves
  * every num_parts with num_parts / gcd(num_parts, 8) <= 16.  For num_parts
  * dividing 8 it reads exactly the partition's rows.  For num_parts in
- * {3, 5, 6, 7} with q_len = 1 it does so too, through a TMA traversal stride
- * of num_parts rows.  Otherwise it gathers partition
+ * {3, 5, 6, 7} it does so too, through a TMA traversal stride of num_parts
+ * rows.  Otherwise it gathers partition
  * part_id mod g of g = gcd(num_parts, 8) and drops the tokens the other
  * partitions own (reading num_parts / g times the partition's own bytes).
  * Larger ratios run a CUDA-core kernel.
@@ -174,8 +173,7 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
  *  workspace    >= mla_decode_dcp_workspace_size(d, num_parts, 0) bytes, same
  *               rules as for mla_decode_partial.
  *
- * num_parts in {1, 2, 4, 8}, and num_parts in {3, 5, 6, 7} with q_len = 1:
- * one decode launch covers every (partition, request) pair,
+ * num_parts <= 8: one decode launch covers every (partition, request) pair,
  * then one kernel merges the requests the decode's schedule split across SMs
  * and combines the partitions (two kernels).  Other num_parts (up to 256):
  * one decode call per partition, then the combine.  Errors and bounds reporting as for mla_decode_partial.

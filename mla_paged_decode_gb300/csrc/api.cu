@@ -131,13 +131,12 @@ bool tensor_core_path(const mla_decode_desc *, int num_parts) {
   return num_parts >= 1 && num_parts / gather_parts(num_parts) <= kMaxOwnerRatio;
 }
 
-// One query token and P in {3, 5, 6, 7}: the tensor-core kernel gathers
-// exactly the partition's rows, with a TMA traversal stride of P rows (at
-// most 8), `strided_apg(P)` atoms of 8 rows per page, for bf16 and e4m3
-// caches alike.  Other P not dividing 8 (or several query tokens) take the
-// owner mask.
-bool strided_path(const mla_decode_desc *d, int num_parts) {
-  return d->q_len == 1 && num_parts > 1 && num_parts < 8 && 8 % num_parts != 0;
+// P in {3, 5, 6, 7}: the tensor-core kernel gathers exactly the partition's
+// rows, with a TMA traversal stride of P rows (at most 8), `strided_apg(P)`
+// atoms of 8 rows per page, for bf16 and e4m3 caches and any q_len.  Other P
+// not dividing 8 take the owner mask.
+bool strided_path(const mla_decode_desc *, int num_parts) {
+  return num_parts > 1 && num_parts < 8 && 8 % num_parts != 0;
 }
 int strided_apg(int num_parts) {
   const int rows = (mla::kPage + num_parts - 1) / num_parts;  // a partition's rows of a page, at most

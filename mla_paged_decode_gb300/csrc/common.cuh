@@ -72,7 +72,7 @@ struct DecodeParams {
   // and own_parts), and the softmax drops every gathered token whose global
   // index is not own_part mod own_parts.  Otherwise own_parts = 0.
   int own_parts = 0, own_part = 0;
-  // Strided gather (tensor-core kernel, one query token, P in {3, 5, 6, 7}):
+  // Strided gather (tensor-core kernel, P in {3, 5, 6, 7}):
   // partition r's rows of page lp are y0 + kP (y0 = (r - 64 lp)
   // mod P), landed by TMA with a traversal stride of P in atoms of 8 rows,
   // `apg` atoms per page.  The tile walk then runs over slots: page lp holds

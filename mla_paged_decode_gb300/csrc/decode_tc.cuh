@@ -29,7 +29,7 @@
 // sm_scale * kv_scale / (that power of two).
 //
 // Partitions: P divides 8 here (64/P owned rows per page), or P in
-// {3, 5, 6, 7} with one query token: the strided gather
+// {3, 5, 6, 7}: the strided gather
 // (DecodeParams::strided; one box per 8-row atom, rows y0 + kP of a page,
 // through the several-row variants, which mask a tile's empty slots).  A
 // call for another P runs the gather of P' = gcd(P, 8) with an owner mask in the
@@ -154,7 +154,7 @@ struct Walk {
       part = FUSED ? b / p.req_batch : p.part_id;
       pc = FUSED ? part : 0;
       const int L = checked_len(p, rb, nullptr);
-      n = MULTI == 2 ? strided_slots(L, p.num_parts, part, p.apg)  // slots, not tokens
+      n = MULTI == 2 ? strided_slots(group_len(p, L, g), p.num_parts, part, p.apg)  // slots
           : MULTI      ? local_len(group_len(p, L, g), p.num_parts, part)
                        : local_len(L, p.num_parts, part);
       return true;
@@ -572,11 +572,16 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
     // owned tokens each of this lane's two rows sees (all w.n unless a request
     // carries several query tokens, each with its own causal bound)
     int nrow[2] = {w.n, w.n};
-    if (MULTI && !STRIDED) {  // query token i of T sees the global tokens t < L - T + i + 1
+    if (MULTI) {  // query token i of T sees the global tokens t < L - T + i + 1
       const int L = checked_len(p, w.rb, nullptr);
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        nrow[h] = local_len(row_len(p, L, w.g * kHeads + row[h]), p.num_parts, w.part);
+      for (int h = 0; h < 2; ++h) {
+        const int Lr = row_len(p, L, w.g * kHeads + row[h]);
+        // strided gather: slots are in token order, so the row's visible
+        // slots end just past its last owned token below Lr
+        nrow[h] = STRIDED ? strided_slots(Lr, p.num_parts, w.part, p.apg)
+                          : local_len(Lr, p.num_parts, w.part);
+      }
     }
     StridedMask smask;  // strided gather: the slots of each tile that hold a row
     if (STRIDED) smask.start(p, w.part, w.t0);

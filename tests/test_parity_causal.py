@@ -43,8 +43,11 @@ CASES = [
     (128, 2, [800, 2, 65], 1, "bf16"),
     (8, 8, [8, 9, 200, 63], 2, "bf16"),
     (16, 4, [4, 900, 70, 1], 4, "e4m3"),
-    (32, 2, [3, 500, 90, 7], 3, "bf16"),               # owner mask: gather 1, keep 1 of 3
-    (16, 3, [1, 2, 5, 300, 130], 6, "e4m3"),           # gather 2, keep 1 of 3
+    (32, 2, [3, 500, 90, 7], 3, "bf16"),               # strided gather: rows y0 + kP of a page
+    (16, 3, [1, 2, 5, 300, 130], 6, "e4m3"),
+    (64, 4, [4, 5, 64, 65, 66, 2000], 5, "bf16"),      # row bounds at page edges, in slots
+    (16, 2, [1, 700, 1025], 7, "e4m3"),
+    (16, 2, [3, 500, 90, 7], 12, "bf16"),              # owner mask: gather 4, keep 1 of 3
 ]
 
 
@@ -84,7 +87,7 @@ def test_a_long_causal_request_split_across_ctas():
     assert_lse_close(lse, rl, 0, what="long causal")
 
 
-@pytest.mark.parametrize("T,num_parts", [(2, 8), (4, 4)])
+@pytest.mark.parametrize("T,num_parts", [(2, 8), (4, 4), (3, 3), (2, 7)])
 def test_all_partitions_call_with_several_query_tokens(T, num_parts):
     lens = [1, 2, T + 3, 700, 5000]
     case = workloads.make_decode_case("mtp_dcp", 16, lens, seed=T, device="cuda", q_len=T,
