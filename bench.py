@@ -787,7 +787,8 @@ def run_dcp_parts(args, world, rank, local):
     GB/s counts each cached row once."""
     mla, dev, stream = gpu_setup(world, rank, local)
     P = args.parts
-    case = workloads.config_long32k(device=dev, seed=args.seed)
+    case = workloads.config_long32k(device=dev, seed=args.seed, batch=args.batch,
+                                    pool_pages=args.pool_pages)
     B, H = case.batch, case.heads
     kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
     ws = mla.make_dcp_workspace(case.q, case.kv_pages, case.block_table, P)
@@ -803,7 +804,10 @@ def run_dcp_parts(args, world, rank, local):
                                  sample_clocks=True)
     assert mla.check_workspace(ws) == 0
     g = math.gcd(P, 8)
+    one_launch = P <= 8
     path = ("one launch for all partitions" if 8 % P == 0 else
+            "one launch for all partitions, strided gather (rows y0 + kP of each page)"
+            if one_launch else
             "one launch per partition, owner mask over the gather of partition r mod %d" % g
             if P // g <= 16 else "the CUDA-core kernel, one launch per partition")
     line = _line(args, world, ms, B, "tokens/s",
@@ -813,11 +817,11 @@ def run_dcp_parts(args, world, rank, local):
                   "parallelism": "DCP partitions emulated on one GPU"},
                  _hbm_roofline(kv_bytes, ms, args.steps,
                                "mla_decode_dcp: every partition's decode and the merge, timed "
-                               "together per call (rows gathered P / gcd(P, 8) times when P "
+                               "together per call (rows gathered P / gcd(P, 8) times when P > 8 "
                                "does not divide 8)"),
                  {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                   "d2h_bytes_per_step": 0, "note": "device-only: see the decode op's e2e"},
-                 (2 if 8 % P == 0 else 2 * P + 1) * args.steps, clock_info)
+                 (2 if one_launch else 2 * P + 1) * args.steps, clock_info)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
