@@ -48,8 +48,9 @@ def _call(lib, case, part_id, base, out, lse):
         out.data_ptr(), lse.data_ptr(), ctypes.byref(d), stream)
 
 
-def test_noalloc_matches_the_workspace_entry_point_twice_in_a_row(lib):
-    case = workloads.make_decode_case("noalloc", 64, [5000, 77, 12000, 1, 0], num_parts=2,
+@pytest.mark.parametrize("num_parts", [2, 3])  # a gather of 64/P rows per page; the strided gather
+def test_noalloc_matches_the_workspace_entry_point_twice_in_a_row(lib, num_parts):
+    case = workloads.make_decode_case("noalloc", 64, [5000, 77, 12000, 1, 0], num_parts=num_parts,
                                       seed=31, device="cuda", pool_pages=400)
     for call, (part_id, base) in enumerate([(0, 0), (1, 1)]):
         ref_out, ref_lse = run_partial(case, part_id, base)
@@ -60,7 +61,7 @@ def test_noalloc_matches_the_workspace_entry_point_twice_in_a_row(lib):
         ref = ref_out.double().cpu().numpy()
         assert_out_close(out, ref, what=f"no-alloc call {call}")
         assert_lse_close(lse, ref_lse.double().cpu().numpy(), base, what=f"no-alloc call {call}")
-        # num_parts = 2 runs the same tensor-core kernels on the same grid
+        # the same tensor-core kernels on the same grid
         assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), call
         assert torch.equal(lse, ref_lse), call
 
