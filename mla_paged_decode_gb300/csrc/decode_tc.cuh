@@ -29,12 +29,12 @@
 // sm_scale * kv_scale / (that power of two).
 //
 // Partitions: P divides 8 here (64/P owned rows per page), or P in
-// {3, 5, 6, 7}: the strided gather
-// (DecodeParams::strided; one box per 8-row atom, rows y0 + kP of a page,
-// through the several-row variants, which mask a tile's empty slots).  A
-// call for another P runs the gather of P' = gcd(P, 8) with an owner mask in the
-// softmax (DecodeParams::own_parts), through the several-query-token
-// variants, which carry the per-row bounds and guards that mask needs.
+// {3, 5, 6, 7}: the strided gather (MULTI == 2, DecodeParams::strided), where
+// producer lane k loads atom k of the tile, rows y0 + iP of its page through a
+// TMA traversal stride, and the softmax masks the tile's empty slots.  A call
+// for another P runs the gather of P' = gcd(P, 8) with an owner mask in the
+// softmax (DecodeParams::own_parts), through the several-row variants
+// (MULTI == 1), which carry the per-row bounds and guards that mask needs.
 //
 // Pipeline per tile i (stage / S buffer i mod 2): producer -> kv_full (per
 // column group) -> MMA S_i (36 MMAs, two interleaved accumulators so
