@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace mla {
 
 constexpr int kDqk = 576;        // 512 latent + 64 rope
@@ -87,11 +90,50 @@ struct DecodeParams {
   int lse_base2;              // output lse in base 2 (else natural)
 };
 
+// ---------------------------------------------------------------- host: per-device set-up
+
+// Raises one kernel's dynamic shared-memory limit on each device the first
+// time it is launched there.  Thread-safe: host threads that launch on the
+// same device for the first time at once take a lock, and later launches
+// read only an atomic flag.  One static instance per kernel.
+struct SmemLimitOnce {
+  std::atomic<uint64_t> done{0};  // bit d: set on device d
+  std::mutex mu;
+  template <typename Kernel>
+  cudaError_t ensure(Kernel kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
+
 // ---------------------------------------------------------------- partition rule
 
 // Tokens owned by partition r of P out of a global length L: t < L, t mod P == r.
 __host__ __device__ __forceinline__ int local_len(int L, int P, int r) {
   return L / P + (r < L % P ? 1 : 0);
+}
+
+// Virtual request v -> its output row b and head group g: group-major,
+// v = g * batch + b.  The split schedule cuts the concatenated tile sequence
+// of all virtual requests into equal cost ranges, one per CTA; in this order
+// the head groups of a request (or the query-token groups of a request with
+// several query tokens) sit at the same offset of head_groups equal stretches
+// of that sequence, so CTAs c, c + G / head_groups, ... walk the same pages
+// at the same time and the later reads of a page find it in L2: the cache
+// is read from HBM once for all rows of a request.
+__host__ __device__ __forceinline__ int vreq_row(const DecodeParams &p, int v) { return v % p.batch; }
+__host__ __device__ __forceinline__ int vreq_group(const DecodeParams &p, int v) { return v / p.batch; }
+__host__ __device__ __forceinline__ int vreq_index(const DecodeParams &p, int b, int g) {
+  return g * p.batch + b;
 }
 
 // Output row bv -> the input request it reads (q, block table, length) and
@@ -171,9 +213,9 @@ struct StridedMask {
 // compile-time switch, so that each kernel keeps only its own length rule.
 template <int MULTI = 0>
 __device__ __forceinline__ int request_len(const DecodeParams &p, int v, int *err) {
-  int bv = v / p.head_groups;
+  int bv = vreq_row(p, v);
   int L = checked_len(p, req_of(p, bv), err);
-  if (MULTI) L = group_len(p, L, v % p.head_groups);
+  if (MULTI) L = group_len(p, L, vreq_group(p, v));
   // under an owner mask, a request the real partition owns no token of is
   // empty (the neutral pair), however many the gathered partition holds
   if (MULTI && p.own_parts > p.num_parts && local_len(L, p.own_parts, p.own_part) == 0) return 0;
@@ -218,7 +260,7 @@ __device__ __forceinline__ int request_tiles(const DecodeParams &p, int v) {
 // ---------------------------------------------------------------- split schedule
 //
 // Cost-weighted stream-K split of the concatenated tile sequence of all
-// virtual requests v = b * head_groups + g (tiles_v = ceil(local_len / 64)).
+// virtual requests v = g * batch + b (tiles_v = ceil(local_len / 64)).
 // Every request with tiles costs tiles_v + kPieceCost: the extra units stand
 // for the per-piece work (Q load, pipeline refill, epilogue), so a CTA whose
 // range crosses a request boundary gets fewer tiles.  Request v occupies cost

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) decode_simt_kernel(DecodePara
     const int tiles = request_tiles(p, v);
     if (tiles == 0) { ++v; continue; }
     const long long t0 = max(r.start, pv) - pv, t1 = min(r.end, pv + tiles) - pv;
-    const int b = v / p.head_groups, g = v % p.head_groups;
+    const int b = vreq_row(p, v), g = vreq_group(p, v);
     const int n = local_len(checked_len(p, b, tid == 0 ? err : nullptr), p.num_parts, p.part_id);
 
     __syncthreads();  // previous request's shared reads are done
@@ -201,18 +201,11 @@ __global__ void __launch_bounds__(kSimtThreads, 1) decode_simt_kernel(DecodePara
 cudaError_t launch_split_merge(const DecodeParams &p, int grid, cudaStream_t stream);
 
 cudaError_t launch_decode_simt(const DecodeParams &p, int grid, cudaStream_t stream) {
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(sizeof(SimtSmem)));
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  static SmemLimitOnce smem_limit;
+  cudaError_t e = smem_limit.ensure(decode_simt_kernel, int(sizeof(SimtSmem)));
+  if (e != cudaSuccess) return e;
   decode_simt_kernel<<<grid, kSimtThreads, sizeof(SimtSmem), stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   return e == cudaSuccess ? launch_split_merge(p, grid, stream) : e;
 }
 

@@ -148,8 +148,8 @@ struct Walk {
       if (tiles == 0) { ++v; continue; }
       t0 = max(r.start, pv) - pv;
       t1 = min(r.end, pv + tiles) - pv;
-      b = v / p.head_groups;
-      g = v % p.head_groups;
+      b = vreq_row(p, v);
+      g = vreq_group(p, v);
       rb = FUSED ? b % p.req_batch : b;
       part = FUSED ? b / p.req_batch : p.part_id;
       pc = FUSED ? part : 0;
@@ -1087,16 +1087,9 @@ cudaError_t launch_dcp_merge_combine(const DecodeParams &p, int grid, cudaStream
 template <bool F8, bool FUSED, int MULTI, int AHEAD>
 static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
                              const CUtensorMap &tm_kvg, int grid, cudaStream_t stream) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<F8, FUSED, MULTI, AHEAD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
+  static SmemLimitOnce smem_limit;
+  const cudaError_t e = smem_limit.ensure(decode_tc_kernel<F8, FUSED, MULTI, AHEAD>, tc::kSmemBytes);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(tc_threads<F8>());

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 7) split_merge_kernel(Decode
   // grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int v = blockIdx.x;
-  const int b = v / p.head_groups, g = v % p.head_groups;
+  const int b = vreq_row(p, v), g = vreq_group(p, v);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hl = blockIdx.y * kMergeWarps + warp;  // head within the group
   const int group_heads = min(p.heads_per_group, p.heads - g * p.heads_per_group);
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kDcpMaxParts * 32) dcp_merge_combine_kernel(De
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   {
     const int bv = warp * p.req_batch + b;  // partition `warp` of request b
-    const int v = bv * p.head_groups + g;
+    const int v = vreq_index(p, bv, g);
     const size_t prow = size_t(bv) * rows + r;
     uint32_t pk[8];
     float l;  // the partition's lse as returned (in the output base)

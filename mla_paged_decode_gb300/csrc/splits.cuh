@@ -46,7 +46,7 @@ __device__ inline void write_empty_requests(const DecodeParams &p) {
   const int V = p.batch * p.head_groups;
   int *err = error_word(p);
   for (int v = blockIdx.x; v < V; v += gridDim.x) {
-    int b = v / p.head_groups, g = v % p.head_groups;  // b: output row
+    int b = vreq_row(p, v), g = vreq_group(p, v);  // b: output row
     if (request_len<MULTI>(p, v, threadIdx.x == 0 ? err : nullptr) != 0) continue;
     int h0 = g * p.heads_per_group;
     int hn = min(p.heads_per_group, p.heads - h0);

@@ -79,3 +79,20 @@ def assert_neutral(gpu_out, gpu_lse, mask_rows):
     for b in mask_rows:
         assert torch.all(o[b].view(torch.int16) == 0), f"request {b}: out not exactly 0"
         assert torch.all(torch.isneginf(l[b])), f"request {b}: lse not -inf"
+
+
+def check_requests(oracle, case, out, lse, part_id, lse_base, requests, atol=OUT_ATOL,
+                   num_parts=None, chunk=8, what=""):
+    """Every request in `requests` against the oracle, `chunk` requests at a
+    time (only their pages leave the GPU, so host memory stays bounded).
+    out / lse are the GPU results for the whole batch ([B, 1, H, 512] and
+    [B, 1, H]); returns the largest absolute output error seen."""
+    worst = 0.0
+    requests = list(requests)
+    for i in range(0, len(requests), chunk):
+        sel = requests[i:i + chunk]
+        ro, rl = oracle_partial_sub(oracle, case, sel, part_id, lse_base, num_parts=num_parts)
+        w = f"{what} requests {sel[0]}..{sel[-1]}"
+        worst = max(worst, assert_out_close(out[sel], ro[:, None], atol=atol, what=w))
+        assert_lse_close(lse[sel], rl[:, None], lse_base, what=w)
+    return worst

@@ -10,7 +10,7 @@ import torch
 import mla_paged_decode_gb300 as mla
 import oracle
 import workloads
-from casebits import case_bits
+from casebits import case_bits, subcase_bits
 from gpu_helpers import FP8_ATOL, assert_lse_close, assert_out_close
 
 pytestmark = pytest.mark.gpu
@@ -104,3 +104,21 @@ def test_all_partitions_call_with_several_query_tokens(T, num_parts):
     fo, fl = oracle.decode_partial_causal(q, kv, bt, sl, 0, 1, case.sm_scale, 1)
     assert_out_close(out, fo, what="merged")
     assert_lse_close(out_lse, fl, 1, what="merged")
+
+
+def test_two_query_tokens_on_the_32k_batch_every_request():
+    """The 32K-context batch with two query tokens per request (two 64-row
+    groups per request, the layout whose groups walk the same pages side by
+    side), every request against the oracle, 8 at a time."""
+    case = workloads.config_long32k(device="cuda", q_len=2)
+    B = case.batch
+    out = torch.full((B, 2, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, 2, 64), float("nan"), dtype=torch.float32, device="cuda")
+    mla.decode_partial(case.q, case.kv_pages, case.block_table, case.seq_lens, 0, 1,
+                       case.sm_scale, 0, out, lse)
+    for i in range(0, B, 8):
+        sel = list(range(i, i + 8))
+        q, kv, bt, sl = subcase_bits(case, sel)
+        ro, rl = oracle.decode_partial_causal(q, kv, bt, sl, 0, 1, case.sm_scale, 0)
+        assert_out_close(out[sel], ro, what=f"requests {sel[0]}..{sel[-1]}")
+        assert_lse_close(lse[sel], rl, 0, what=f"requests {sel[0]}..{sel[-1]}")

@@ -1,7 +1,8 @@
 """GPU parity of mla_decode_dcp (all partitions in one call, then their merge):
 every partition's (out, lse) against the oracle's partition, the merged
 result against the unpartitioned oracle, the merge against mla_lse_combine of
-the returned partials (bit for bit), and the full-size DCP workload sampled.
+the returned partials (bit for bit), and the full-size DCP workload: every
+partition of 20 of its 64 requests (the four short ones among them).
 """
 import numpy as np
 import pytest
@@ -12,7 +13,7 @@ import oracle
 import workloads
 from casebits import case_bits
 from gpu_helpers import (FP8_ATOL, assert_lse_close, assert_neutral, assert_out_close,
-                         oracle_partial_sub, run_partial)
+                         check_requests, run_partial)
 
 pytestmark = pytest.mark.gpu
 
@@ -87,16 +88,19 @@ def test_full_size_dcp8_in_one_call():
     out, _, parts, plses = mla.decode_dcp(case.q, case.kv_pages, case.block_table, case.seq_lens,
                                           8, case.sm_scale, 1, workspace=ws)
     assert mla.check_workspace(ws) == 0
-    short = [60, 61, 62, 63]   # L = 1, 3, 5, 7
-    sample = [0, 59] + short
+    long_ = list(range(0, 60, 4)) + [59]   # 16 of the 60 long requests
+    short = [60, 61, 62, 63]               # L = 1, 3, 5, 7
     lens = case.seq_lens.cpu().tolist()
     for r in range(8):
-        ro, rl = oracle_partial_sub(oracle, case, sample, r, 1)
-        assert_out_close(parts[r][sample], ro[:, None], what=f"dcp8 partition {r}")
-        assert_lse_close(plses[r][sample], rl[:, None], 1, what=f"dcp8 partition {r}")
+        check_requests(oracle, case, parts[r], plses[r], r, 1, long_ + short, chunk=4,
+                       what=f"dcp8 partition {r}")
         assert_neutral(parts[r], plses[r], [b for b in short if r >= lens[b]])
-    fo, _ = oracle_partial_sub(oracle, case, sample, 0, 1, num_parts=1)
-    assert_out_close(out[sample], fo[:, None], what="dcp8 merged vs unpartitioned")
+    out_lse = torch.empty(B, 1, H, dtype=torch.float32, device="cuda")
+    out2, _, _, _ = mla.decode_dcp(case.q, case.kv_pages, case.block_table, case.seq_lens, 8,
+                                   case.sm_scale, 1, workspace=ws, out_lse=out_lse)
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+    check_requests(oracle, case, out, out_lse, 0, 1, long_ + short, num_parts=1, chunk=4,
+                   what="dcp8 merged vs unpartitioned")
     # partition 3 computed alone agrees with its slice of the fused launch
     alone, alone_lse = run_partial(case, 3, 1)
     assert_out_close(parts[3], alone.float().cpu().numpy().astype(np.float64), what="fused vs alone")

@@ -2,8 +2,11 @@
 
 Small cases are compared element by element on every request and partition;
 the full-size workloads (the configuration the bench times, in the same launch
-configuration) on sampled requests the oracle computes one by one, plus the
-properties that hold at any size (finite outputs, exact neutral pairs).
+configuration) on every request of the 32K-context and e4m3 batches and on
+every partition of 20 of the 64 requests of the eight-partition batch (the
+four short ones among them), which the oracle computes a few requests at a
+time, plus the properties that hold at any size (finite outputs, exact
+neutral pairs).
 """
 import numpy as np
 import pytest
@@ -14,7 +17,12 @@ import oracle
 import workloads
 from casebits import case_bits
 from gpu_helpers import (FP8_ATOL, assert_lse_close, assert_neutral, assert_out_close,
-                         oracle_partial_sub, run_partial)
+                         check_requests, oracle_partial_sub, run_partial)
+
+# the long requests of the eight-partition batch checked at full size, then
+# its four short ones (L = 1, 3, 5, 7)
+DCP8_LONG = list(range(0, 60, 4)) + [59]
+DCP8_SHORT = [60, 61, 62, 63]
 
 pytestmark = pytest.mark.gpu
 
@@ -137,15 +145,11 @@ def test_single_request_spread_over_every_cta():
     assert_lse_close(lse, rl[:, None], 0)
 
 
-def test_long32k_full_size_sampled():
+def test_long32k_full_size_every_request():
     case = workloads.config_long32k(device="cuda")
     out, lse = run_partial(case, 0, 0)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
-    lens = case.seq_lens.cpu()
-    sample = sorted({0, 31, 63, int(lens.argmax()), int(lens.argmin())})
-    ro, rl = oracle_partial_sub(oracle, case, sample, 0, 0)
-    assert_out_close(out[sample], ro[:, None], what="long32k sample")
-    assert_lse_close(lse[sample], rl[:, None], 0, what="long32k sample")
+    check_requests(oracle, case, out, lse, 0, 0, range(case.batch), what="long32k")
 
 
 def test_dcp8_full_size_partials_and_combine():
@@ -157,28 +161,24 @@ def test_dcp8_full_size_partials_and_combine():
     for r in range(8):
         run_partial(case, r, 1, workspace=ws, out=outs[r], lse=lses[r])
     assert mla.check_workspace(ws) == 0
-    short = [60, 61, 62, 63]   # L = 1, 3, 5, 7
-    sample = [0, 59] + short
+    lens = case.seq_lens.cpu().tolist()
     for r in range(8):
-        ro, rl = oracle_partial_sub(oracle, case, sample, r, 1)
-        assert_out_close(outs[r][sample], ro[:, None], what=f"dcp8 part {r}")
-        assert_lse_close(lses[r][sample], rl[:, None], 1, what=f"dcp8 part {r}")
-        lens = case.seq_lens.cpu().tolist()
-        assert_neutral(outs[r], lses[r], [b for b in short if r >= lens[b]])
-    merged = torch.empty(B, H, 512, dtype=torch.bfloat16, device="cuda")
-    mla.lse_combine(outs.view(8, B, H, 512), lses.view(8, B, H), 8, merged, lse_base=1)
-    fo, _ = oracle_partial_sub(oracle, case, sample, 0, 1, num_parts=1)
-    assert_out_close(merged[sample], fo, what="dcp8 merged vs unpartitioned")
+        check_requests(oracle, case, outs[r], lses[r], r, 1, DCP8_LONG + DCP8_SHORT, chunk=4,
+                       what=f"dcp8 part {r}")
+        assert_neutral(outs[r], lses[r], [b for b in DCP8_SHORT if r >= lens[b]])
+    merged = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device="cuda")
+    merged_lse = torch.empty(B, 1, H, dtype=torch.float32, device="cuda")
+    mla.lse_combine(outs.view(8, B, H, 512), lses.view(8, B, H), 8, merged.view(B, H, 512),
+                    lse_base=1, out_lse=merged_lse.view(B, H))
+    check_requests(oracle, case, merged, merged_lse, 0, 1, DCP8_LONG + DCP8_SHORT, num_parts=1,
+                   chunk=4, what="dcp8 merged vs unpartitioned")
 
 
-def test_fp8_full_size_sampled():
+def test_fp8_full_size_every_request():
     case = workloads.config_fp8(device="cuda")
     out, lse = run_partial(case, 0, 0)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
-    sample = [0, 1, 64, 127]
-    ro, rl = oracle_partial_sub(oracle, case, sample, 0, 0)
-    assert_out_close(out[sample], ro[:, None], atol=FP8_ATOL, what="fp8 sample")
-    assert_lse_close(lse[sample], rl[:, None], 0, what="fp8 sample")
+    check_requests(oracle, case, out, lse, 0, 0, range(case.batch), atol=FP8_ATOL, what="fp8")
 
 
 def test_outputs_are_deterministic_and_placement_free():
