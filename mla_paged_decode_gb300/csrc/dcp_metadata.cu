@@ -3,7 +3,10 @@
 // _apply_dcp_cuda_graph_metadata): global lengths (+ the draft tokens of a
 // target-verify step), the rank-local lengths under the round-robin owner
 // rule, and the rank-local page table over the rank's compact pool (local
-// page i of a request = the pool page of its local token 64 i).
+// page i of a request = the pool page of its local token 64 i).  A page table
+// can only describe a pool that holds each request's local tokens in whole
+// pages, so a slot of local token 64 i that is negative or not the first slot
+// of a page pads that page and sets the error word.
 //
 // A warp per request: lane 0 writes the lengths, the lanes fill the table row.
 #include "common.cuh"
@@ -37,7 +40,7 @@ __global__ void __launch_bounds__(kMetaWarps * 32)
     int32_t v = pad;
     if (ok && i < npages) {
       const int32_t slot = req_to_token[size_t(req) * r2t_width + size_t(i) * kPage];
-      if (slot < 0)
+      if (slot < 0 || slot % kPage != 0)
         neg = true;
       else
         v = slot / kPage;

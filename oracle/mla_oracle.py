@@ -68,8 +68,10 @@ def dcp_local_metadata(seq_lens, req_pool_indices, req_to_token, part_id: int, n
     pad_value after.  A request is counted bad (and its whole table row is
     pad_value) if its global length is negative (local length 0), its pool
     index is outside req_to_token, its pages do not fit max_pages or the
-    width of req_to_token; a negative token slot gives pad_value for that
-    page and also counts the request.  Returns (global, local, table, bad)."""
+    width of req_to_token; a token slot that is negative, or not the first
+    slot of a pool page (a page table can only describe a pool that holds a
+    request's local tokens in whole pages), gives pad_value for that page and
+    also counts the request.  Returns (global, local, table, bad)."""
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
     r2t = np.asarray(req_to_token)
     B = len(seq_lens)
@@ -92,7 +94,7 @@ def dcp_local_metadata(seq_lens, req_pool_indices, req_to_token, part_id: int, n
         neg = False
         for i in range(npages):
             slot = int(r2t[req, i * page_size])
-            if slot < 0:
+            if slot < 0 or slot % page_size != 0:
                 neg = True
             else:
                 table[b, i] = slot // page_size

@@ -48,14 +48,18 @@ def test_table_recovers_the_page_assignment():
 def test_bad_requests_are_counted_and_padded():
     r2t = np.arange(2 * 256, dtype=np.int32).reshape(2, 256)
     r2t[1, 64] = -1                                        # a negative slot
-    lens = np.array([-5, 100, 100, 1000, 200], dtype=np.int32)
-    idx = np.array([0, 5, 1, 0, 0], dtype=np.int32)       # request 1: no such pool row
+    r2t[0, 128] += 3                                       # a slot inside a page
+    lens = np.array([-5, 100, 100, 1000, 200, 150, 128], dtype=np.int32)
+    idx = np.array([0, 5, 1, 0, 0, 0, 0], dtype=np.int32)  # request 1: no such pool row
     g, loc, table, bad = oracle.dcp_local_metadata(lens, idx, r2t, 0, 1, max_pages=3, pad_value=9)
     # -5: negative; idx 5: outside; request 2: slot -1 on its second page;
-    # 1000 tokens: 16 pages > 3; 200 tokens: 4 pages > 3
-    assert bad == 5
+    # 1000 tokens: 16 pages > 3; 200 tokens: 4 pages > 3; 150 tokens: its
+    # third page starts at a slot that is not a page's first (128 tokens
+    # stop short of it and are fine)
+    assert bad == 6
     assert loc[0] == 0 and (table[[0, 1, 3, 4]] == 9).all()
     assert table[2, 0] == r2t[1, 0] // 64 and table[2, 1] == 9 and table[2, 2] == 9
+    assert list(table[5]) == [0, 1, 9] and list(table[6]) == [0, 1, 9]
 
 
 @pytest.mark.parametrize("r,P", [(0, 1), (1, 2), (2, 4), (5, 8)])

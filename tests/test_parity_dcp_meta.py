@@ -35,9 +35,14 @@ def test_metadata_matches_the_oracle(num_parts, extra):
     B, width, slots = 37, 4096, 50
     lens = rng.integers(0, 3000, size=B).astype(np.int32)
     lens[:4] = [0, 1, num_parts - 1, 64 * num_parts]
-    idx = rng.integers(0, slots, size=B).astype(np.int32)
-    r2t = rng.integers(0, 1 << 20, size=(slots, width)).astype(np.int32)
+    idx = rng.integers(0, slots - 1, size=B).astype(np.int32)
+    # a pool in whole pages: slot = 64 * (a random page) + the token's row
+    pages = rng.integers(0, 1 << 14, size=(slots, width // 64)).astype(np.int32)
+    r2t = (64 * np.repeat(pages, 64, axis=1) + np.tile(np.arange(64, dtype=np.int32), width // 64))
+    r2t = np.ascontiguousarray(r2t.astype(np.int32))
     lens[5], idx[6], r2t[idx[7], 0] = -3, slots + 2, -1       # the bad cases
+    lens[8], idx[8] = 300 * num_parts, slots - 1              # and a slot inside a page
+    r2t[slots - 1, 128] += 5
     for r in range(num_parts):
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         g, loc, tab = mla.dcp_local_metadata(_dev(lens), _dev(idx), _dev(r2t), r, num_parts,
@@ -48,6 +53,24 @@ def test_metadata_matches_the_oracle(num_parts, extra):
         np.testing.assert_array_equal(loc.cpu().numpy(), ol)
         np.testing.assert_array_equal(tab.cpu().numpy(), ot)
         assert (int(err.item()) != 0) == (bad > 0)
+
+
+def test_metadata_flags_a_slot_inside_a_page():
+    # two requests of 200 tokens (4 local pages each) over a pool in whole
+    # pages; then the same with one fault only: request 1's second local page
+    # starting one slot into a page
+    aligned = np.ascontiguousarray((np.arange(2 * 256, dtype=np.int32) + 64 * 7).reshape(2, 256))
+    faulted = aligned.copy()
+    faulted[1, 64] += 1
+    lens, idx = np.array([200, 200], np.int32), np.array([0, 1], np.int32)
+    for r2t, fault in ((aligned, False), (faulted, True)):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        _, _, tab = mla.dcp_local_metadata(_dev(lens), _dev(idx), _dev(r2t), 0, 1, max_pages=4,
+                                           pad_value=-1, error_word=err)
+        _, _, ot, bad = oracle.dcp_local_metadata(lens, idx, r2t, 0, 1, 0, 4, -1)
+        np.testing.assert_array_equal(tab.cpu().numpy(), ot)
+        assert bad == int(fault) and (int(err.item()) != 0) == fault
+        assert (ot[1, 1] == -1) == fault and list(ot[0]) == [7, 8, 9, 10]
 
 
 @pytest.mark.parametrize("kv_dtype,heads,num_parts", [("bf16", 16, 8), ("bf16", 64, 2),
