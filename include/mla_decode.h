@@ -206,7 +206,12 @@ int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_tab
  * different host threads) race and must be serialised by the caller.  Each
  * call clears the array's error word before its kernels; kernel-side bounds
  * errors are not reported by this variant (use mla_decode_partial with
- * mla_decode_check_workspace to diagnose them).
+ * mla_decode_check_workspace to diagnose them).  The kernels are those of
+ * mla_decode_partial (tensor cores whenever num_parts / gcd(num_parts, 8)
+ * <= 16, else the CUDA-core kernel) on at most 152 CTAs, the number of split
+ * partials the array holds: on a GPU with at most 152 SMs the outputs equal
+ * mla_decode_partial's bit for bit; with more SMs the split points differ,
+ * and so may the rounding of requests cut across CTAs.
  */
 int mla_decode_partial_noalloc(const void *q, const void *kv_pages, const int32_t *block_table,
                                const int32_t *seq_lens, int part_id, int num_parts,

@@ -116,8 +116,11 @@ extern "C" int mla_decode_partial_noalloc(const void *q, const void *kv_pages,
   // The scratch keeps the previous call's contents: the error word must start
   // at zero (every other part is rewritten before it is read).
   if (cudaMemsetAsync(dev.scratch, 0, 256, s) != cudaSuccess) return MLA_ERR_CUDA;
-  // the kernels of mla_decode_partial (tensor-core when num_parts divides 8)
-  // on the built-in scratch
+  // the kernels of mla_decode_partial on the built-in scratch: the
+  // tensor-core kernel whenever num_parts / gcd(num_parts, 8) <= 16 (the
+  // strided gather and the owner mask included), else the CUDA-core kernel.
+  // The split layout depends on the grid, so the outputs equal
+  // mla_decode_partial's bit for bit on GPUs with at most 152 SMs.
   return mla::enqueue_partial(q, kv_pages, block_table, seq_lens, part_id, num_parts, sm_scale,
                               lse_base, out, lse, d, dev.scratch, grid, s);
 }

@@ -61,9 +61,11 @@ def test_noalloc_matches_the_workspace_entry_point_twice_in_a_row(lib, num_parts
         ref = ref_out.double().cpu().numpy()
         assert_out_close(out, ref, what=f"no-alloc call {call}")
         assert_lse_close(lse, ref_lse.double().cpu().numpy(), base, what=f"no-alloc call {call}")
-        # the same tensor-core kernels on the same grid
-        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), call
-        assert torch.equal(lse, ref_lse), call
+        # the same tensor-core kernels on the same grid (the no-alloc grid is
+        # capped at 152 CTAs: with more SMs the split points differ)
+        if torch.cuda.get_device_properties(0).multi_processor_count <= 152:
+            assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), call
+            assert torch.equal(lse, ref_lse), call
 
 
 def test_noalloc_refuses_batches_beyond_its_scratch(lib):
