@@ -9,7 +9,12 @@ than the 129 MB L2, so no flush is needed between steps.  Prints one JSON line:
 tokens/s (one new token per request per step), KV GB/s and its fraction of
 the measured HBM copy peak, the end-to-end figure through the C ABI with host
 buffers, the fp64 CPU oracle timed on the host cores, and SM clocks sampled
-during the timed region.
+from before the warm-up to after the timed region (the GPU kept under the
+same load throughout).  At one GPU the line also carries, under "configs",
+the same record for the other workloads, measured in the same process: the
+small two-partition case (B=1, H=16, L=300, P=2), the eight-partition DCP
+batch (B=64, H=16, 60 x 131072 + {1, 3, 5, 7}), the e4m3 batch (B=128,
+H=128) and the standalone LSE combine (P=8, T up to 128).
 
 N > 1 (torchrun, one process per GPU): every rank runs its own replica of the
 workload (the method's partitions are emulated on one GPU; there is no
@@ -44,6 +49,10 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 ROW_BYTES = {"bf16": 576 * 2, "e4m3": 576}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_partial_long32k_traffic.txt")
+DCP8_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_dcp_dcp8_traffic.txt")
+FP8_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_partial_fp8_traffic.txt")
+SMALL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_dcp_small_traffic.txt")
+COMBINE_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lse_combine_t128_traffic.txt")
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -114,13 +123,13 @@ def kernel_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
-    if not os.path.exists(TRAFFIC_FILE):
+def recorded_traffic(path=TRAFFIC_FILE):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, if
+    it was taken on the current kernel source (else None)."""
+    if not os.path.exists(path):
         return None
     kv = {}
-    for line in open(TRAFFIC_FILE):
+    for line in open(path):
         if "=" in line and not line.startswith("#"):
             k, v = line.strip().split("=", 1)
             kv[k.strip()] = v.strip()
@@ -133,7 +142,12 @@ def recorded_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background.
+
+    Started before the warm-up: wait_first() returns once nvidia-smi has
+    written its first sample (taken before any load, so stop() leaves it
+    out), and the caller then keeps the GPU under the step's load from
+    before the warm-up until after the timed region."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -158,6 +172,24 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def wait_first(self, timeout_s: float = 5.0) -> bool:
+        """True once the first sample line is on disk (False on timeout)."""
+        if self.proc is None:
+            return False
+        t_end = time.perf_counter() + timeout_s
+        while time.perf_counter() < t_end:
+            self.out.flush()
+            try:
+                with open(self.path) as f:
+                    if f.read().count("\n") >= 1:
+                        return True
+            except OSError:
+                pass
+            if self.proc.poll() is not None:
+                return False
+            time.sleep(0.01)
+        return False
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
@@ -170,7 +202,8 @@ class ClockSampler:
         self.out.close()
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        lines = open(self.path).read().splitlines()
+        for line in lines[1:]:  # the first sample was taken before the load
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -187,7 +220,10 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "nvidia-smi every 50 ms while the GPU runs this step: %.2f s of the "
+                          "same steps before the warm-up, the warm-up, the timed region and "
+                          "%.2f s of the same steps after it" % (LOAD_BEFORE_S, LOAD_AFTER_S)}
 
 
 def gpu_setup(world: int, rank: int, local: int):
@@ -211,7 +247,17 @@ def timed_steps(step, steps: int, warmup: int, world: int, dev, stream, sample_c
     bracketed by a barrier and a synchronize on both sides and timed with CUDA
     events on `stream` (which side streams wait for before their first copy;
     `tail` runs after the last step, inside the region).  Returns the
-    milliseconds (max over ranks) and the clock record (or None)."""
+    milliseconds (max over ranks) and the clock record (or None).
+
+    With sample_clocks, nvidia-smi samples from before the warm-up until after
+    the timed region; untimed runs of the same step before the warm-up and
+    after the region keep the GPU under this load long enough for samples
+    even when the region itself lasts a few milliseconds."""
+    clocks = None
+    if sample_clocks:
+        clocks = ClockSampler(dev.index)
+        clocks.wait_first()
+        _load(step, LOAD_BEFORE_S, dev)
     for _ in range(warmup):
         step()
     if tail:
@@ -219,7 +265,6 @@ def timed_steps(step, steps: int, warmup: int, world: int, dev, stream, sample_c
     torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(dev.index) if sample_clocks else None
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for st in side_streams:
@@ -231,8 +276,24 @@ def timed_steps(step, steps: int, warmup: int, world: int, dev, stream, sample_c
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    info = clocks.stop() if clocks else None
+    info = None
+    if clocks:
+        _load(step, LOAD_AFTER_S, dev)
+        info = clocks.stop()
     return max_over_ranks(e0.elapsed_time(e1), world, dev), info
+
+
+LOAD_BEFORE_S = 0.4   # untimed runs of the step around a clock-sampled region
+LOAD_AFTER_S = 0.2
+
+
+def _load(step, seconds: float, dev):
+    """Runs step() for about `seconds` (untimed), in batches of 8 calls."""
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        for _ in range(8):
+            step()
+        torch.cuda.synchronize(dev)
 
 
 GRAPH_CALLS = 20  # calls captured in one graph
@@ -299,7 +360,31 @@ def _oracle_threads() -> int:
 # ---------------------------------------------------------------- the two arms
 
 def run_ours(args, world, rank, local):
+    """The headline line; at one GPU it also carries, under "configs", the
+    same record for each of the other workloads (the small two-partition
+    case, the eight-partition DCP batch, the e4m3 batch and the standalone
+    combine), measured in the same process."""
     mla, dev, stream = gpu_setup(world, rank, local)
+    line = measure_decode(args, world, rank, mla, dev, stream)
+    if world == 1 and not args.no_configs:
+        sub = argparse.Namespace(**vars(args))
+        sub.steps = min(max(args.steps, 20), 200)
+        sub.cpu_seconds = min(args.cpu_seconds, 6.0)
+        configs = {}
+        for measure in (measure_small, measure_dcp8, measure_fp8, measure_combine):
+            torch.cuda.empty_cache()
+            sub.batch = 128 if measure is measure_fp8 else 64  # each workload's own batch
+            rec = measure(sub, world, rank, mla, dev, stream)
+            configs[rec["config"]["workload"]] = rec
+        line["configs"] = configs
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_decode(args, world, rank, mla, dev, stream):
+    """One mla_decode_partial call (P = 1) over the 32K-context batch per step."""
     case = workloads.config_long32k(device=dev, seed=args.seed, batch=args.batch,
                                     pool_pages=args.pool_pages)
     if args.batch != 64 or args.pool_pages != 40000:
@@ -445,10 +530,7 @@ def run_ours(args, world, rank, local):
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    return line
 
 
 def run_reference(args, world, rank):
@@ -593,11 +675,22 @@ def run_append(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
-def run_dcp8(args, world, rank, local):
+def _print_line(make):
+    """Runs one op's measurement and prints its line (rank 0)."""
+    def run(args, world, rank, local):
+        mla, dev, stream = gpu_setup(world, rank, local)
+        line = make(args, world, rank, mla, dev, stream)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    return run
+
+
+def measure_dcp8(args, world, rank, mla, dev, stream):
     """--op dcp8: the decode-context-parallel workload (B=64, H=16, P=8; 60
     requests of 131072 tokens and four of 1, 3, 5, 7) as one mla_decode_dcp
     call per step: every partition's (out, lse) and their combine."""
-    mla, dev, stream = gpu_setup(world, rank, local)
     case = workloads.config_dcp8(device=dev, seed=args.seed)
     B, H, P = case.batch, case.heads, case.num_parts
     kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
@@ -647,7 +740,7 @@ def run_dcp8(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": kv_bytes / per_s / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": kv_bytes / per_s / 1e9 / peak,
                      "peak_source": peak_kind, "frac_of_8tbs": kv_bytes / per_s / 1e9 / 8000.0,
-                     "traffic": None,
+                     "traffic": recorded_traffic(DCP8_TRAFFIC_FILE),
                      "kernel": "mla_decode_dcp: one decode launch over the 8 partitions and "
                                "one split merge with the LSE combine fused, timed together "
                                "per call",
@@ -676,18 +769,18 @@ def run_dcp8(args, world, rank, local):
                                 "kind": "oracle",
                                 "sample": f"all {P} partitions of the first {done} of {B} requests "
                                           f"({tokens} cached tokens), fp64 numpy, {spent:.1f} s"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    return line
 
 
-def run_fp8(args, world, rank, local):
+run_dcp8 = _print_line(measure_dcp8)
+
+
+def measure_fp8(args, world, rank, mla, dev, stream):
     """--op fp8: the e4m3-cache workload (B=128, H=128, lognormal lengths with
     median 8192, per-tensor scale, P=1) through mla_decode_partial.  Its
     roofline is the tensor pipe: the MMAs run on f16 operands expanded from
-    the cache, and each 64-head group reads the cache again."""
-    mla, dev, stream = gpu_setup(world, rank, local)
+    the cache; the two 64-head groups of a request walk its pages side by
+    side on two SMs, so the second read of a page is served by L2."""
     case = workloads.config_fp8(device=dev, seed=args.seed, batch=args.batch)
     if args.batch != 128:
         case.name += f"_b{args.batch}"
@@ -735,12 +828,13 @@ def run_fp8(args, world, rank, local):
                                % args.seed,
                    "page_size": 64, "pool_pages": case.num_pages, "kv_dtype": "e4m3",
                    "kv_bytes_per_step": kv_bytes,
-                   "l2": "%.2f GB of e4m3 KV per step; each of the two 64-head groups reads it"
+                   "l2": "%.2f GB of e4m3 KV per step (more than L2); the two 64-head groups "
+                         "of a request read it side by side, the second read from L2"
                          % (kv_bytes / 1e9),
                    "parallelism": "single GPU"},
         "roofline": {"bound": "tensor", "achieved": flops / per_s / 1e12, "peak": tpeak,
                      "unit": "TFLOP/s", "frac": flops / per_s / 1e12 / tpeak,
-                     "peak_source": tpeak_kind, "traffic": None,
+                     "peak_source": tpeak_kind, "traffic": recorded_traffic(FP8_TRAFFIC_FILE),
                      "kernel": "mla_decode_partial on an e4m3 cache: decode kernel + split merge, "
                                "timed together per call (f16 MMAs on the expanded cache; real "
                                "heads' flops, QK^T over 576 dims and PV over 512)",
@@ -754,10 +848,10 @@ def run_fp8(args, world, rank, local):
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    return line
+
+
+run_fp8 = _print_line(measure_fp8)
 
 
 def _line(args, world, ms, units, unit, config, roofline, e2e, launches, clock_info,
@@ -832,7 +926,9 @@ def run_mtp(args, world, rank, local):
     """--op mtp --q-len T: T query tokens per request (multi-token prediction
     or target verify) on the 32K-context lengths, B=64, H=64, P=1; query token
     i attends to the tokens before L - T + i + 1.  One 64-row group per query
-    token: the cache is walked once per group."""
+    token, each on its own SM; the groups of a request walk its pages side by
+    side, so HBM serves each page once and L2 the other groups' reads.  KV
+    GB/s counts each cached row once."""
     mla, dev, stream = gpu_setup(world, rank, local)
     T = args.q_len
     case = workloads.config_long32k(device=dev, seed=args.seed, q_len=T)
@@ -855,9 +951,10 @@ def run_mtp(args, world, rank, local):
                   "num_parts": 1, "row_groups_per_request": groups, "kv_bytes_per_step": kv_bytes,
                   "l2": "inputs larger than L2: %.2f GB of KV per step" % (kv_bytes / 1e9),
                   "parallelism": "single GPU"},
-                 _hbm_roofline(kv_bytes * groups, ms, args.steps,
+                 _hbm_roofline(kv_bytes, ms, args.steps,
                                "mla_decode_partial with %d query tokens: decode kernel + split "
-                               "merge; bytes = the KV once per 64-row group (%d)" % (T, groups)),
+                               "merge; bytes = the KV once (%d 64-row groups read it side by "
+                               "side)" % (T, groups)),
                  {"value": None, "unit": "query tokens/s", "h2d_bytes_per_step": 0,
                   "d2h_bytes_per_step": 0, "note": "device-only: see the decode op's e2e"},
                  2 * args.steps, clock_info)
@@ -867,13 +964,14 @@ def run_mtp(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
-def run_combine(args, world, rank, local):
+def measure_combine(args, world, rank, mla, dev, stream):
     """--op combine: mla_lse_combine alone on the micro-benchmark shapes (P=8,
     H=16, D=512, T in {1, 8, 16, 32, 64, 128} tokens; partials N(0, 1) bf16,
     lse N(5, 3), one partition per token holding the neutral pair), each
     call replayed from CUDA graphs so that the small launches are timed on
-    the device.  value: GB/s at T = 128; every T in `points`."""
-    mla, dev, stream = gpu_setup(world, rank, local)
+    the device.  value: GB/s at T = 128; every T in `points`.  e2e: the
+    T = 128 call with its partials and lses copied in from pinned host
+    memory and its result read back, every step."""
     P, H, D = 8, 16, 512
     points = []
     for T in (1, 8, 16, 32, 64, 128):
@@ -893,8 +991,27 @@ def run_combine(args, world, rank, local):
         nbytes = c.partials.numel() * 2 + c.lses.numel() * 4 + out.numel() * 2 + out_lse.numel() * 4
         points.append({"tokens": T, "us_per_call": us, "gbs": nbytes / us / 1e3,
                        "bytes_per_call": nbytes})
+    # end to end at T = 128 through the C ABI with host buffers
+    parts_h, lses_h = c.partials.cpu().pin_memory(), c.lses.cpu().pin_memory()
+    parts_d, lses_d = torch.empty_like(c.partials), torch.empty_like(c.lses)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    olse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+
+    def e2e_step():
+        parts_d.copy_(parts_h, non_blocking=True)
+        lses_d.copy_(lses_h, non_blocking=True)
+        mla.lse_combine(parts_d, lses_d, P, out, lse_base=mla.LSE_NATURAL, out_lse=out_lse,
+                        stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        olse_h.copy_(out_lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e_ms, clock_info = timed_steps(e2e_step, args.steps, args.warmup, world, dev, stream,
+                                       sample_clocks=True)
     peak, peak_kind = measured_peaks()
     top = points[-1]
+    h2d = parts_h.numel() * 2 + lses_h.numel() * 4
+    d2h = out_h.numel() * 2 + olse_h.numel() * 4
     line = {
         "metric": "MLA LSE combine GB/s (P=8, H=16, D=512) on 1 GB300",
         "value": top["gbs"] * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -902,18 +1019,115 @@ def run_combine(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": "combine_p8_h16_d512", "points": points,
-                   "timing": "CUDA graphs of %d calls, replayed" % GRAPH_CALLS},
+                   "timing": "CUDA graphs of %d calls, replayed" % GRAPH_CALLS,
+                   "l2": "no flush: 19 MB per call at T = 128 stays in L2 (an upper bound "
+                         "on the HBM rate)"},
         "roofline": {"bound": "hbm", "achieved": top["gbs"], "peak": peak, "unit": "GB/s",
-                     "frac": top["gbs"] / peak, "peak_source": peak_kind, "traffic": None,
+                     "frac": top["gbs"] / peak, "peak_source": peak_kind,
+                     "traffic": recorded_traffic(COMBINE_TRAFFIC_FILE),
                      "kernel": "lse_combine_kernel at T = 128 (latency-bound below)"},
-        "e2e": {"value": None, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
-                "note": "a device-only micro-benchmark"},
+        "e2e": {"value": top["bytes_per_call"] / (e_ms / args.steps) / 1e6 * world, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "T = 128: partials and lses copied in from pinned host memory and the "
+                        "merged out and lse read back every step, one stream; GB/s counts the "
+                        "combine's own bytes"},
         "gpu_launches": args.steps * len(points),
+        "clocks": clock_info,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        pb = c.partials.view(torch.int16).cpu().numpy().view(np.uint16)
+        parts64 = oracle.bf16_to_f64(pb)
+        lses64 = c.lses.cpu().numpy().astype(np.float64)
+        spent, calls = 0.0, 0
+        while spent < min(args.cpu_seconds, 3.0):
+            a = time.perf_counter()
+            oracle.lse_combine(parts64, lses64, oracle.LSE_NATURAL)
+            spent += time.perf_counter() - a
+            calls += 1
+        line["cpu_baseline"] = {"value": top["bytes_per_call"] * calls / spent / 1e9,
+                                "unit": "GB/s", "cores": _oracle_threads(), "kind": "oracle",
+                                "sample": f"{calls} fp64 combines of the T = 128 case (8 x 128 x "
+                                          f"16 rows of 512), {spent:.1f} s; GB/s counts the "
+                                          f"kernel's bf16 / fp32 bytes"}
+    return line
+
+
+run_combine = _print_line(measure_combine)
+
+
+def measure_small(args, world, rank, mla, dev, stream):
+    """The small case: B=1, H=16, L=300, bf16, its two round-robin partitions
+    and their combine as one mla_decode_dcp call per step (one decode launch
+    for both partitions, one merge-and-combine launch).  Latency-bound: 345.6
+    KB of KV."""
+    case = workloads.config_small(device=dev, seed=args.seed)
+    B, H, P = case.batch, case.heads, case.num_parts
+    kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
+    ws = mla.make_dcp_workspace(case.q, case.kv_pages, case.block_table, P)
+    parts = torch.empty(P, B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+    plse = torch.empty(P, B, 1, H, dtype=torch.float32, device=dev)
+    out = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+    out_lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
+
+    def step(q=case.q, bt=case.block_table, sl=case.seq_lens):
+        mla.decode_dcp(q, case.kv_pages, bt, sl, P, case.sm_scale, 0, partials=parts,
+                       partial_lses=plse, out=out, out_lse=out_lse, workspace=ws, stream=stream)
+
+    ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
+                                 sample_clocks=True)
+    assert mla.check_workspace(ws) == 0
+    q_h, bt_h, sl_h = (case.q.cpu().pin_memory(), case.block_table.cpu().pin_memory(),
+                       case.seq_lens.cpu().pin_memory())
+    q_d, bt_d, sl_d = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        step(q_d, bt_d, sl_d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(out_lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e_ms, _ = timed_steps(e2e_step, args.steps, max(3, args.warmup), world, dev, stream)
+    roof = _hbm_roofline(kv_bytes, ms, args.steps,
+                         "mla_decode_dcp with P = 2: one decode launch for both partitions and "
+                         "one merge-and-combine launch, timed together per call; latency-bound "
+                         "(345.6 KB of KV, L2-resident across steps)")
+    roof["traffic"] = recorded_traffic(SMALL_TRAFFIC_FILE)
+    line = _line(args, world, ms, B, "tokens/s",
+                 {"workload": case.name, "batch": B, "heads": H, "q_len": 1, "num_parts": P,
+                  "seq_lens": "300", "page_size": 64, "pool_pages": case.num_pages,
+                  "kv_dtype": "bf16", "kv_bytes_per_step": kv_bytes,
+                  "l2": "no flush: 345.6 KB of KV stays in L2 (a latency measurement)",
+                  "parallelism": "DCP partitions emulated on one GPU"},
+                 roof,
+                 {"value": aggregate(e_ms, args.steps, B, world), "unit": "tokens/s",
+                  "h2d_bytes_per_step": q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4,
+                  "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4},
+                 2 * args.steps, clock_info)
+    line["us_per_step"] = ms * 1e3 / args.steps
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from casebits import case_bits
+        q, kv, bt, lens = case_bits(case)
+        spent, calls = 0.0, 0
+        while spent < min(args.cpu_seconds, 3.0):
+            a = time.perf_counter()
+            po, pl = zip(*[oracle.decode_partial(q, kv, bt, lens, r, P, case.sm_scale, 0)
+                           for r in range(P)])
+            oracle.lse_combine(np.stack(po), np.stack(pl), oracle.LSE_NATURAL)
+            spent += time.perf_counter() - a
+            calls += 1
+        line["cpu_baseline"] = {"value": calls * B / spent, "unit": "tokens/s",
+                                "cores": _oracle_threads(), "kind": "oracle",
+                                "sample": f"{calls} steps of the whole case (both partitions "
+                                          f"and the combine, fp64 numpy), {spent:.1f} s"}
+    return line
 
 
 def main(argv=None):
@@ -922,11 +1136,16 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["decode", "dcp8", "fp8", "kv_append", "combine", "dcp", "mtp"],
+    ap.add_argument("--op", choices=["decode", "small", "dcp8", "fp8", "kv_append", "combine",
+                                     "dcp", "mtp"],
                     default="decode",
-                    help="decode (the headline), dcp8 (the 8-partition DCP workload in one "
-                         "mla_decode_dcp call), fp8 (the e4m3-cache workload), or the KV "
-                         "append of one row per request")
+                    help="decode (the headline; at one GPU its line also carries the small, "
+                         "dcp8, fp8 and combine records under \"configs\"), small (B=1, H=16, "
+                         "L=300, P=2), dcp8 (the 8-partition DCP workload in one "
+                         "mla_decode_dcp call), fp8 (the e4m3-cache workload), combine, dcp "
+                         "--parts P, mtp --q-len T, or the KV append of one row per request")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="decode: the headline record alone, without the other workloads")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--parts", type=int, default=3, help="partitions for --op dcp")
     ap.add_argument("--q-len", type=int, default=2, help="query tokens per request for --op mtp")
@@ -955,6 +1174,12 @@ def main(argv=None):
                               "the oracle of these workloads is the decode op's reference arm"}))
             return
         (run_dcp_parts if args.op == "dcp" else run_mtp)(args, world, rank, local)
+    elif args.op == "small":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the small case's CPU oracle is reported as cpu_baseline of --op small"}))
+            return
+        _print_line(measure_small)(args, world, rank, local)
     elif args.op == "combine":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":
