@@ -898,8 +898,9 @@ def run_dcp_parts(args, world, rank, local):
                                  sample_clocks=True)
     assert mla.check_workspace(ws) == 0
     g = math.gcd(P, 8)
-    one_launch = P <= 8
-    path = ("one launch for all partitions" if 8 % P == 0 else
+    one_launch = 1 < P <= 8
+    path = ("mla_decode_partial's kernels on the one partition, then the combine (a copy)"
+            if P == 1 else "one launch for all partitions" if 8 % P == 0 else
             "one launch for all partitions, strided gather (rows y0 + kP of each page)"
             if one_launch else
             "one launch per partition, owner mask over the gather of partition r mod %d" % g
@@ -915,7 +916,7 @@ def run_dcp_parts(args, world, rank, local):
                                "does not divide 8)"),
                  {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                   "d2h_bytes_per_step": 0, "note": "device-only: see the decode op's e2e"},
-                 (2 if one_launch else 2 * P + 1) * args.steps, clock_info)
+                 (2 if one_launch else 2 * P + 1) * args.steps, clock_info)  # + split merges, combine
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

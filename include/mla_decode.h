@@ -173,10 +173,11 @@ int mla_decode_partial(const void *q, const void *kv_pages, const int32_t *block
  *  workspace    >= mla_decode_dcp_workspace_size(d, num_parts, 0) bytes, same
  *               rules as for mla_decode_partial.
  *
- * num_parts <= 8: one decode launch covers every (partition, request) pair,
- * then one kernel merges the requests the decode's schedule split across SMs
- * and combines the partitions (two kernels).  Other num_parts (up to 256):
- * one decode call per partition, then the combine.  Errors and bounds reporting as for mla_decode_partial.
+ * 2 <= num_parts <= 8: one decode launch covers every (partition, request)
+ * pair, then one kernel merges the requests the decode's schedule split
+ * across SMs and combines the partitions (two kernels).  num_parts = 1 and
+ * num_parts > 8 (up to 256): one mla_decode_partial call per partition, then
+ * the combine (for one partition a copy of its result).  Errors and bounds reporting as for mla_decode_partial.
  */
 size_t mla_decode_dcp_workspace_size(const mla_decode_desc *d, int num_parts, int num_sms);
 

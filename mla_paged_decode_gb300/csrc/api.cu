@@ -474,9 +474,11 @@ int mla_decode_dcp(const void *q, const void *kv_pages, const int32_t *block_tab
     return MLA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t rows = size_t(d->batch) * rows_of(d);
-  if (fused_path(d, num_parts)) {
+  if (num_parts > 1 && fused_path(d, num_parts)) {
     // every partition in one decode launch, then one kernel that merges the
-    // splits and combines the partitions
+    // splits and combines the partitions (one partition takes the loop below:
+    // the single-partition kernel, whose tiles are one page each, and the
+    // combine, then a copy)
     return enqueue_decode(q, kv_pages, block_table, seq_lens, 0, num_parts, true, sm_scale,
                           lse_base, partials, partial_lses, d, workspace, f.sms, s, out,
                           out_lse);

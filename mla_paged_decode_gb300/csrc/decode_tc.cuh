@@ -1044,6 +1044,14 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     tma_prefetch_desc(&tm_kv);
     if (KBG != kKb) tma_prefetch_desc(&tm_kvg);
   }
+  // While the previous kernel finishes, pull the lengths and the head of the
+  // block table into L2 (the KV stream of a previous call evicted them): a
+  // hint that reads nothing back, so it may precede the wait below.
+  if (warp == 2) {
+    if (lane < min(32, (p.req_batch * 4 + 127) / 128))
+      prefetch_l2(reinterpret_cast<const char *>(p.seq_lens) + 128 * lane);
+    if (lane == 31) prefetch_l2(p.block_table);
+  }
   fence_proxy_async_smem();
   // Launched as a programmatic dependent of the stream's previous kernel, so
   // that this prologue overlaps its tail: everything above touches only this

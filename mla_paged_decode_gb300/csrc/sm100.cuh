@@ -81,6 +81,12 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
 
 // ------------------------------------------------------------------ L2 policy
 
+// Brings the line holding `p` into L2 (a hint: nothing is read back, so it
+// may be issued before the data is final).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 // A 16-byte global store whose line L2 keeps ahead of normal-priority data
 // (evict_last): for small results that a later kernel reads back while a
 // large stream passes through L2 in between.

@@ -90,14 +90,11 @@ __device__ __forceinline__ void store_row(__nv_bfloat16 *row, const uint32_t (&p
   dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
 }
 
-// the split record of v is only current for a request with tiles (an empty
-// one keeps whatever an earlier call left); split k > 0 lives in slot
-// 2 (first + k): never past the 2 x grid slots
-__device__ __forceinline__ bool is_split(const DecodeParams &p, int v, int4 info, int grid) {
-  const int tiles = p.strided       ? request_tiles<2>(p, v)
-                    : multi_rows(p) ? request_tiles<1>(p, v)
-                                    : request_tiles<0>(p, v);
-  return tiles > 0 && info.y > 1 && info.x >= 0 && info.x + info.y <= grid;
+// The decode rewrote every record this call (requests with no owned token
+// get {-1, 0, 0}); split k > 0 lives in slot 2 (first + k): never past the
+// 2 x grid slots.
+__device__ __forceinline__ bool is_split(int4 info, int grid) {
+  return info.y > 1 && info.x >= 0 && info.x + info.y <= grid;
 }
 
 __global__ void __launch_bounds__(kMergeWarps * 32, 7) split_merge_kernel(DecodeParams p, int grid) {
@@ -111,7 +108,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 7) split_merge_kernel(Decode
   const int group_heads = min(p.heads_per_group, p.heads - g * p.heads_per_group);
   if (hl >= group_heads) return;
   const int4 info = info_ptr(p)[v];
-  if (!is_split(p, v, info, grid)) return;
+  if (!is_split(info, grid)) return;
   uint32_t pk[8];
   float lse2;
   merge_split_row(p, info, hl, pk, &lse2);
@@ -145,7 +142,7 @@ __global__ void __launch_bounds__(kDcpMaxParts * 32) dcp_merge_combine_kernel(De
     uint32_t pk[8];
     float l;  // the partition's lse as returned (in the output base)
     const int4 info = info_ptr(p)[v];
-    if (is_split(p, v, info, grid)) {
+    if (is_split(info, grid)) {
       float lse2;
       merge_split_row(p, info, hl, pk, &lse2);
       store_row(p.out + prow * kDv, pk);

@@ -39,8 +39,10 @@ __device__ __forceinline__ float lse_out(const DecodeParams &p, float lse2) {
   return p.lse_base2 ? lse2 : lse2 * kLn2;
 }
 
-// The neutral pair (0, -inf) for every virtual request with no owned token.
-// Virtual request v is handled by CTA v mod gridDim.x.  Block-wide.
+// The neutral pair (0, -inf) for every virtual request with no owned token,
+// and its split record {-1, 0, 0} (no splits), so that every record is
+// rewritten by each call and the merge reads no lengths.  Virtual request v
+// is handled by CTA v mod gridDim.x.  Block-wide.
 template <int MULTI = 0>
 __device__ inline void write_empty_requests(const DecodeParams &p) {
   const int V = p.batch * p.head_groups;
@@ -48,6 +50,7 @@ __device__ inline void write_empty_requests(const DecodeParams &p) {
   for (int v = blockIdx.x; v < V; v += gridDim.x) {
     int b = vreq_row(p, v), g = vreq_group(p, v);  // b: output row
     if (request_len<MULTI>(p, v, threadIdx.x == 0 ? err : nullptr) != 0) continue;
+    if (threadIdx.x == 0) info_ptr(p)[v] = make_int4(-1, 0, 0, 0);
     int h0 = g * p.heads_per_group;
     int hn = min(p.heads_per_group, p.heads - h0);
     uint4 *dst = reinterpret_cast<uint4 *>(p.out + (size_t(b) * p.heads + h0) * kDv);
@@ -59,7 +62,8 @@ __device__ inline void write_empty_requests(const DecodeParams &p) {
 
 // Called (by one thread) in each CTA that worked on request v: the CTA that
 // holds the request's first tile records where its splits are, for the merge
-// kernel.  Every request with owned tokens gets a fresh record each call.
+// kernel.  Every request with owned tokens gets a fresh record each call
+// (and every other one the empty record of write_empty_requests).
 __device__ __forceinline__ void record_split(const DecodeParams &p, int v, const SplitInfo &si) {
   if (int(blockIdx.x) == si.c_first) info_ptr(p)[v] = make_int4(si.c_first, si.nsplits, si.slot, 0);
 }
