@@ -691,7 +691,9 @@ def measure_dcp8(args, world, rank, mla, dev, stream):
     """--op dcp8: the decode-context-parallel workload (B=64, H=16, P=8; 60
     requests of 131072 tokens and four of 1, 3, 5, 7) as one mla_decode_dcp
     call per step: every partition's (out, lse) and their combine."""
-    case = workloads.config_dcp8(device=dev, seed=args.seed)
+    case = workloads.config_dcp8(device=dev, seed=args.seed, n_long=args.n_long)
+    if args.n_long != 60:
+        case.name += f"_long{args.n_long}"
     B, H, P = case.batch, case.heads, case.num_parts
     kv_bytes = int(case.seq_lens.sum().item()) * ROW_BYTES[case.kv_dtype]
     ws = mla.make_dcp_workspace(case.q, case.kv_pages, case.block_table, P)
@@ -975,7 +977,7 @@ def measure_combine(args, world, rank, mla, dev, stream):
     memory and its result read back, every step."""
     P, H, D = 8, 16, 512
     points = []
-    for T in (1, 8, 16, 32, 64, 128):
+    for T in args.tokens:
         c = workloads.combine_case(T, num_parts=P, heads=H, dim=D, seed=args.seed, device=dev)
         out = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
         out_lse = torch.empty(T, H, dtype=torch.float32, device=dev)
@@ -1157,6 +1159,11 @@ def main(argv=None):
                          "128 for fp8; smaller only for profiling)")
     ap.add_argument("--pool-pages", type=int, default=40000,
                     help="cache pool size in pages (40000 = the headline workload)")
+    ap.add_argument("--n-long", type=int, default=60,
+                    help="dcp8: requests of 131072 tokens (60 = the workload; fewer only for profiling)")
+    ap.add_argument("--tokens", type=lambda s: [int(x) for x in s.split(",")],
+                    default=[1, 8, 16, 32, 64, 128],
+                    help="combine: token counts (the last one is the line's value)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
