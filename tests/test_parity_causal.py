@@ -122,3 +122,25 @@ def test_two_query_tokens_on_the_32k_batch_every_request():
         ro, rl = oracle.decode_partial_causal(q, kv, bt, sl, 0, 1, case.sm_scale, 0)
         assert_out_close(out[sel], ro, what=f"requests {sel[0]}..{sel[-1]}")
         assert_lse_close(lse[sel], rl, 0, what=f"requests {sel[0]}..{sel[-1]}")
+
+
+def test_sixteen_query_tokens_at_128_heads():
+    """The widest request: 16 query tokens x 128 heads = 2048 rows, 32 head
+    groups walking the same pages side by side (and a request shorter than
+    16 tokens, whose first rows see nothing)."""
+    lens = [3000, 9, 700]
+    case = workloads.make_decode_case("mtp16", 128, lens, seed=16, device="cuda", q_len=16,
+                                      tail_poison=True,
+                                      pool_pages=sum((L + 63) // 64 for L in lens) + 3)
+    q, kv, bt, sl = case_bits(case)
+    B = case.batch
+    out = torch.full((B, 16, 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, 16, 128), float("nan"), dtype=torch.float32, device="cuda")
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table)
+    mla.decode_partial(case.q, case.kv_pages, case.block_table, case.seq_lens, 0, 1,
+                       case.sm_scale, 1, out, lse, workspace=ws)
+    assert mla.check_workspace(ws) == 0
+    ro, rl = oracle.decode_partial_causal(q, kv, bt, sl, 0, 1, case.sm_scale, 1)
+    assert_out_close(out, ro, what="16 tokens x 128 heads")
+    assert_lse_close(lse, rl, 1, what="16 tokens x 128 heads")
+    _neutral_rows(out, lse, lens, 16, 1, 0)

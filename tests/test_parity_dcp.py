@@ -41,6 +41,9 @@ CASES = [
     (64, [700, 2, 1500], 7, "e4m3"),
     (64, [1500, 33, 640, 0], 4, "e4m3"),
     (16, [1, 2, 3, 900, 2049], 8, "e4m3"),
+    (128, [3000, 1, 700, 64], 8, "bf16"),     # two head groups of every partition, one launch
+    (128, [1100, 2, 90], 3, "e4m3"),          # the same through the strided gather
+    (96, [5000, 129], 1, "bf16"),             # one partition through mla_decode_dcp
 ]
 
 
