@@ -323,6 +323,105 @@ def graph_time(call, dev, stream, steps: int) -> float:
     return e0.elapsed_time(e1) * steps / (replays * GRAPH_CALLS)
 
 
+def e2e_times(op, host_in, outputs, args, world, dev, stream):
+    """End-to-end timing of a call through the public API with host buffers.
+
+    host_in: the step's inputs as pinned host tensors; outputs: device
+    tensors shaped like the step's results; op(inp, out) enqueues the call on
+    `stream` with device inputs `inp` and outputs `out` (dicts by the same
+    names).  Every step copies its inputs in from pinned host memory and reads
+    its results back.  Timed twice: serially on one stream, and as a serving
+    loop runs it (device inputs and outputs double-buffered, step i's inputs
+    copied in on one copy stream while step i - 1 computes, its results read
+    back on another while step i + 1 computes; the last read-back is inside
+    the region).  Returns (pipelined ms, serial ms, H2D bytes, D2H bytes) per
+    `args.steps` steps; the results of both loops must agree bit for bit."""
+    def dev_like(t):
+        return torch.empty(t.shape, dtype=t.dtype, device=dev)
+
+    def host_like(t):
+        return torch.empty(t.shape, dtype=t.dtype).pin_memory()
+
+    d_in = {k: dev_like(v) for k, v in host_in.items()}
+    d_out = {k: dev_like(v) for k, v in outputs.items()}
+    h_out = {k: host_like(v) for k, v in outputs.items()}
+
+    def serial_step():
+        for k, v in host_in.items():
+            d_in[k].copy_(v, non_blocking=True)
+        op(d_in, d_out)
+        for k, v in h_out.items():
+            v.copy_(d_out[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        serial_ms, _ = timed_steps(serial_step, args.steps, max(3, args.warmup), world, dev, stream)
+
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    bufs = [dict(inp={k: dev_like(v) for k, v in host_in.items()},
+                 out={k: dev_like(v) for k, v in outputs.items()},
+                 host={k: host_like(v) for k, v in outputs.items()},
+                 ev_in=torch.cuda.Event(), ev_done=torch.cuda.Event(), ev_out=torch.cuda.Event())
+            for _ in range(2)]
+    for bb in bufs:  # so that the first waits on them are satisfied
+        bb["ev_done"].record(stream)
+        bb["ev_out"].record(stream)
+    it = [0]
+
+    def pipelined_step():
+        bb = bufs[it[0] % 2]
+        it[0] += 1
+        h2d_s.wait_event(bb["ev_done"])        # the call that last read these inputs
+        with torch.cuda.stream(h2d_s):
+            for k, v in host_in.items():
+                bb["inp"][k].copy_(v, non_blocking=True)
+        bb["ev_in"].record(h2d_s)
+        stream.wait_event(bb["ev_in"])
+        stream.wait_event(bb["ev_out"])         # the read-back of this buffer's last results
+        op(bb["inp"], bb["out"])
+        bb["ev_done"].record(stream)
+        d2h_s.wait_event(bb["ev_done"])
+        with torch.cuda.stream(d2h_s):
+            for k, v in bb["host"].items():
+                v.copy_(bb["out"][k], non_blocking=True)
+        bb["ev_out"].record(d2h_s)
+
+    def drain():  # the last results are read back inside the timed region
+        for bb in bufs:
+            stream.wait_event(bb["ev_out"])
+
+    pipe_ms, _ = timed_steps(pipelined_step, args.steps, max(3, args.warmup), world, dev, stream,
+                             side_streams=(h2d_s, d2h_s), tail=drain)
+    torch.cuda.synchronize(dev)
+    for bb in bufs:
+        for k, v in h_out.items():
+            a, b = bb["host"][k], v
+            if a.dtype == torch.bfloat16:
+                a, b = a.view(torch.int16), b.view(torch.int16)
+            assert torch.equal(a, b), k
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in outputs.values())
+    return pipe_ms, serial_ms, h2d, d2h
+
+
+E2E_NOTE = ("inputs copied from pinned host memory and results read back every step; the KV "
+            "cache stays resident in HBM. pipelined_value: copies double-buffered on two copy "
+            "streams, overlapping the neighbouring steps' computation (a serving loop); "
+            "serial_value: every copy and the call in sequence on one stream; value: the "
+            "faster of the two (mode)")
+
+
+def e2e_record(units_per_step, args, world, pipe_ms, serial_ms, h2d, d2h, unit, what):
+    """The e2e key: the faster of the pipelined and serial loops as `value`
+    (a latency-bound step gains nothing from the copy streams and pays their
+    bookkeeping), both reported."""
+    pipe = aggregate(pipe_ms, args.steps, units_per_step, world)
+    serial = aggregate(serial_ms, args.steps, units_per_step, world)
+    return {"value": max(pipe, serial), "unit": unit,
+            "mode": "pipelined" if pipe >= serial else "serial",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelined_value": pipe, "serial_value": serial, "note": what + ": " + E2E_NOTE}
+
+
 def cpu_baseline(case, seconds: float):
     """The fp64 oracle, as it stands, on whole requests of the same workload
     until ``seconds`` of CPU time have passed."""
@@ -412,74 +511,14 @@ def measure_decode(args, world, rank, mla, dev, stream):
     assert mla.check_workspace(ws) == 0
 
     # end to end through the C ABI with host buffers: pinned H2D inputs, D2H results
-    q_h = case.q.cpu().pin_memory()
-    bt_h = case.block_table.cpu().pin_memory()
-    sl_h = case.seq_lens.cpu().pin_memory()
-    q_d, bt_d, sl_d = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    def e2e_op(inp, o):
+        mla.decode_partial(inp["q"], case.kv_pages, inp["bt"], inp["sl"], 0, 1, case.sm_scale, 0,
+                           o["out"], o["lse"], workspace=ws, stream=stream)
 
-    def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        mla.decode_partial(q_d, case.kv_pages, bt_d, sl_d, 0, 1, case.sm_scale, 0, out, lse,
-                           workspace=ws, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        e_serial_ms, _ = timed_steps(e2e_step, args.steps, max(3, args.warmup), world, dev,
-                                     stream)
-    assert torch.isfinite(out_h.float()).all()
-
-    # The same steps as a serving loop runs them: double-buffered device inputs
-    # and outputs, step i's inputs copied in on one copy stream while step
-    # i - 1 decodes, its result read back on another while step i + 1 decodes.
-    # Every step still copies its own inputs in and reads its own result back.
-    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    bufs = [dict(q=torch.empty_like(case.q), bt=torch.empty_like(case.block_table),
-                 sl=torch.empty_like(case.seq_lens), out=torch.empty_like(out),
-                 lse=torch.empty_like(lse),
-                 out_h=torch.empty(out.shape, dtype=out.dtype).pin_memory(),
-                 lse_h=torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
-                 ev_in=torch.cuda.Event(), ev_done=torch.cuda.Event(), ev_out=torch.cuda.Event())
-            for _ in range(2)]
-    for bb in bufs:  # so that the first waits on them are satisfied
-        bb["ev_done"].record(stream)
-        bb["ev_out"].record(stream)
-    it = [0]
-
-    def e2e_pipelined_step():
-        bb = bufs[it[0] % 2]
-        it[0] += 1
-        h2d_s.wait_event(bb["ev_done"])        # the decode that last read these inputs
-        with torch.cuda.stream(h2d_s):
-            bb["q"].copy_(q_h, non_blocking=True)
-            bb["bt"].copy_(bt_h, non_blocking=True)
-            bb["sl"].copy_(sl_h, non_blocking=True)
-        bb["ev_in"].record(h2d_s)
-        stream.wait_event(bb["ev_in"])
-        stream.wait_event(bb["ev_out"])         # the read-back of this buffer's last result
-        mla.decode_partial(bb["q"], case.kv_pages, bb["bt"], bb["sl"], 0, 1, case.sm_scale, 0,
-                           bb["out"], bb["lse"], workspace=ws, stream=stream)
-        bb["ev_done"].record(stream)
-        d2h_s.wait_event(bb["ev_done"])
-        with torch.cuda.stream(d2h_s):
-            bb["out_h"].copy_(bb["out"], non_blocking=True)
-            bb["lse_h"].copy_(bb["lse"], non_blocking=True)
-        bb["ev_out"].record(d2h_s)
-
-    def drain():  # the last results are read back inside the timed region
-        for bb in bufs:
-            stream.wait_event(bb["ev_out"])
-
-    e_ms_max, _ = timed_steps(e2e_pipelined_step, args.steps, max(3, args.warmup), world, dev,
-                              stream, side_streams=(h2d_s, d2h_s), tail=drain)
-    for bb in bufs:
-        assert torch.equal(bb["out_h"].view(torch.int16), out_h.view(torch.int16))
+    e_ms_max, e_serial_ms, h2d, d2h = e2e_times(
+        e2e_op, {"q": case.q.cpu().pin_memory(), "bt": case.block_table.cpu().pin_memory(),
+                 "sl": case.seq_lens.cpu().pin_memory()}, {"out": out, "lse": lse},
+        args, world, dev, stream)
 
     value = aggregate(ms_max, args.steps, B, world)
     avg_launch_s = ms_max / 1e3 / args.steps
@@ -513,14 +552,8 @@ def measure_decode(args, world, rank, mla, dev, stream):
                      # score MMA to 64 rows is not counted
                      "tensor_tflops": tflops, "tensor_peak_tflops": tpeak,
                      "tensor_frac": tflops / tpeak, "tensor_peak_source": tpeak_kind},
-        "e2e": {"value": aggregate(e_ms_max, args.steps, B, world), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "serial_value": aggregate(e_serial_ms, args.steps, B, world),
-                "note": "q, block table and lengths copied from pinned host memory, out and "
-                        "lse read back, every step; the KV cache stays resident in HBM. value: "
-                        "copies double-buffered on two copy streams, overlapping the "
-                        "neighbouring steps' decode (a serving loop); serial_value: every "
-                        "copy and the decode in sequence on one stream"},
+        "e2e": e2e_record(B, args, world, e_ms_max, e_serial_ms, h2d, d2h, "tokens/s",
+                          "q, block table and lengths in, out and lse back"),
         "graph": {"value": aggregate(graph_ms_max, args.steps, B, world), "unit": "tokens/s",
                   "ms_per_step": graph_ms_max / args.steps, "calls_per_graph": GRAPH_CALLS,
                   "note": "the same calls replayed from CUDA graphs (not the headline)"},
@@ -709,21 +742,15 @@ def measure_dcp8(args, world, rank, mla, dev, stream):
     ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
                                  sample_clocks=True)
     assert mla.check_workspace(ws) == 0
-    q_h, bt_h, sl_h = (case.q.cpu().pin_memory(), case.block_table.cpu().pin_memory(),
-                       case.seq_lens.cpu().pin_memory())
-    q_d, bt_d, sl_d = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+    def e2e_op(inp, o):
+        mla.decode_dcp(inp["q"], case.kv_pages, inp["bt"], inp["sl"], P, case.sm_scale, 1,
+                       partials=parts, partial_lses=plse, out=o["out"], out_lse=o["lse"],
+                       workspace=ws, stream=stream)
 
-    def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        step(q_d, bt_d, sl_d)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(out_lse, non_blocking=True)
-
-    e_ms, _ = timed_steps(e2e_step, args.steps, 3, world, dev, stream)
+    e_ms, e_serial_ms, h2d, d2h = e2e_times(
+        e2e_op, {"q": case.q.cpu().pin_memory(), "bt": case.block_table.cpu().pin_memory(),
+                 "sl": case.seq_lens.cpu().pin_memory()}, {"out": out, "lse": out_lse},
+        args, world, dev, stream)
     per_s = ms / 1e3 / args.steps
     peak, peak_kind = measured_peaks()
     tpeak, tpeak_kind = measured_bf16_tflops()
@@ -748,9 +775,8 @@ def measure_dcp8(args, world, rank, mla, dev, stream):
                                "per call",
                      "tensor_tflops": flops / per_s / 1e12, "tensor_peak_tflops": tpeak,
                      "tensor_frac": flops / per_s / 1e12 / tpeak, "tensor_peak_source": tpeak_kind},
-        "e2e": {"value": aggregate(e_ms, args.steps, B, world), "unit": "tokens/s",
-                "h2d_bytes_per_step": q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4,
-                "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4},
+        "e2e": e2e_record(B, args, world, e_ms, e_serial_ms, h2d, d2h, "tokens/s",
+                          "q, block table and lengths in, the result and its lse back"),
         "gpu_launches": 2 * args.steps,
         "clocks": clock_info,
     }
@@ -800,21 +826,14 @@ def measure_fp8(args, world, rank, mla, dev, stream):
     ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
                                  sample_clocks=True)
     assert mla.check_workspace(ws) == 0
-    q_h, bt_h, sl_h = (case.q.cpu().pin_memory(), case.block_table.cpu().pin_memory(),
-                       case.seq_lens.cpu().pin_memory())
-    q_d, bt_d, sl_d = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    def e2e_op(inp, o):
+        mla.decode_partial(inp["q"], case.kv_pages, inp["bt"], inp["sl"], 0, 1, case.sm_scale, 0,
+                           o["out"], o["lse"], kv_scale=case.kv_scale, workspace=ws, stream=stream)
 
-    def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        step(q_d, bt_d, sl_d)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-
-    e_ms, _ = timed_steps(e2e_step, args.steps, 3, world, dev, stream)
+    e_ms, e_serial_ms, h2d, d2h = e2e_times(
+        e2e_op, {"q": case.q.cpu().pin_memory(), "bt": case.block_table.cpu().pin_memory(),
+                 "sl": case.seq_lens.cpu().pin_memory()}, {"out": out, "lse": lse},
+        args, world, dev, stream)
     per_s = ms / 1e3 / args.steps
     peak, peak_kind = measured_peaks()
     tpeak, tpeak_kind = measured_bf16_tflops()
@@ -842,9 +861,8 @@ def measure_fp8(args, world, rank, mla, dev, stream):
                                "heads' flops, QK^T over 576 dims and PV over 512)",
                      "hbm_achieved_gbs": kv_bytes / per_s / 1e9, "hbm_peak_gbs": peak,
                      "hbm_frac": kv_bytes / per_s / 1e9 / peak, "hbm_peak_source": peak_kind},
-        "e2e": {"value": aggregate(e_ms, args.steps, B, world), "unit": "tokens/s",
-                "h2d_bytes_per_step": q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4,
-                "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4},
+        "e2e": e2e_record(B, args, world, e_ms, e_serial_ms, h2d, d2h, "tokens/s",
+                          "q, block table and lengths in, the result and its lse back"),
         "gpu_launches": 2 * args.steps,
         "clocks": clock_info,
     }
@@ -994,27 +1012,20 @@ def measure_combine(args, world, rank, mla, dev, stream):
         nbytes = c.partials.numel() * 2 + c.lses.numel() * 4 + out.numel() * 2 + out_lse.numel() * 4
         points.append({"tokens": T, "us_per_call": us, "gbs": nbytes / us / 1e3,
                        "bytes_per_call": nbytes})
-    # end to end at T = 128 through the C ABI with host buffers
-    parts_h, lses_h = c.partials.cpu().pin_memory(), c.lses.cpu().pin_memory()
-    parts_d, lses_d = torch.empty_like(c.partials), torch.empty_like(c.lses)
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    olse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+    # the clock record: the same call eagerly, sampled around its region
+    _, clock_info = timed_steps(lambda: call(stream), args.steps, args.warmup, world, dev, stream,
+                                sample_clocks=True)
 
-    def e2e_step():
-        parts_d.copy_(parts_h, non_blocking=True)
-        lses_d.copy_(lses_h, non_blocking=True)
-        mla.lse_combine(parts_d, lses_d, P, out, lse_base=mla.LSE_NATURAL, out_lse=out_lse,
-                        stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        olse_h.copy_(out_lse, non_blocking=True)
+    # end to end at the last T through the C ABI with host buffers
+    def e2e_op(inp, o):
+        mla.lse_combine(inp["partials"], inp["lses"], P, o["out"], lse_base=mla.LSE_NATURAL,
+                        out_lse=o["lse"], stream=stream)
 
-    with torch.cuda.stream(stream):
-        e_ms, clock_info = timed_steps(e2e_step, args.steps, args.warmup, world, dev, stream,
-                                       sample_clocks=True)
+    e_ms, e_serial_ms, h2d, d2h = e2e_times(
+        e2e_op, {"partials": c.partials.cpu().pin_memory(), "lses": c.lses.cpu().pin_memory()},
+        {"out": out, "lse": out_lse}, args, world, dev, stream)
     peak, peak_kind = measured_peaks()
     top = points[-1]
-    h2d = parts_h.numel() * 2 + lses_h.numel() * 4
-    d2h = out_h.numel() * 2 + olse_h.numel() * 4
     line = {
         "metric": "MLA LSE combine GB/s (P=8, H=16, D=512) on 1 GB300",
         "value": top["gbs"] * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -1029,11 +1040,9 @@ def measure_combine(args, world, rank, mla, dev, stream):
                      "frac": top["gbs"] / peak, "peak_source": peak_kind,
                      "traffic": recorded_traffic(COMBINE_TRAFFIC_FILE),
                      "kernel": "lse_combine_kernel at T = 128 (latency-bound below)"},
-        "e2e": {"value": top["bytes_per_call"] / (e_ms / args.steps) / 1e6 * world, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "T = 128: partials and lses copied in from pinned host memory and the "
-                        "merged out and lse read back every step, one stream; GB/s counts the "
-                        "combine's own bytes"},
+        "e2e": e2e_record(top["bytes_per_call"] / 1e9, args, world, e_ms, e_serial_ms, h2d, d2h,
+                          "GB/s", "partials and lses in, the merged out and lse back (GB/s "
+                          "counts the combine's own bytes)"),
         "gpu_launches": args.steps * len(points),
         "clocks": clock_info,
     }
@@ -1080,22 +1089,15 @@ def measure_small(args, world, rank, mla, dev, stream):
     ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
                                  sample_clocks=True)
     assert mla.check_workspace(ws) == 0
-    q_h, bt_h, sl_h = (case.q.cpu().pin_memory(), case.block_table.cpu().pin_memory(),
-                       case.seq_lens.cpu().pin_memory())
-    q_d, bt_d, sl_d = torch.empty_like(case.q), torch.empty_like(case.block_table), torch.empty_like(case.seq_lens)
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+    def e2e_op(inp, o):
+        mla.decode_dcp(inp["q"], case.kv_pages, inp["bt"], inp["sl"], P, case.sm_scale, 0,
+                       partials=parts, partial_lses=plse, out=o["out"], out_lse=o["lse"],
+                       workspace=ws, stream=stream)
 
-    def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        step(q_d, bt_d, sl_d)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(out_lse, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        e_ms, _ = timed_steps(e2e_step, args.steps, max(3, args.warmup), world, dev, stream)
+    e_ms, e_serial_ms, h2d, d2h = e2e_times(
+        e2e_op, {"q": case.q.cpu().pin_memory(), "bt": case.block_table.cpu().pin_memory(),
+                 "sl": case.seq_lens.cpu().pin_memory()}, {"out": out, "lse": out_lse},
+        args, world, dev, stream)
     roof = _hbm_roofline(kv_bytes, ms, args.steps,
                          "mla_decode_dcp with P = 2: one decode launch for both partitions and "
                          "one merge-and-combine launch, timed together per call; latency-bound "
@@ -1108,9 +1110,8 @@ def measure_small(args, world, rank, mla, dev, stream):
                   "l2": "no flush: 345.6 KB of KV stays in L2 (a latency measurement)",
                   "parallelism": "DCP partitions emulated on one GPU"},
                  roof,
-                 {"value": aggregate(e_ms, args.steps, B, world), "unit": "tokens/s",
-                  "h2d_bytes_per_step": q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4,
-                  "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4},
+                 e2e_record(B, args, world, e_ms, e_serial_ms, h2d, d2h, "tokens/s",
+                            "q, block table and lengths in, the merged result and its lse back"),
                  2 * args.steps, clock_info)
     line["us_per_step"] = ms * 1e3 / args.steps
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
