@@ -652,18 +652,13 @@ def run_append(args, world, rank, local):
                                  sample_clocks=True)
     assert int(err.item()) == 0
     # end to end: the new rows and positions from pinned host memory, the error word back
-    new_h, pos_h = new.cpu().pin_memory(), pos.cpu().pin_memory()
-    err_h = torch.zeros(1, dtype=torch.int32).pin_memory()
-    new_d, pos_d = torch.empty_like(new), torch.empty_like(pos)
+    def e2e_op(inp, o):
+        mla.kv_append(inp["new"], case.kv_pages, case.block_table, inp["pos"], 0, 1,
+                      error_word=o["err"], stream=stream)
 
-    def e2e_step():
-        new_d.copy_(new_h, non_blocking=True)
-        pos_d.copy_(pos_h, non_blocking=True)
-        mla.kv_append(new_d, case.kv_pages, case.block_table, pos_d, 0, 1, error_word=err,
-                      stream=stream)
-        err_h.copy_(err, non_blocking=True)
-
-    e_ms, _ = timed_steps(e2e_step, args.steps, 3, world, dev, stream)
+    e_ms, e_serial_ms, h2d, d2h = e2e_times(
+        e2e_op, {"new": new.cpu().pin_memory(), "pos": pos.cpu().pin_memory()},
+        {"err": torch.zeros(1, dtype=torch.int32, device=dev)}, args, world, dev, stream)
     per_s = ms / 1e3 / args.steps
     byts = B * (1152 + 1152 + 8)   # new row read, cache row written, position + table entry
     peak, peak_kind = measured_peaks()
@@ -681,8 +676,8 @@ def run_append(args, world, rank, local):
                      "traffic": None,
                      "kernel": "mla_kv_append (one launch per step); far below the HBM roof: "
                                "a launch-latency-bound write of B rows"},
-        "e2e": {"value": aggregate(e_ms, args.steps, B, world), "unit": "rows/s",
-                "h2d_bytes_per_step": B * 1152 + B * 4, "d2h_bytes_per_step": 4},
+        "e2e": e2e_record(B, args, world, e_ms, e_serial_ms, h2d, d2h, "rows/s",
+                          "the new rows and positions in, the error word back"),
         "gpu_launches": args.steps,
         "clocks": clock_info,
     }
@@ -895,10 +890,11 @@ def _hbm_roofline(kv_bytes, ms, steps, kernel):
 def run_dcp_parts(args, world, rank, local):
     """--op dcp --parts P: the 32K-context batch (B=64, H=64, bf16) as P
     round-robin partitions and their merge, one mla_decode_dcp call per step
-    (the tensor-core kernel: one launch for all partitions when P divides 8 or
-    P is 3, 5, 6 or 7 (the strided gather), else one launch per partition with
-    the owner mask when P / gcd(P, 8) <= 16, else the CUDA-core kernel).  KV
-    GB/s counts each cached row once."""
+    (the tensor-core kernel: one launch for all partitions when P > 1 divides 8
+    or P is 3, 5, 6 or 7 (the strided gather), else one launch per partition:
+    P = 1 the single-partition kernel, larger P the owner mask when
+    P / gcd(P, 8) <= 16, else the CUDA-core kernel).  KV GB/s counts each
+    cached row once."""
     mla, dev, stream = gpu_setup(world, rank, local)
     P = args.parts
     case = workloads.config_long32k(device=dev, seed=args.seed, batch=args.batch,
@@ -917,6 +913,17 @@ def run_dcp_parts(args, world, rank, local):
     ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
                                  sample_clocks=True)
     assert mla.check_workspace(ws) == 0
+
+    def e2e_op(inp, o):
+        mla.decode_dcp(inp["q"], case.kv_pages, inp["bt"], inp["sl"], P, case.sm_scale, 0,
+                       partials=parts, partial_lses=plse, out=o["out"], out_lse=o["lse"],
+                       workspace=ws, stream=stream)
+
+    e_ms, e_serial_ms, h2d, d2h = e2e_times(
+        e2e_op, {"q": case.q.cpu().pin_memory(), "bt": case.block_table.cpu().pin_memory(),
+                 "sl": case.seq_lens.cpu().pin_memory()},
+        {"out": out, "lse": torch.empty(B, 1, H, dtype=torch.float32, device=dev)},
+        args, world, dev, stream)
     g = math.gcd(P, 8)
     one_launch = 1 < P <= 8
     path = ("mla_decode_partial's kernels on the one partition, then the combine (a copy)"
@@ -934,9 +941,10 @@ def run_dcp_parts(args, world, rank, local):
                                "mla_decode_dcp: every partition's decode and the merge, timed "
                                "together per call (rows gathered P / gcd(P, 8) times when P > 8 "
                                "does not divide 8)"),
-                 {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                  "d2h_bytes_per_step": 0, "note": "device-only: see the decode op's e2e"},
-                 (2 if one_launch else 2 * P + 1) * args.steps, clock_info)  # + split merges, combine
+                 e2e_record(B, args, world, e_ms, e_serial_ms, h2d, d2h, "tokens/s",
+                            "q, block table and lengths in, the merged result and its lse back"),
+                 # the decode (+ its split merge) per partition launch, then the combine
+                 (2 if one_launch else 2 * P + 1) * args.steps, clock_info)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -966,6 +974,15 @@ def run_mtp(args, world, rank, local):
     ms, clock_info = timed_steps(step, args.steps, args.warmup, world, dev, stream,
                                  sample_clocks=True)
     assert mla.check_workspace(ws) == 0
+
+    def e2e_op(inp, o):
+        mla.decode_partial(inp["q"], case.kv_pages, inp["bt"], inp["sl"], 0, 1, case.sm_scale, 0,
+                           o["out"], o["lse"], workspace=ws, stream=stream)
+
+    e_ms, e_serial_ms, h2d, d2h = e2e_times(
+        e2e_op, {"q": case.q.cpu().pin_memory(), "bt": case.block_table.cpu().pin_memory(),
+                 "sl": case.seq_lens.cpu().pin_memory()}, {"out": out, "lse": lse},
+        args, world, dev, stream)
     groups = -(-T * H // 64)
     line = _line(args, world, ms, B * T, "query tokens/s",
                  {"workload": "long32k_b64_h64_bf16_q%d" % T, "batch": B, "heads": H, "q_len": T,
@@ -976,8 +993,8 @@ def run_mtp(args, world, rank, local):
                                "mla_decode_partial with %d query tokens: decode kernel + split "
                                "merge; bytes = the KV once (%d 64-row groups read it side by "
                                "side)" % (T, groups)),
-                 {"value": None, "unit": "query tokens/s", "h2d_bytes_per_step": 0,
-                  "d2h_bytes_per_step": 0, "note": "device-only: see the decode op's e2e"},
+                 e2e_record(B * T, args, world, e_ms, e_serial_ms, h2d, d2h, "query tokens/s",
+                            "q (all query tokens), block table and lengths in, out and lse back"),
                  2 * args.steps, clock_info)
     if rank == 0:
         print(json.dumps(line), flush=True)

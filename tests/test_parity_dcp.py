@@ -109,3 +109,19 @@ def test_full_size_dcp8_in_one_call():
     assert_out_close(parts[3], alone.float().cpu().numpy().astype(np.float64), what="fused vs alone")
     # fp32 sums split at other boundaries: base-2 lse ~16 agrees to a few 1e-4
     assert torch.allclose(plses[3], alone_lse, atol=2e-3, rtol=0)
+
+
+def test_one_partition_call_equals_the_partial_bit_for_bit():
+    """mla_decode_dcp with one partition runs mla_decode_partial's kernels
+    and a combine of one partial, which returns it unchanged: its partition
+    output and its merged output both equal mla_decode_partial's bits."""
+    case = workloads.make_decode_case("dcp_one", 64, [5000, 33, 1, 0, 2049], seed=41,
+                                      device="cuda", pool_pages=120)
+    B = case.batch
+    out_lse = torch.empty(B, 1, 64, dtype=torch.float32, device="cuda")
+    out, _, parts, plses = mla.decode_dcp(case.q, case.kv_pages, case.block_table, case.seq_lens,
+                                          1, case.sm_scale, 1, out_lse=out_lse)
+    ref_out, ref_lse = run_partial(case, 0, 1)
+    for o, l in ((parts[0], plses[0]), (out, out_lse)):
+        assert torch.equal(o.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(l, ref_lse)
