@@ -7,6 +7,7 @@ CPU fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -111,6 +112,14 @@ def _check(status: int):
         raise MlaError(status, msg)
 
 
+def _on(device):
+    """The device context for a call: nothing to switch when it is current
+    (the switch costs a few microseconds, felt by small decodes)."""
+    if torch.cuda.current_device() == device.index:
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def _stream_ptr(stream, device) -> int:
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return int(s.cuda_stream)
@@ -124,7 +133,23 @@ def _kv_dtype_code(kv_pages: torch.Tensor) -> int:
     raise TypeError(f"kv_pages must be bf16 or e4m3 bytes, got {kv_pages.dtype}")
 
 
+_DESCS: dict = {}
+
+
 def _decode_desc(q, kv_pages, block_table, kv_scale) -> DecodeDesc:
+    """The call's size descriptor, built once per distinct set of shapes (the
+    library only reads it during the call)."""
+    key = (q.shape, kv_pages.shape, kv_pages.dtype, block_table.shape, float(kv_scale))
+    d = _DESCS.get(key)
+    if d is None:
+        d = _make_decode_desc(q, kv_pages, block_table, kv_scale)
+        if len(_DESCS) > 256:
+            _DESCS.clear()
+        _DESCS[key] = d
+    return d
+
+
+def _make_decode_desc(q, kv_pages, block_table, kv_scale) -> DecodeDesc:
     if q.dim() != 4:
         raise ValueError("q must be [B, q_len, H, 576]")
     B, q_len, H, dqk = q.shape
@@ -189,7 +214,7 @@ def decode_partial(q, kv_pages, block_table, seq_lens, part_id: int, num_parts: 
     if workspace is None:
         workspace = make_workspace(q, kv_pages, block_table, kv_scale)
     _need(workspace, "workspace", (torch.uint8,), dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load_library().mla_decode_partial(
             q.data_ptr(), kv_pages.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
             int(part_id), int(num_parts), float(sm_scale), int(lse_base), out.data_ptr(),
@@ -229,7 +254,7 @@ def kv_append(kv_new, kv_pages, block_table, positions, part_id: int = 0, num_pa
                    page_size=kv_pages.shape[1], num_pages=kv_pages.shape[0],
                    max_pages_per_seq=block_table.shape[1], kv_dtype=_kv_dtype_code(kv_pages),
                    kv_scale=float(kv_scale))
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load_library().mla_kv_append(
             kv_new.data_ptr(), kv_pages.data_ptr(), block_table.data_ptr(), positions.data_ptr(),
             int(part_id), int(num_parts), ctypes.byref(d),
@@ -287,7 +312,7 @@ def decode_dcp(q, kv_pages, block_table, seq_lens, num_parts: int, sm_scale: flo
     if workspace is None:
         workspace = make_dcp_workspace(q, kv_pages, block_table, P, kv_scale)
     _need(workspace, "workspace", (torch.uint8,), dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load_library().mla_decode_dcp(
             q.data_ptr(), kv_pages.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), P,
             float(sm_scale), int(lse_base), partials.data_ptr(), partial_lses.data_ptr(),
@@ -327,7 +352,7 @@ def dcp_local_metadata(seq_lens, req_pool_indices, req_to_token, part_id: int, n
     d = DcpMetaDesc(batch=B, num_req_slots=req_to_token.shape[0],
                     req_to_token_width=req_to_token.shape[1], max_pages_per_seq=int(max_pages),
                     extra_tokens=int(extra_tokens), pad_value=int(pad_value), page_size=64)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load_library().mla_dcp_local_metadata(
             seq_lens.data_ptr(), req_pool_indices.data_ptr(), req_to_token.data_ptr(), int(part_id),
             int(num_parts), ctypes.byref(d), global_lens.data_ptr(), local_lens.data_ptr(),
@@ -377,7 +402,7 @@ def lse_combine(partials, lses, num_parts: int, out, *, lse_base: int = LSE_NATU
             raise ValueError("out_lse must be [T,H]")
     d = CombineDesc(num_tokens=T, num_heads=H, head_dim=D, lse_base=int(lse_base),
                     out_lse=out_lse.data_ptr() if out_lse is not None else None)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load_library().mla_lse_combine(partials.data_ptr(), lses.data_ptr(), int(num_parts),
                                             out.data_ptr(), ctypes.byref(d), _stream_ptr(stream, dev))
     _check(st)
@@ -407,7 +432,7 @@ def decode_partial_noalloc(q, kv_pages, block_table, seq_lens, part_id: int, num
     fn.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, vp, vp,
                    ctypes.POINTER(DecodeDesc), vp]
     fn.restype = i32
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = fn(q.data_ptr(), kv_pages.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
                 int(part_id), int(num_parts), float(sm_scale), int(lse_base), out.data_ptr(),
                 lse.data_ptr(), ctypes.byref(d), _stream_ptr(stream, dev))
