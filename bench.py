@@ -1131,6 +1131,15 @@ def measure_small(args, world, rank, mla, dev, stream):
                             "q, block table and lengths in, the merged result and its lse back"),
                  2 * args.steps, clock_info)
     line["us_per_step"] = ms * 1e3 / args.steps
+    # the same calls replayed from CUDA graphs: the device time of a step
+    # whose eager launches are partly bound by the host
+    graph_ms = max_over_ranks(graph_time(lambda st: mla.decode_dcp(
+        case.q, case.kv_pages, case.block_table, case.seq_lens, P, case.sm_scale, 0,
+        partials=parts, partial_lses=plse, out=out, out_lse=out_lse, workspace=ws, stream=st),
+        dev, stream, args.steps), world, dev)
+    line["graph"] = {"value": aggregate(graph_ms, args.steps, B, world), "unit": "tokens/s",
+                     "us_per_step": graph_ms * 1e3 / args.steps, "calls_per_graph": GRAPH_CALLS,
+                     "note": "the same calls replayed from CUDA graphs (device time)"}
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         import oracle
         sys.path.insert(0, os.path.join(ROOT, "tests"))
