@@ -5,13 +5,18 @@
 // One warp per output row (token, head).  The row's P LSEs are reduced with
 // warp shuffles in the base-2 domain, the weights kept in shared memory, and
 // the D values streamed as 16-byte bf16 vectors; a partition whose weight is
-// exactly zero (lse = -inf) is not read.
+// exactly zero (lse = -inf) is not read.  For up to 8 partitions and rows of
+// up to 512 values every load of a lane is issued before the first is used
+// (one memory round trip per row instead of one per partition and chunk);
+// the arithmetic, and so every bit of the result, is the same either way.
 #include "common.cuh"
 
 namespace mla {
 
 constexpr int kCombineWarps = 8;
 constexpr int kCombineMaxParts = 256;
+constexpr int kFastParts = 8;   // partitions whose loads a lane keeps in flight together
+constexpr int kFastChunks = 2;  // 16-byte chunks per lane: rows of up to 512 values
 
 __global__ void __launch_bounds__(kCombineWarps * 32)
 lse_combine_kernel(const __nv_bfloat16 *__restrict__ partials, const float *__restrict__ lses,
@@ -45,7 +50,42 @@ lse_combine_kernel(const __nv_bfloat16 *__restrict__ partials, const float *__re
   __syncwarp();
   const float inv = 1.f / sum;
 
-  for (int c = lane; c < chunks; c += 32) {
+  if (num_parts <= kFastParts && chunks <= kFastChunks * 32) {
+    // this lane's chunks lane + 32 k of every partition with a weight
+    uint4 u[kFastChunks][kFastParts];
+#pragma unroll
+    for (int k = 0; k < kFastChunks; ++k)
+#pragma unroll
+      for (int q = 0; q < kFastParts; ++q)
+        if (lane + 32 * k < chunks && q < num_parts && w[q] != 0.f)
+          u[k][q] = __ldg(reinterpret_cast<const uint4 *>(partials + (size_t(q) * rows + row) * dim) +
+                          lane + 32 * k);
+#pragma unroll
+    for (int k = 0; k < kFastChunks; ++k) {
+      const int c = lane + 32 * k;
+      if (c >= chunks) continue;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < kFastParts; ++q) {
+        if (q >= num_parts) break;
+        const float wq = w[q];
+        if (wq == 0.f) continue;
+        const uint32_t x[4] = {u[k][q].x, u[k][q].y, u[k][q].z, u[k][q].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(wq, __uint_as_float(x[i] << 16), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wq, __uint_as_float(x[i] & 0xffff0000u), acc[2 * i + 1]);
+        }
+      }
+      uint32_t pk[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 t2 = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+        pk[i] = *reinterpret_cast<uint32_t *>(&t2);
+      }
+      dst[c] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  } else for (int c = lane; c < chunks; c += 32) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int q = 0; q < num_parts; ++q) {
       const float wq = w[q];
