@@ -113,19 +113,23 @@ def measured_bf16_tflops():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_digest() -> str:
+def kernel_digest(sources=None) -> str:
+    """Digest of the kernel sources: the named files of csrc/ (those one
+    kernel and its launch are built from), else all of them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_paged_decode_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    names = sorted(sources) if sources else sorted(
+        n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(path=TRAFFIC_FILE):
     """DRAM bytes per launch from a committed ncu summary under profiles/, if
-    it was taken on the current kernel source (else None)."""
+    it was taken on the current sources of that kernel (its `sources` line
+    names them; else None)."""
     if not os.path.exists(path):
         return None
     kv = {}
@@ -133,7 +137,8 @@ def recorded_traffic(path=TRAFFIC_FILE):
         if "=" in line and not line.startswith("#"):
             k, v = line.strip().split("=", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("kernel_digest") != kernel_digest():
+    sources = [s.strip() for s in kv.get("sources", "").split(",") if s.strip()]
+    if kv.get("kernel_digest") != kernel_digest(sources or None):
         return None
     try:
         return int(kv["dram_bytes_per_launch"])
