@@ -152,9 +152,11 @@ bool fused_path(const mla_decode_desc *d, int num_parts) {
 // Q as [B*H rows, 576] bf16, one 64-column swizzled box of min(64, H) rows;
 // partition rows of a bf16 cache as a 5-D view (64 dims, 8 rows of stride P,
 // 9 blocks of 64 dims, groups of 8 rows, partitions), one box = one page's
-// owned rows; of an e4m3 cache as a 3-D view (144 words of 4 fp8 values,
-// rows of stride P, partitions), one unswizzled box = one page's 64/P owned
-// rows of 576 B.  For one partition (`part_id`) the base is offset to its
+// owned rows; of an e4m3 cache as a 3-D view (576 bytes, rows of stride P,
+// partitions), one swizzled box = 128 dims of one page's 64/P owned rows,
+// with an unswizzled view of whole 576-byte rows for the L2 prefetch.  The
+// strided gather's maps take an atom's rows through a traversal stride P.
+// For one partition (`part_id`) the base is offset to its
 // first row and the partition dimension is left off (4-D / 2-D maps, the
 // faster boxes); for all P partitions (`all_parts`) it is added, with a stride
 // of one row (5-D / 3-D maps, coordinate r).
@@ -192,7 +194,16 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 strided", r);
-    *tm_kvg = *tm_kv;
+    // the kernel's loads (the box above serves the L2 prefetch): (576 bytes,
+    // 64 page rows, pages), one swizzled box of 128 dims of an atom's rows c,
+    // c + P, ..., c + 7P
+    cuuint64_t fdims[3] = {row8, cuuint64_t(mla::kPage), cuuint64_t(d->num_pages)};
+    cuuint64_t fstrides[2] = {row8, cuuint64_t(mla::kPage) * row8};
+    cuuint32_t fbox[3] = {128, 8 * P, 1};
+    r = enc(tm_kvg, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(kv), fdims, fstrides, fbox, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 strided blocks", r);
   } else if (d->kv_dtype == MLA_KV_E4M3) {
     const cuuint64_t P = cuuint64_t(num_parts);
     const cuuint32_t R = cuuint32_t(mla::kPage / num_parts);
@@ -207,7 +218,17 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3", r);
-    *tm_kvg = *tm_kv;  // unused: the e4m3 stage lands in one box per page
+    // the kernel's loads (the box above serves the L2 prefetch): (576 bytes,
+    // owned rows, partitions) with a swizzled box of 128 dims of a page's
+    // 64/P owned rows; block 4 (dims 512..639) runs past the row and reads
+    // zeros there
+    cuuint64_t fdims[3] = {row8, cuuint64_t(d->num_pages) * R, P};
+    cuuint64_t fstrides[2] = {P * row8, row8};
+    cuuint32_t fbox[3] = {128, R, 1};
+    r = enc(tm_kvg, CU_TENSOR_MAP_DATA_TYPE_UINT8, all_parts ? 3 : 2, const_cast<char *>(base), fdims,
+            fstrides, fbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 blocks", r);
   } else if (strided) {
     // (64 dims, 64 page rows, 9 blocks of 64 dims, pages): one box is one
     // atom, rows c, c + P, ..., c + 7P of a page (traversal stride P), which

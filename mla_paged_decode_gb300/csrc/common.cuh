@@ -368,6 +368,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   return r;
 }
 
+// Two floats -> two OCP e4m3 bytes, round to nearest even, saturated to the
+// finite range (hardware conversion): `lo` in the low byte.
+__device__ __forceinline__ uint16_t float2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("{ cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2; }" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
   uint32_t h = e4m3x2_to_f16x2(two);
   __half2 hh = *reinterpret_cast<__half2 *>(&h);

@@ -5,7 +5,7 @@
 // online softmax between them.
 //
 // Roles (288 threads):
-//   warp 0          TMA producer: Q of each request (9 boxes of 64 dims) and,
+//   warp 0          TMA producer: Q of each request (bf16: 9 boxes of 64 dims) and,
 //                   per tile, the 64/P rows the partition owns of each page
 //                   (lane k: page k) into a swizzled [column group][atom]
 //                   [dim block][8 rows][128 B] layout that serves both MMAs:
@@ -14,19 +14,24 @@
 //   warp 1          TMEM owner (alloc/free).
 //   warps 1, 2      lane 0 issues half of the score MMAs (one accumulator each).
 //   warps 3, 8      lane 0 issues the PV MMAs of two of the four value chunks.
+//   warps 9..11     (e4m3) Q of each request, split into two e4m3 terms.
 //   warps 4..7      softmax and epilogue.  The S accumulator (M = 64) puts
 //                   head 16q + i in TMEM lane 32q + i (i < 16); read with the
 //                   16x256b shape, each lane of warp q gets 2 heads x 16 of the
 //                   64 tokens.  For the epilogue every thread owns TMEM lane
 //                   32q + lane of O^T: one value dimension.
 //
-// e4m3 caches (the same kernel with F8 = true, 384 threads): the producer
-// lands each owned fp8 row (576 B) in the upper half of its stage, and
-// warps 9..11 expand them in place into the same swizzled layout as f16 (an
-// exact conversion), converting the request's Q to f16 as well with one
-// power-of-two scale that keeps its largest element in [2^14, 2^15); the
-// MMAs then run with f16 operands, P is written as f16, and the scores carry
-// sm_scale * kv_scale / (that power of two).
+// e4m3 caches (the same kernel with F8 = true, 384 threads): the MMAs are
+// kind::f8f6f4 and read the cache's raw rows as landed, in five swizzled
+// blocks of 128 dims (three 40 KB stages).  Warps 9..11 read each request's
+// Q (bf16) and split 2^k Q into two e4m3 terms, hi + lo, that hold it exactly
+// down to 2^-2 of the scaled values (k puts the largest |q| in [2^7, 2^8));
+// the score issuers take one term each (S = Q_hi K^T + Q_lo K^T, 18 K-steps
+// of 32 dims), the scores carry sm_scale * kv_scale * 2^-k, and the softmax
+// writes P, scaled by 2^4 (with the O rescale threshold lowered to 2^4), as
+// two e4m3 terms as well, so that each PV step is two MMAs; the output is
+// normalised by the sum of P as stored, the LSE takes the sum before
+// rounding.  V^T is the raw rows read MN-major.
 //
 // Partitions: P divides 8 here (64/P owned rows per page), or P in
 // {3, 5, 6, 7}: the strided gather (MULTI == 2, DecodeParams::strided), where
@@ -36,11 +41,12 @@
 // softmax (DecodeParams::own_parts), through the several-row variants
 // (MULTI == 1), which carry the per-row bounds and guards that mask needs.
 //
-// Pipeline per tile i (stage / S buffer i mod 2): producer -> kv_full (per
-// column group) -> MMA S_i (36 MMAs, two interleaved accumulators so
-// consecutive MMAs are independent) -> s_full -> softmax reads S_i, frees it (s_free), waits for
-// PV_{i-1} (p_free), rescales O^T only when some head's running max grew by
-// more than 2^8, writes P_i (bf16) -> p_full -> MMA PV_i (4 independent
+// Pipeline per tile i (stage i mod 2, i mod 3 for e4m3; S buffer i mod 2):
+// producer -> kv_full (per column group or block) -> MMA S_i (36 MMAs, two
+// accumulators so consecutive MMAs are independent) -> s_full -> softmax
+// reads S_i, frees it (s_free), waits for PV_{i-1} (p_free) and rescales
+// O^T only when some head's running max grew by more than the threshold
+// (2^8; e4m3: 2^4), writes P_i -> p_full -> MMA PV_i (4 independent
 // value-dim chunks) -> kv_empty + p_free.  The score issuers start S_{i+1} as
 // soon as tile i+1 lands, so the score MMAs of the next tile overlap this
 // tile's softmax, and the producer keeps the pages of the next tile (two
@@ -88,10 +94,38 @@ template <int KBG>
 __host__ __device__ constexpr uint32_t kb_off(int kb) {
   return uint32_t(kb / KBG) * 8u * atom_stride<KBG>() + uint32_t(kb % KBG) * 1024u;
 }
-constexpr int kMaxGroups = 3;
+constexpr int kMaxGroups = 5;
 constexpr int kOffQ = 0;
 constexpr int kOffKv = kOffQ + kQBytes;
 constexpr int kOffMisc = kOffKv + 2 * kStageBytes;
+
+// e4m3 caches, read by fp8 MMAs straight from the raw rows: Q as two e4m3
+// terms, hi and lo, each [5 blocks of 128 dims][64 rows][128 B], swizzled
+// K-major; three stages of the raw rows as landed, [5 blocks][8 atoms][8
+// rows][128 B] (dims 576..639 of block 4 are the copy's zero fill).  Block 4
+// (the rope dims), dead once the scores are computed, then holds P as two
+// e4m3 terms [64 heads][64 tokens] of 4 KB each, unswizzled: 8-head x
+// 16-token core matrices of 128 B.
+constexpr int kFxBlocks = 5;
+constexpr int kFxBlock = 64 * 128;                   // one block of 64 rows
+constexpr int kFxQTerm = kFxBlocks * kFxBlock;       // 40 KB
+constexpr int kFxStageBytes = kFxBlocks * kFxBlock;  // 40 KB
+constexpr uint32_t kFxPLbo = 128, kFxPSbo = 512;     // P core matrices along tokens / heads
+constexpr int kFxPTerm = 4096;                       // P lo after P hi
+// P is stored as 2^(8 - threshold) p (p <= 2^threshold): it stays below the
+// e4m3 maximum (448), and weights down to 2^-13 of the running maximum stay
+// above e4m3's subnormal floor (2^-9).  The sum that normalises the output
+// takes P as stored; the LSE takes the sum of P before rounding.
+constexpr float kFxRescaleThreshold = 4.f;
+constexpr float kFxPLog2Scale = 8.f - kFxRescaleThreshold;
+template <bool F8>
+constexpr int num_stages() { return F8 ? 3 : 2; }
+template <bool F8>
+constexpr int stage_bytes() { return F8 ? kFxStageBytes : kStageBytes; }
+template <bool F8>
+constexpr int off_kv() { return F8 ? 2 * kFxQTerm : kOffKv; }
+template <bool F8>
+constexpr int off_misc() { return off_kv<F8>() + num_stages<F8>() * stage_bytes<F8>(); }
 constexpr int kSmemBytes = 232448;           // per-block maximum on sm_100 parts
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                // O^T chunk c: columns [64c, 64c + npv)
@@ -99,8 +133,6 @@ constexpr uint32_t kColS = 256;              // S(buffer s, chain k): 256 + 64 (
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr float kRescaleThreshold = 8.f;     // base-2 units
-constexpr int kRawOff = kStageBytes / 2;     // e4m3: raw [64 rows][576 B] in the stage's upper half
-constexpr int kRawRow = kDqk;                // bytes of one fp8 row
 }  // namespace tc
 
 struct TcParams {
@@ -113,22 +145,30 @@ struct TcParams {
 template <bool F8>
 constexpr int tc_threads() { return F8 ? tc::kThreadsF8 : tc::kThreads; }
 
+// Barriers and scratch; NS shared-memory stages (the two S buffers in TMEM
+// are separate from them).
+template <int NS>
 struct TcMisc {
-  uint64_t kv_full[2][tc::kMaxGroups], kv_empty[2], q_full, q_empty, s_full[2], s_free[2];
-  uint64_t p_full[2], p_free, o_full, o_free, drain;
-  uint64_t kv_conv[2], q_ready;  // e4m3 only: stage / Q expanded to f16
+  uint64_t kv_full[NS][tc::kMaxGroups], kv_empty[NS], q_full, q_empty, s_full[2], s_free[2];
+  uint64_t p_full[NS], p_free[NS], o_full, o_free, drain;
+  uint64_t q_ready;               // e4m3 only: Q split into its two terms
   uint32_t tmem_base;
   int abort;
   float alpha[2][64];
   float ell[64];
-  float tscale[2];               // e4m3 only: score scale (base 2) of the tile in each stage
+  float qinv[4];                 // e4m3 only: 2^-k of Q's scale, by request piece mod 4
+  int qinv_v[4];                 // e4m3 only: the virtual request each qinv slot holds
   uint32_t vote[2][4];           // softmax: per-warp flags of the tile, by tile parity
   alignas(16) unsigned char stage_out[4][2048];  // epilogue: per-warp transpose buffer
   uint32_t conv_max[4];
   CtaRange range;
   long long scratch[tc::kThreadsF8 / 32 + 1];
 };
-static_assert(sizeof(TcMisc) + 1024 <= tc::kSmemBytes - tc::kOffMisc, "shared memory budget");
+static_assert(sizeof(TcMisc<2>) + 1024 <= tc::kSmemBytes - tc::off_misc<false>(), "shared memory budget");
+static_assert(sizeof(TcMisc<3>) + 1024 <= tc::kSmemBytes - tc::off_misc<true>(), "shared memory budget");
+
+template <bool F8>
+using TcMiscFor = TcMisc<tc::num_stages<F8>()>;
 
 // The requests (and tile ranges) this CTA owns, in order; every role walks it.
 // FUSED: all partitions in one launch (output row b = partition * B + input
@@ -225,24 +265,27 @@ __device__ __forceinline__ bool lane_page(const DecodeParams &p, int part, long 
 // measured best of 0..4).  It is a template parameter because the same choice
 // made at run time costs more than it gains.
 template <bool F8, bool FUSED, int MULTI, int AHEAD>
-__device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
-                            uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
+__device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMiscFor<F8> &m,
+                            uint32_t sQ, uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
                             const CUtensorMap *tm_kvg, int *err) {
   using namespace tc;
   constexpr bool STRIDED = MULTI == 2;
+  constexpr int NS = num_stages<F8>();
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const int lane = threadIdx.x & 31;
   uint32_t kv_it = 0, q_it = 0;
-  int last_q = -1, last_kv[2] = {-1, -1};
-  // bf16: one 4-D box of groups_per_page swizzled atoms per page; e4m3: one
-  // 2-D box of the page's 8 * groups_per_page owned rows, 576 B each
+  int last_q = -1, last_kv[NS];
+#pragma unroll
+  for (int s = 0; s < NS; ++s) last_kv[s] = -1;
+  // bf16: one 4-D box of groups_per_page swizzled atoms per page; e4m3: per
+  // block of 128 dims (one barrier each), one swizzled box of the page's
+  // 8 * groups_per_page owned rows (the strided gather: of one atom's rows)
   const int rows_per_page = 8 * tp.groups_per_page;
-  constexpr int KBG = stage_kbg<F8, AHEAD>(), kG = num_groups<KBG>();
-  // bytes one page lands per barrier: all its fp8 rows, or one column group
-  const uint32_t page_bytes = F8 ? uint32_t(rows_per_page * kRawRow)
+  constexpr int KBG = stage_kbg<F8, AHEAD>(), kG = F8 ? kFxBlocks : num_groups<KBG>();
+  // bytes one page lands per barrier: its rows of one block, or one column group
+  const uint32_t page_bytes = F8 ? uint32_t(tp.groups_per_page) * 1024u
                                  : uint32_t(tp.groups_per_page) * atom_stride<KBG>();
-  const uint32_t dst0 = F8 ? sKv + kRawOff : sKv;
   bool ok = true;
 
   // The whole warp produces: lane k handles page k of a tile (a tile spans P
@@ -287,7 +330,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 
   TileCursor<FUSED, MULTI> cur(p, r);
   while (cur.live) {
-    if (cur.first()) {
+    if (!F8 && cur.first()) {  // (e4m3: warps 9..11 load and split Q)
       checked_len(p, cur.w.rb, err);
       if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(m.q_empty), (q_it & 1) ^ 1, abort, kTimeoutNs))) {
         ok = false;
@@ -301,7 +344,8 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
       last_q = q_it & 1;
       ++q_it;
     }
-    const int s = kv_it & 1;
+    if (F8 && cur.first()) checked_len(p, cur.w.rb, err);
+    const int s = kv_it % NS;
     int lp, row0;
     const bool mine = lane_page<STRIDED>(p, cur.w.part, cur.t, cur.w.n, lane, &lp, &row0);
     int pg = ring[0];
@@ -311,7 +355,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
     }
     const bool load = mine && pg >= 0;
     const uint32_t bytes = uint32_t(__popc(__ballot_sync(0xffffffffu, load))) * page_bytes;
-    if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(m.kv_empty[s]), ((kv_it >> 1) & 1) ^ 1, abort,
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(m.kv_empty[s]), ((kv_it / NS) & 1) ^ 1, abort,
                                            kTimeoutNs))) {
       ok = false;
       break;
@@ -319,15 +363,21 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
     if (lane < kG) mbar_arrive_expect_tx(bar_addr(m.kv_full[s][lane]), bytes);
     __syncwarp();
     if (load) {
-      const uint32_t dst = dst0 + s * kStageBytes + lane * page_bytes;
-      if (F8 && STRIDED) {
-        // one atom: raw rows row0 + iP (traversal stride P) of page pg
-        tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, row0, pg);
-      } else if (F8) {
-        if (FUSED)
-          tma_load_3d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, pg * rows_per_page, cur.w.pc);
-        else
-          tma_load_2d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, pg * rows_per_page);
+      const uint32_t dst = sKv + s * stage_bytes<F8>() + lane * page_bytes;
+      if (F8) {
+        // block g: dims [128 g, 128 g + 128) (block 4 runs past the row: zero
+        // fill) of this lane's rows: its page's owned rows, or one atom of the
+        // strided gather, rows row0 + iP of page pg (traversal stride P)
+#pragma unroll
+        for (int g = 0; g < kFxBlocks; ++g) {
+          const uint32_t dg = dst + uint32_t(g) * kFxBlock;
+          if (STRIDED)
+            tma_load_3d(dg, tm_kvg, bar_addr(m.kv_full[s][g]), 128 * g, row0, pg);
+          else if (FUSED)
+            tma_load_3d(dg, tm_kvg, bar_addr(m.kv_full[s][g]), 128 * g, pg * rows_per_page, cur.w.pc);
+          else
+            tma_load_2d(dg, tm_kvg, bar_addr(m.kv_full[s][g]), 128 * g, pg * rows_per_page);
+        }
       } else if (STRIDED) {
         // one atom: rows row0 + iP (traversal stride P) of page pg, all dims
         tma_load_4d(dst, tm_kv, bar_addr(m.kv_full[s][0]), 0, row0, 0, pg);
@@ -345,7 +395,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
         }
       }
     }
-    last_kv[s] = (kv_it >> 1) & 1;
+    last_kv[s] = (kv_it / NS) & 1;
     ++kv_it;
 #pragma unroll
     for (int i = 0; i + 1 < AHEAD; ++i) ring[i] = ring[i + 1];
@@ -355,7 +405,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   if (!ok && lane == 0) atomicOr(err, kErrTimeout);
   // never leave the CTA with a copy still in flight into its shared memory
   if (last_q >= 0) mbar_wait_drain(bar_addr(m.q_full), last_q, kDrainNs);
-  for (int s = 0; s < 2; ++s)
+  for (int s = 0; s < NS; ++s)
     if (last_kv[s] >= 0)
       for (int g = 0; g < kG; ++g) mbar_wait_drain(bar_addr(m.kv_full[s][g]), last_kv[s], kDrainNs);
 }
@@ -370,15 +420,58 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 // Descriptors: an offset is added to the encoded start address (bits 0..13,
 // address >> 4), which never carries because shared addresses stay below 256 KB.
 template <bool F8, bool FUSED, int MULTI, int KBG>
-__device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sQ,
-                         uint32_t sKv, uint32_t tmem, int chain, int *err) {
+__device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, TcMiscFor<F8> &m,
+                         uint32_t sQ, uint32_t sKv, uint32_t tmem, int chain, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
-  const uint32_t idesc_s = idesc_f32acc(64, 64, false, false, !F8);
-  // e4m3: the stage and Q are ready once the converter has expanded them;
-  // bf16: column group g of the stage once its own box has landed
+  // bf16: Q once landed, column group g of the stage once its own box has
+  // landed; e4m3: Q once split into its two terms, block g once landed
   uint64_t &q_ready = F8 ? m.q_ready : m.q_full;
+  if constexpr (F8) {
+    // chain 0 scores with Q's hi term, chain 1 with its lo term: 18 K-steps
+    // of 32 dims each (blocks 0..3: 4; block 4: 2)
+    constexpr int NS = num_stages<F8>();
+    const uint32_t idesc_s = idesc_e4m3_f32(64, 64, false, false);
+    const uint64_t dq = smem_desc_sw128(sQ + uint32_t(chain) * kFxQTerm, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sKv, 16, 1024);
+    constexpr uint64_t kStageEnc = uint64_t(kFxStageBytes) >> 4;
+    uint32_t s_it = 0, q_it = 0;
+    bool ok = true;
+    for (TileCursor<FUSED, MULTI> sc(p, r); sc.live; sc.step(), ++s_it) {
+      const int st = s_it % NS, sb = s_it & 1;
+      const uint32_t ph = (s_it / NS) & 1;
+      if (sc.first()) {
+        if (!mbar_wait(bar_addr(q_ready), q_it & 1, abort, kTimeoutNs)) { ok = false; break; }
+        ++q_it;
+      }
+      if (!mbar_wait(bar_addr(m.s_free[sb]), ((s_it >> 1) & 1) ^ 1, abort, kTimeoutNs)) {
+        ok = false;
+        break;
+      }
+      const uint64_t dk = dk0 + st * kStageEnc;
+      const uint32_t d = tmem + kColS + 64 * (2 * sb + chain);
+      bool landed = true;
+#pragma unroll
+      for (int kb = 0; kb < kFxBlocks; ++kb) {
+        landed = mbar_wait(bar_addr(m.kv_full[st][kb]), ph, abort, kTimeoutNs);
+        if (!landed) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < (kb < 4 ? 4 : 2); ++ks)
+          mma_f8_ss(d, dq + ((kb * kFxBlock + ks * 32) >> 4), dk + ((kb * kFxBlock + ks * 32) >> 4),
+                    idesc_s, kb > 0 || ks > 0);
+      }
+      if (!landed) { ok = false; break; }
+      mma_commit(bar_addr(m.s_full[sb]));
+      if (sc.last()) mma_commit(bar_addr(m.q_empty));
+    }
+    if (!ok) atomicOr(err, kErrTimeout);
+    mma_commit(bar_addr(m.drain));
+    mbar_wait_drain(bar_addr(m.drain), 0, kDrainNs);
+    return;
+  }
+  const uint32_t idesc_s = idesc_bf16_f32(64, 64, false, false);
   const uint64_t dq = smem_desc_sw128(sQ, 16, 1024);                         // Q, K-major
   const uint64_t dk0 = smem_desc_sw128(sKv + 32 * chain, 16, atom_stride<KBG>());  // K tile, K-major
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
@@ -387,7 +480,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
   for (TileCursor<FUSED, MULTI> sc(p, r); sc.live; sc.step(), ++s_it) {
     const int st = s_it & 1;
     const uint32_t ph = (s_it >> 1) & 1;
-    if (!mbar_wait(bar_addr(F8 ? m.kv_conv[st] : m.kv_full[st][0]), ph, abort, kTimeoutNs)) {
+    if (!mbar_wait(bar_addr(m.kv_full[st][0]), ph, abort, kTimeoutNs)) {
       ok = false;
       break;
     }
@@ -404,7 +497,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
 #pragma unroll
     for (int i = 0; i < kKb * 2; ++i) {
       const int kb = i >> 1;
-      if (!F8 && i > 0 && kb % KBG == 0 && (i & 1) == 0) {
+      if (i > 0 && kb % KBG == 0 && (i & 1) == 0) {
         landed = mbar_wait(bar_addr(m.kv_full[st][kb / KBG]), ph, abort, kTimeoutNs);
         if (!landed) break;
         tc_fence_after();
@@ -425,12 +518,63 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
 // O^T(chunk c) (+)= V^T(tile) P^T over ceil(nv/16) steps of 16 tokens; issuer
 // `half` takes value chunks 2 half and 2 half + 1.
 template <bool F8, bool FUSED, int MULTI, int KBG>
-__device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMisc &m, uint32_t sKv,
-                          uint32_t tmem, int half, int *err) {
+__device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r, TcMiscFor<F8> &m,
+                          uint32_t sKv, uint32_t tmem, int half, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
-  const uint32_t idesc_o = idesc_f32acc(128, tp.npv, true, false, !F8);
+  if constexpr (F8) {
+    // O^T(chunk c) += V^T P_hi^T + V^T P_lo^T over ceil(nv / 32) steps of 32
+    // tokens: V^T of chunk c is block c of the raw rows, MN-major (128 value
+    // dims per swizzled row); P's terms are K-major, unswizzled
+    constexpr int NS = num_stages<F8>();
+    const uint32_t idesc_o = idesc_e4m3_f32(128, tp.npv, true, false);
+    constexpr uint64_t kStageEnc = uint64_t(kFxStageBytes) >> 4;
+    uint64_t dv0[2];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) dv0[cc] = smem_desc_sw128(sKv + (2 * half + cc) * kFxBlock, kFxBlock, 1024);
+    const uint64_t dp0 = smem_desc_noswz(sKv + 4 * kFxBlock, kFxPLbo, kFxPSbo);
+    uint32_t pv_it = 0, o_it = 0;
+    bool ok = true;
+    for (TileCursor<FUSED, MULTI> pc(p, r); pc.live; pc.step(), ++pv_it) {
+      const int st = pv_it % NS;
+      if (!mbar_wait(bar_addr(m.p_full[st]), (pv_it / NS) & 1, abort, kTimeoutNs)) {
+        ok = false;
+        break;
+      }
+      const bool fresh = pc.first();
+      if (fresh && !mbar_wait(bar_addr(m.o_free), (o_it & 1) ^ 1, abort, kTimeoutNs)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t dp = dp0 + st * kStageEnc;
+      const int ksteps = (pc.nv() + 31) >> 5;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        if (ks < ksteps) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const uint32_t dcol = tmem + kColO + 64 * (2 * half + cc);
+            const uint64_t dv = dv0[cc] + st * kStageEnc + ((ks * 4 * 1024) >> 4);
+            mma_f8_ss(dcol, dv, dp + ((ks * 2 * kFxPLbo) >> 4), idesc_o, !(fresh && ks == 0));
+            mma_f8_ss(dcol, dv, dp + ((kFxPTerm + ks * 2 * kFxPLbo) >> 4), idesc_o, 1u);
+          }
+        }
+      }
+      mma_commit(bar_addr(m.kv_empty[st]));
+      mma_commit(bar_addr(m.p_free[st]));
+      if (pc.last()) {
+        mma_commit(bar_addr(m.o_full));
+        ++o_it;
+      }
+    }
+    if (!ok) atomicOr(err, kErrTimeout);
+    mma_commit(bar_addr(m.drain));
+    mbar_wait_drain(bar_addr(m.drain), 0, kDrainNs);
+    return;
+  }
+  const uint32_t idesc_o = idesc_bf16_f32(128, tp.npv, true, false);
   // V^T of value chunk c (dim blocks 2c, 2c + 1), MN-major; P, K-major
   uint64_t dv0[2];
 #pragma unroll
@@ -470,7 +614,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
       }
     }
     mma_commit(bar_addr(m.kv_empty[st]));
-    mma_commit(bar_addr(m.p_free));
+    mma_commit(bar_addr(m.p_free[st]));
     if (pc.last()) {
       mma_commit(bar_addr(m.o_full));
       ++o_it;
@@ -530,6 +674,18 @@ __device__ __forceinline__ float ex2(float x) {
   return r;
 }
 
+// Value rows [nv, roundup32(nv)) of a raw e4m3 stage (512 B of value dims
+// each, blocks 0..3), zeroed by the softmax warpgroup (rank gt).
+static __device__ __noinline__ void zero_value_tail_fx(unsigned char *stage, int nv, int gt) {
+  using namespace tc;
+  const int nrow = ((nv + 31) & ~31) - nv;
+  for (int i = gt; i < nrow * 32; i += 128) {
+    const int rr = nv + (i >> 5), kb = (i >> 3) & 3, ch = i & 7;
+    *reinterpret_cast<uint4 *>(stage + kb * kFxBlock + (rr >> 3) * 1024 + (rr & 7) * 128 + ch * 16) =
+        make_uint4(0, 0, 0, 0);
+  }
+}
+
 // Value rows [nv, roundup16(nv)) of a stage (the last tile of a request),
 // zeroed by the softmax warpgroup (rank gt): out of line, once per request.
 template <int KBG>
@@ -544,10 +700,12 @@ static __device__ __noinline__ void zero_value_tail(unsigned char *stage, int nv
 }
 
 template <bool F8, bool FUSED, int MULTI, int KBG>
-__device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMisc &m,
+__device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r, TcMiscFor<F8> &m,
                            unsigned char *smem, uint32_t tmem, int *err) {
   using namespace tc;
   constexpr bool STRIDED = MULTI == 2;
+  constexpr int NS = num_stages<F8>();
+  constexpr float kThreshold = F8 ? kFxRescaleThreshold : kRescaleThreshold;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const int gt = int(threadIdx.x) - 128;  // rank in the warpgroup
@@ -566,9 +724,23 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
   OwnerMask own{};
   if (masked) own = owner_mask_of(p);
 
+  uint32_t piece = 0;
   Walk<FUSED, MULTI> w(p, r);
-  for (; ok && w.next(); w.advance()) {
+  for (; ok && w.next(); w.advance(), ++piece) {
     const int hn = min(kHeads, p.heads - w.g * kHeads);
+    if (F8) {
+      // Q's scale, written by warps 9..11 before the scores of this piece
+      // were computed (its slot is checked against the request: bounded)
+      const int slot = piece & 3;
+      const volatile int *vv = m.qinv_v;
+      const uint64_t t0 = globaltimer();
+      while (vv[slot] != w.v && globaltimer() - t0 < kTimeoutNs) {
+      }
+      __threadfence_block();
+      const bool have = vv[slot] == w.v;
+      if (!have) atomicOr(err, kErrTimeout);
+      cs = p.score_scale_log2 * p.kv_scale * (have ? m.qinv[slot] : 0.f);
+    }
     // owned tokens each of this lane's two rows sees (all w.n unless a request
     // carries several query tokens, each with its own causal bound)
     int nrow[2] = {w.n, w.n};
@@ -587,18 +759,15 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
     if (STRIDED) smask.start(p, w.part, w.t0);
     float mrun[2] = {-INFINITY, -INFINITY};  // running max (base-2 units) of each head
     float ellp[2] = {0.f, 0.f};              // this lane's share of each head's sum
+    float ellx[2] = {0.f, 0.f};              // e4m3: the same of P before rounding
     for (long long t = w.t0; t < w.t1; ++t, ++kv_it, ++p_it) {
-      const int s = kv_it & 1;
+      const int s = kv_it & 1;          // S buffer
+      const int st = kv_it % NS;        // shared-memory stage
       const uint32_t ph = (kv_it >> 1) & 1;
       const int nv = min(kTile, w.n - int(t) * kTile);
       // Every wait of the warpgroup is followed by a group vote, so that a
       // wait that gave up in one warp never strands the others at a barrier.
       bool got = __all_sync(0xffffffffu, mbar_wait(bar_addr(m.s_full[s]), ph, abort, kTimeoutNs));
-      if (F8 && got) {
-        // the converter's scale of this tile (Q's power of two folded in)
-        got = __all_sync(0xffffffffu, mbar_wait(bar_addr(m.kv_conv[s]), ph, abort, kTimeoutNs));
-        cs = m.tscale[s];
-      }
       // unscaled scores in token pairs: xp[2j + h] = head row[h], tokens
       // 8j + pair + {0, 1}
       float2 xp[16];
@@ -659,7 +828,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
         alpha[h] = 1.f;
         if (t == w.t0) {
           mnew[h] = sm;
-        } else if (sm > mrun[h] + kRescaleThreshold) {
+        } else if (sm > mrun[h] + kThreshold) {
           mnew[h] = sm;
           alpha[h] = exp2f(mrun[h] - sm);
           resc = true;
@@ -684,59 +853,93 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
       if (vote & 2u) { ok = false; break; }
       if (vote & 1u) {
         // rescaling O^T needs the previous tile's PV to have finished
-        const bool pv_done = mbar_wait(bar_addr(m.p_free), (p_it - 1) & 1, abort, kTimeoutNs);
+        // (one barrier per stage: its phase lags tile p_it - 1 by at most one,
+        // as the stage's reload for that tile waited for PV p_it - 1 - NS)
+        const bool pv_done =
+            mbar_wait(bar_addr(m.p_free[(p_it - 1) % NS]), ((p_it - 1) / NS) & 1, abort, kTimeoutNs);
         if (!named_sync_and(1, 128, pv_done)) { ok = false; break; }
         tc_fence_after();
         rescale_o(tq, m.alpha[p_it & 1], tp.npv);
       }
-      // P = 2^(s cs - m) in bf16 (f16 for e4m3 caches), row-major
-      // [head][token] in the swizzled K-major layout: each lane writes 4-byte
-      // token pairs; the sum takes the rounded values the MMA will read
+      // P = 2^(s cs - m), rounded as the MMAs will read it (bf16; two e4m3
+      // terms for e4m3 caches); the sum takes the rounded values
+      if constexpr (F8) {
+        // P scaled by 2^kFxPLog2Scale as hi + lo, two e4m3 terms; the sum
+        // takes the values the MMAs will read.  Token pair (8j + pair, + 1)
+        // of head r: core matrix (r / 8, (8j + pair) / 16), row r % 8, byte
+        // (8j + pair) % 16
+        unsigned char *pst = smem + off_kv<F8>() + st * kFxStageBytes + 4 * kFxBlock;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        unsigned char *prow = smem + kOffKv + s * kStageBytes + kb_off<KBG>(8) +
-                              (row[h] >> 3) * atom_stride<KBG>() + (row[h] & 7) * 128 + (lane & 3) * 4;
-        // a row that has seen no token yet keeps a -inf max: its P is 0
-        const float mref = MULTI && mnew[h] == -INFINITY ? 0.f : mnew[h];
-        const float2 c2 = make_float2(cs, cs), m2 = make_float2(-mref, -mref);
-        float2 lsum = make_float2(0.f, 0.f);
+        for (int h = 0; h < 2; ++h) {
+          const float mref = MULTI && mnew[h] == -INFINITY ? 0.f : mnew[h] - kFxPLog2Scale;
+          const float2 c2 = make_float2(cs, cs), m2 = make_float2(-mref, -mref);
+          unsigned char *prow = pst + (row[h] >> 3) * kFxPSbo + (row[h] & 7) * 16 + pair;
+          float2 lsum = make_float2(0.f, 0.f), xsum = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float2 arg = fma2(xp[2 * j + h], c2, m2);
-          const float e0 = ex2(arg.x), e1 = ex2(arg.y);
-          float2 back;
-          uint32_t bits;
-          if (F8) {
-            __half2 v = __floats2half2_rn(e0, e1);
-            back = __half22float2(v);
-            bits = *reinterpret_cast<uint32_t *>(&v);
-          } else {
-            __nv_bfloat162 v = __floats2bfloat162_rn(e0, e1);
-            bits = *reinterpret_cast<uint32_t *>(&v);
-            back = make_float2(__uint_as_float(bits << 16), __uint_as_float(bits & 0xffff0000u));
+          for (int j = 0; j < 8; ++j) {
+            const float2 arg = fma2(xp[2 * j + h], c2, m2);
+            const float e0 = ex2(arg.x), e1 = ex2(arg.y);
+            const uint16_t hi = float2_to_e4m3x2(e0, e1);
+            const float2 bh = e4m3x2_to_float2(hi);
+            const uint16_t lo = float2_to_e4m3x2(e0 - bh.x, e1 - bh.y);
+            const float2 bl = e4m3x2_to_float2(lo);
+            lsum = add2(lsum, add2(bh, bl));
+            xsum = add2(xsum, make_float2(e0, e1));
+            const int off = (j >> 1) * int(kFxPLbo) + 8 * (j & 1);
+            *reinterpret_cast<uint16_t *>(prow + off) = hi;
+            *reinterpret_cast<uint16_t *>(prow + kFxPTerm + off) = lo;
           }
-          lsum = add2(lsum, back);
-          *reinterpret_cast<uint32_t *>(prow + ((j ^ (row[h] & 7)) << 4)) = bits;
+          ellp[h] = ellp[h] * alpha[h] + (lsum.x + lsum.y);
+          ellx[h] = ellx[h] * alpha[h] + (xsum.x + xsum.y);
+          mrun[h] = mnew[h];
         }
-        ellp[h] = ellp[h] * alpha[h] + (lsum.x + lsum.y);
-        mrun[h] = mnew[h];
+        if (nv & 31) zero_value_tail_fx(smem + off_kv<F8>() + st * kFxStageBytes, nv, gt);
+      } else {
+        // bf16 P [head][token] in the stage's rope block, swizzled K-major:
+        // each lane writes 4-byte token pairs
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          unsigned char *prow = smem + kOffKv + s * kStageBytes + kb_off<KBG>(8) +
+                                (row[h] >> 3) * atom_stride<KBG>() + (row[h] & 7) * 128 + (lane & 3) * 4;
+          // a row that has seen no token yet keeps a -inf max: its P is 0
+          const float mref = MULTI && mnew[h] == -INFINITY ? 0.f : mnew[h];
+          const float2 c2 = make_float2(cs, cs), m2 = make_float2(-mref, -mref);
+          float2 lsum = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float2 arg = fma2(xp[2 * j + h], c2, m2);
+            const float e0 = ex2(arg.x), e1 = ex2(arg.y);
+            __nv_bfloat162 v = __floats2bfloat162_rn(e0, e1);
+            const uint32_t bits = *reinterpret_cast<uint32_t *>(&v);
+            lsum = add2(lsum, make_float2(__uint_as_float(bits << 16), __uint_as_float(bits & 0xffff0000u)));
+            *reinterpret_cast<uint32_t *>(prow + ((j ^ (row[h] & 7)) << 4)) = bits;
+          }
+          ellp[h] = ellp[h] * alpha[h] + (lsum.x + lsum.y);
+          mrun[h] = mnew[h];
+        }
+        // rows [nv, roundup16(nv)) of V are read by the last PV step but hold no
+        // owned token (stale or unowned data): zero their 512 value dims
+        if (nv & 15) zero_value_tail<KBG>(smem + kOffKv + s * kStageBytes, nv, gt);
       }
-      // rows [nv, roundup16(nv)) of V are read by the last PV step but hold no
-      // owned token (stale or unowned data): zero their 512 value dims
-      if (nv & 15) zero_value_tail<KBG>(smem + kOffKv + s * kStageBytes, nv, gt);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(m.p_full[s]));
+      if (lane == 0) mbar_arrive(bar_addr(m.p_full[st]));
     }
     if (!ok) break;
 
     // the four lanes of a head hold parts of its sum
-    float ell[2];
+    float ell[2], elx[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       ell[h] = ellp[h] + __shfl_xor_sync(0xffffffffu, ellp[h], 1);
       ell[h] += __shfl_xor_sync(0xffffffffu, ell[h], 2);
+      if (F8) {
+        elx[h] = ellx[h] + __shfl_xor_sync(0xffffffffu, ellx[h], 1);
+        elx[h] += __shfl_xor_sync(0xffffffffu, elx[h], 2);
+      } else {
+        elx[h] = ell[h];
+      }
     }
     // ---- epilogue of this CTA's share of request v
     if ((lane & 3) == 0) {  // per-head output scale: kv_scale / sum (0 for a row that saw nothing)
@@ -814,7 +1017,8 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
 #pragma unroll
     for (int h = 0; h < 2; ++h)
       if ((lane & 3) == 0 && row[h] < hn) {
-        const float lse2 = mrun[h] + log2f(ell[h]);
+        // (e4m3: the sum is of P scaled by 2^kFxPLog2Scale, before rounding)
+        const float lse2 = mrun[h] + log2f(elx[h]) - (F8 ? kFxPLog2Scale : 0.f);
         if (!split)
           p.lse[out_row0 + row[h]] = lse_out(p, lse2);
         else
@@ -825,166 +1029,80 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
   if (!ok) atomicOr(err, kErrTimeout);
 }
 
-// ------------------------------------------------------------------ e4m3 converter
+// ------------------------------------------------------------------ Q of an e4m3 cache
 //
-// Warps 9..11.  Q (bf16, as landed by TMA) becomes f16 scaled by 2^k, k chosen
-// from the largest |q| of the request so that it lies in [2^14, 2^15): every
-// bf16 value down to 2^-31 of that maximum is exact in f16 and nothing
-// overflows; the scores then carry 2^-k.  Each 8-byte chunk of fp8 values
-// (one row, 8 consecutive dims) becomes one 16-byte f16 chunk of the
-// swizzled [atom][dim block][8 rows][128 B] layout.
-
-// bf16 pair -> f16 pair, both scaled by the power of two `sc` (exact unless
-// the scaled value leaves f16's range, which the choice of k rules out).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc) {
-  const float lo = __uint_as_float(w << 16) * sc;
-  const float hi = __uint_as_float(w & 0xffff0000u) * sc;
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// 8 e4m3 values -> one 16-byte f16 chunk at `dst`.
-__device__ __forceinline__ void expand_fp8_store(unsigned char *dst, uint2 w) {
-  uint4 o;
-  o.x = e4m3x2_to_f16x2(uint16_t(w.x));
-  o.y = e4m3x2_to_f16x2(uint16_t(w.x >> 16));
-  o.z = e4m3x2_to_f16x2(uint16_t(w.y));
-  o.w = e4m3x2_to_f16x2(uint16_t(w.y >> 16));
-  *reinterpret_cast<uint4 *>(dst) = o;
-}
-
-// The request's Q (bf16, as landed) to f16 in place, scaled by 2^k; *qinv =
-// 2^-k.  Once per request piece: out of line.
-static __device__ __noinline__ bool convert_q(const TcParams &tp, TcMisc &m, unsigned char *smem, int g,
-                                       uint32_t q_it, float *qinv) {
-  using namespace tc;
-  const DecodeParams &p = tp.p;
-  volatile int *abort = &m.abort;
-  const int ct = int(threadIdx.x) - kConvWarp0 * 32;
-  const int cw = ct >> 5, lane = ct & 31;
-  constexpr int kQPer = kQBytes / 16 / kConvThreads;  // 48 uint4 of Q per thread
-  static_assert(kQBytes / 16 % kConvThreads == 0 && kQPer % 8 == 0, "Q split");
-  const bool got = mbar_wait(bar_addr(m.q_full), q_it & 1, abort, kTimeoutNs);
-  if (!named_sync_and(3, kConvThreads, got)) return false;
-  uint4 *qv = reinterpret_cast<uint4 *>(smem + kOffQ);  // [kb][64 rows][8 chunks]
-  // the maximum over this request's heads; rows past them (zeros, or the
-  // next request's heads that the box also covers) only feed score rows
-  // the epilogue drops
-  const int hn = min(kHeads, p.heads - g * kHeads);
-  uint32_t mx = 0;
-#pragma unroll 8
-  for (int u = 0; u < kQPer; ++u) {
-    const int i = ct + u * kConvThreads;
-    if (((i >> 3) & 63) >= hn) continue;
-    const uint4 w = qv[i];
-    mx = __vmaxu2(mx, w.x & 0x7fff7fffu);
-    mx = __vmaxu2(mx, w.y & 0x7fff7fffu);
-    mx = __vmaxu2(mx, w.z & 0x7fff7fffu);
-    mx = __vmaxu2(mx, w.w & 0x7fff7fffu);
-  }
-  mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
-  if (lane == 0) m.conv_max[cw] = mx;
-  named_sync(3, kConvThreads);
-  mx = max(m.conv_max[0], max(m.conv_max[1], m.conv_max[2]));
-  // |q| bits are ordered like magnitudes; an Inf or NaN keeps k = 0
-  int k = 0;
-  if (mx < 0x7f80u) k = min(126, max(-126, 14 - (int(mx >> 7) - 127)));
-  const float sc = __int_as_float((127 + k) << 23);
-  *qinv = __int_as_float((127 - k) << 23);
-#pragma unroll 8
-  for (int u = 0; u < kQPer; ++u) {
-    uint4 w = qv[ct + u * kConvThreads];
-    w.x = bf16x2_to_f16x2_scaled(w.x, sc);
-    w.y = bf16x2_to_f16x2_scaled(w.y, sc);
-    w.z = bf16x2_to_f16x2_scaled(w.z, sc);
-    w.w = bf16x2_to_f16x2_scaled(w.w, sc);
-    qv[ct + u * kConvThreads] = w;
-  }
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar_addr(m.q_ready));
-  return true;
-}
-
+// Warps 9..11: once per request piece, after the previous piece's score
+// MMAs have read Q, they read the piece's Q rows (bf16) from
+// global memory, take 2^k with the largest |q| of the piece in [2^7, 2^8),
+// and write hi = e4m3(2^k q) and lo = e4m3(2^k q - hi) into the two Q terms
+// (rows past the request's heads are zero).  hi + lo equals 2^k q exactly
+// down to 2^-2 (below that e4m3's subnormal step, 2^-9, bounds the error), so
+// the scores keep bf16 Q's precision; 2^-k goes to the softmax through a
+// slot tagged with the request.
 template <bool FUSED, int MULTI>
-__device__ __forceinline__ void tc_convert(const TcParams &tp, const CtaRange &r, TcMisc &m,
+__device__ __forceinline__ void tc_split_q(const TcParams &tp, const CtaRange &r, TcMisc<3> &m,
                                            unsigned char *smem, int *err) {
   using namespace tc;
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const int ct = int(threadIdx.x) - kConvWarp0 * 32;  // 0 .. 95
-  const int lane = ct & 31;
-  // Thread (tr, tc) = (ct / 24, ct % 24) converts, of rows 4k + tr, the 8-value
-  // chunks tc, tc + 24 and tc + 48: chunk c lands in dim block c / 8 at
-  // swizzled position (c % 8) ^ (row % 8), so the three chunks sit 3 blocks
-  // (3072 B) apart, and row 4k + tr has row % 8 = tr + 4 (k % 2), atom k / 2.
-  const int tr = ct / 24, tc = ct - 24 * (ct / 24);
-  const int src0 = tr * kRawRow + tc * 8;
-  const int dst0 = (tc >> 3) * 1024 + tr * 128 + (((tc & 7) ^ tr) << 4);
-  const int dst1 = (tc >> 3) * 1024 + (tr + 4) * 128 + (((tc & 7) ^ (tr + 4)) << 4);
-  static_assert(kConvThreads == 4 * 24 && kRawRow == 72 * 8, "converter split");
-  uint32_t kv_it = 0, q_it = 0;
-  float qinv = 1.f;
+  const int cw = ct >> 5, lane = ct & 31;
+  constexpr int kRowChunks = kDqk / 8;                // 72 chunks of 8 dims per row
+  uint32_t q_it = 0;
   bool ok = true;
-  for (TileCursor<FUSED, MULTI> c(p, r); c.live; c.step(), ++kv_it) {
-    if (c.first()) {
-      if (!convert_q(tp, m, smem, c.w.g, q_it, &qinv)) { ok = false; break; }
-      ++q_it;
-    }
-    const int s = kv_it & 1;
-    const bool got = mbar_wait(bar_addr(m.kv_full[s][0]), (kv_it >> 1) & 1, abort, kTimeoutNs);
+  Walk<FUSED, MULTI> w(p, r);
+  for (; w.next(); w.advance(), ++q_it) {
+    const bool got = mbar_wait(bar_addr(m.q_empty), (q_it & 1) ^ 1, abort, kTimeoutNs);
     if (!named_sync_and(3, kConvThreads, got)) { ok = false; break; }
-    unsigned char *stage = smem + kOffKv + s * kStageBytes;
-    const unsigned char *raw = stage + kRawOff;
-    // Rows past the request's end stay unconverted: their scores are masked
-    // and the softmax zeroes the value rows the last PV step reads.
-    //
-    // Destination atom a (rows 8a .. 8a + 7) covers raw rows 16 (a - 4) ..
-    // 16 (a - 4) + 15 for a >= 4, so the rows go in four groups: 0..31 (below
-    // the raw rows), 32..47 (over raw rows 0..31), 48..55 (over 32..47), and
-    // 56..63, which overlaps its own raw rows: read first, written last.
-    const int nv = c.nv();
-    uint2 w[4][3];
-    // steps k0 .. k0 + n - 1: loads, then conversions and stores
-    auto load = [&](int k0, int n) {
-#pragma unroll
-      for (int k = 0; k < n; ++k)
-        if (4 * (k0 + k) + tr < nv)
-#pragma unroll
-          for (int e = 0; e < 3; ++e)
-            w[k][e] = *reinterpret_cast<const uint2 *>(raw + src0 + (k0 + k) * 4 * kRawRow + e * 192);
-    };
-    auto store = [&](int k0, int n) {
-#pragma unroll
-      for (int k = 0; k < n; ++k)
-        if (4 * (k0 + k) + tr < nv)
-#pragma unroll
-          for (int e = 0; e < 3; ++e)
-            expand_fp8_store(stage + ((k0 + k) >> 1) * kAtomBytes + (((k0 + k) & 1) ? dst1 : dst0) +
-                                 e * 3072,
-                             w[k][e]);
-    };
-    load(0, 4); store(0, 4);
-    load(4, 4); store(4, 4);
-    if (nv > 32) {
-      named_sync(3, kConvThreads);
-      load(8, 4); store(8, 4);
-      if (nv > 48) {
-        named_sync(3, kConvThreads);
-        load(12, 4);            // rows 48..63
-        store(12, 2);           // rows 48..55 over raw rows 32..47
-        if (nv > 56) {
-          named_sync(3, kConvThreads);
-#pragma unroll
-          for (int k = 0; k < 2; ++k) w[k][0] = w[k + 2][0], w[k][1] = w[k + 2][1], w[k][2] = w[k + 2][2];
-          store(14, 2);
-        }
-      }
+    const int hn = min(kHeads, p.heads - w.g * kHeads);
+    const uint4 *qg =
+        reinterpret_cast<const uint4 *>(p.q + (size_t(w.rb) * p.heads + size_t(w.g) * kHeads) * kDqk);
+    uint32_t mx = 0;
+    for (int i = ct; i < hn * kRowChunks; i += kConvThreads) {
+      const uint4 v = qg[i];
+      mx = __vmaxu2(mx, v.x & 0x7fff7fffu);
+      mx = __vmaxu2(mx, v.y & 0x7fff7fffu);
+      mx = __vmaxu2(mx, v.z & 0x7fff7fffu);
+      mx = __vmaxu2(mx, v.w & 0x7fff7fffu);
     }
-    if (ct == 0) m.tscale[s] = p.score_scale_log2 * p.kv_scale * qinv;
+    mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
+    if (lane == 0) m.conv_max[cw] = mx;
+    named_sync(3, kConvThreads);
+    mx = max(m.conv_max[0], max(m.conv_max[1], m.conv_max[2]));
+    // |q| bits are ordered like magnitudes; an Inf or NaN keeps k = 0
+    int k = 0;
+    if (mx < 0x7f80u) k = min(126, max(-126, 134 - int(mx >> 7)));
+    const float sc = __int_as_float((127 + k) << 23);
+    for (int i = ct; i < kHeads * kRowChunks; i += kConvThreads) {
+      const int rr = i / kRowChunks, c = i - kRowChunks * rr;
+      const uint4 v = rr < hn ? qg[i] : make_uint4(0, 0, 0, 0);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t hw[2] = {0, 0}, lw[2] = {0, 0};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float f0 = __uint_as_float(wv[e] << 16) * sc, f1 = __uint_as_float(wv[e] & 0xffff0000u) * sc;
+        const uint16_t h = float2_to_e4m3x2(f0, f1);
+        const float2 bh = e4m3x2_to_float2(h);
+        const uint16_t l = float2_to_e4m3x2(f0 - bh.x, f1 - bh.y);
+        hw[e >> 1] |= uint32_t(h) << (16 * (e & 1));
+        lw[e >> 1] |= uint32_t(l) << (16 * (e & 1));
+      }
+      // dims 8c .. 8c + 7: block c / 16, bytes 8 (c % 16) of the 128-byte row,
+      // 16-byte chunk (c % 16) / 2 at its swizzled place
+      const int b = c & 15;
+      const int off = (c >> 4) * kFxBlock + (rr >> 3) * 1024 + (rr & 7) * 128 + (((b >> 1) ^ (rr & 7)) << 4) +
+                      8 * (b & 1);
+      *reinterpret_cast<uint2 *>(smem + off) = make_uint2(hw[0], hw[1]);
+      *reinterpret_cast<uint2 *>(smem + kFxQTerm + off) = make_uint2(lw[0], lw[1]);
+    }
+    if (ct == 0) {
+      m.qinv[q_it & 3] = __int_as_float((127 - k) << 23);
+      __threadfence_block();
+      reinterpret_cast<volatile int *>(m.qinv_v)[q_it & 3] = w.v;
+    }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar_addr(m.kv_conv[s]));
+    if (lane == 0) mbar_arrive(bar_addr(m.q_ready));
   }
   if (!ok) atomicOr(err, kErrTimeout);
 }
@@ -1002,7 +1120,8 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
   unsigned char *smem = smem_raw + pad;
   const uint32_t sbase = raw + pad;
-  TcMisc &m = *reinterpret_cast<TcMisc *>(smem + kOffMisc);
+  constexpr int NS = num_stages<F8>();
+  TcMiscFor<F8> &m = *reinterpret_cast<TcMiscFor<F8> *>(smem + off_misc<F8>());
   const DecodeParams &p = tp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int *err = error_word(p);
@@ -1010,28 +1129,29 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
 
   // Q rows past the request's heads are read by the MMAs but never loaded:
   // they must hold finite values.  (P rows past them are written each tile.)
-  for (int i = tid; i < kQBytes / 16; i += tc_threads<F8>())
+  for (int i = tid; i < off_kv<F8>() / 16; i += tc_threads<F8>())
     reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NS; ++s) {
       for (int g = 0; g < kMaxGroups; ++g) mbar_init(bar_addr(m.kv_full[s][g]), 1);
       mbar_init(bar_addr(m.kv_empty[s]), 2);  // both PV issuers commit
-      mbar_init(bar_addr(m.s_full[s]), 2);   // both score issuers commit
-      mbar_init(bar_addr(m.s_free[s]), 4);
+      // one per stage: the softmax runs ahead of the PV issuers, and tile
+      // k + NS (same stage) cannot reach the softmax before PV k has been
+      // issued
+      mbar_init(bar_addr(m.p_full[s]), 4);
+      mbar_init(bar_addr(m.p_free[s]), 2);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_addr(m.s_full[b]), 2);  // both score issuers commit
+      mbar_init(bar_addr(m.s_free[b]), 4);
     }
     mbar_init(bar_addr(m.q_full), 1);
     mbar_init(bar_addr(m.q_empty), 2);
-    // one per stage: the softmax runs ahead of the PV issuers, and tile k + 2
-    // (same stage) cannot reach the softmax before PV k has been issued
-    mbar_init(bar_addr(m.p_full[0]), 4);
-    mbar_init(bar_addr(m.p_full[1]), 4);
-    mbar_init(bar_addr(m.p_free), 2);
     mbar_init(bar_addr(m.o_full), 2);
     mbar_init(bar_addr(m.o_free), 4);
     mbar_init(bar_addr(m.drain), 4);       // all four MMA issuers
-    mbar_init(bar_addr(m.kv_conv[0]), 3);  // one arrival per converter warp
-    mbar_init(bar_addr(m.kv_conv[1]), 3);
-    mbar_init(bar_addr(m.q_ready), 3);
+    mbar_init(bar_addr(m.q_ready), 3);     // one arrival per Q-splitting warp
+    for (int i = 0; i < 4; ++i) m.qinv_v[i] = -1;
     m.abort = 0;
     fence_barrier_init();
   }
@@ -1068,17 +1188,17 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
   const CtaRange r = m.range;
 
   if (r.start < r.end) {
+    const uint32_t sKv = sbase + off_kv<F8>();
     if (warp == 0) {
-      tc_producer<F8, FUSED, MULTI, AHEAD>(tp, r, m, sbase + kOffQ, sbase + kOffKv, &tm_q, &tm_kv, &tm_kvg,
-                                           err);
+      tc_producer<F8, FUSED, MULTI, AHEAD>(tp, r, m, sbase + kOffQ, sKv, &tm_q, &tm_kv, &tm_kvg, err);
     } else if (warp == 1 || warp == 2) {
-      if (lane == 0) tc_mma_s<F8, FUSED, MULTI, KBG>(tp, r, m, sbase + kOffQ, sbase + kOffKv, tmem, warp - 1, err);
+      if (lane == 0) tc_mma_s<F8, FUSED, MULTI, KBG>(tp, r, m, sbase + kOffQ, sKv, tmem, warp - 1, err);
     } else if (warp == 3 || warp == 8) {
-      if (lane == 0) tc_mma_pv<F8, FUSED, MULTI, KBG>(tp, r, m, sbase + kOffKv, tmem, warp == 8, err);
+      if (lane == 0) tc_mma_pv<F8, FUSED, MULTI, KBG>(tp, r, m, sKv, tmem, warp == 8, err);
     } else if (warp < 8) {
       tc_softmax<F8, FUSED, MULTI, KBG>(tp, r, m, smem, tmem, err);
-    } else if (F8) {
-      tc_convert<FUSED, MULTI>(tp, r, m, smem, err);
+    } else if constexpr (F8) {
+      tc_split_q<FUSED, MULTI>(tp, r, m, smem, err);
     }
   }
   tc_fence_before();

@@ -181,6 +181,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
          (uint64_t((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same for an unswizzled K-major operand (layout type 0): 8-row x 16-byte
+// core matrices stored as 128 contiguous bytes; `lbo` is the distance between
+// core matrices adjacent along K, `sbo` between those adjacent along M / N.
+__device__ __forceinline__ uint64_t smem_desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo & 0x3FFFFu) >> 4) << 16) |
+         (uint64_t((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: operand stored MN-major (else K-major).
 // kind::f16 instruction descriptor with an f32 accumulator; A and B are both
@@ -194,6 +202,12 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn, boo
 
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
   return idesc_f32acc(M, N, a_mn, b_mn, true);
+}
+
+// kind::f8f6f4 instruction descriptor: A and B both e4m3 (format 0), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -224,6 +238,16 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
   asm volatile(
       "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem] x B[smem], 8-bit operands (K = 32 per instruction).
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
