@@ -376,6 +376,22 @@ __device__ __forceinline__ uint16_t float2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Two floats -> two OCP e5m2 bytes (hardware conversion, RNE, saturated):
+// `lo` in the low byte.
+__device__ __forceinline__ uint16_t float2_to_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("{ cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2; }" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two e5m2 bytes -> two exact floats (through the hardware f16 conversion).
+__device__ __forceinline__ float2 e5m2x2_to_float2(uint16_t two) {
+  uint32_t h;
+  asm("{ cvt.rn.f16x2.e5m2x2 %0, %1; }" : "=r"(h) : "h"(two));
+  __half2 hh = *reinterpret_cast<__half2 *>(&h);
+  return __half22float2(hh);
+}
+
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
   uint32_t h = e4m3x2_to_f16x2(two);
   __half2 hh = *reinterpret_cast<__half2 *>(&h);

@@ -29,7 +29,7 @@
 // the score issuers take one term each (S = Q_hi K^T + Q_lo K^T, 18 K-steps
 // of 32 dims), the scores carry sm_scale * kv_scale * 2^-k, and the softmax
 // writes P, scaled by 2^4 (with the O rescale threshold lowered to 2^4), as
-// two e4m3 terms as well, so that each PV step is two MMAs; the output is
+// two terms as well (hi e4m3, lo e5m2), so that each PV step is two MMAs; the output is
 // normalised by the sum of P as stored, the LSE takes the sum before
 // rounding.  V^T is the raw rows read MN-major.
 //
@@ -104,18 +104,20 @@ constexpr int kOffMisc = kOffKv + 2 * kStageBytes;
 // K-major; three stages of the raw rows as landed, [5 blocks][8 atoms][8
 // rows][128 B] (dims 576..639 of block 4 are the copy's zero fill).  Block 4
 // (the rope dims), dead once the scores are computed, then holds P as two
-// e4m3 terms [64 heads][64 tokens] of 4 KB each, unswizzled: 8-head x
-// 16-token core matrices of 128 B.
+// terms [64 heads][64 tokens] of 4 KB each, hi in e4m3 and lo in e5m2,
+// unswizzled: 8-head x 16-token core matrices of 128 B.
 constexpr int kFxBlocks = 5;
 constexpr int kFxBlock = 64 * 128;                   // one block of 64 rows
 constexpr int kFxQTerm = kFxBlocks * kFxBlock;       // 40 KB
 constexpr int kFxStageBytes = kFxBlocks * kFxBlock;  // 40 KB
 constexpr uint32_t kFxPLbo = 128, kFxPSbo = 512;     // P core matrices along tokens / heads
 constexpr int kFxPTerm = 4096;                       // P lo after P hi
-// P is stored as 2^(8 - threshold) p (p <= 2^threshold): it stays below the
-// e4m3 maximum (448), and weights down to 2^-13 of the running maximum stay
-// above e4m3's subnormal floor (2^-9).  The sum that normalises the output
-// takes P as stored; the LSE takes the sum of P before rounding.
+// P is stored as 2^(8 - threshold) p (p <= 2^threshold), below the e4m3
+// maximum (448).  Its lo term is e5m2, whose subnormals reach 2^-16: weights
+// down to 2^-20 of the running maximum keep a value (e4m3's floor, 2^-9,
+// would drop those below 2^-13, and a long context's tail of such weights
+// can hold much of the mass).  The sum that normalises the output takes P
+// as stored; the LSE takes the sum of P before rounding.
 constexpr float kFxRescaleThreshold = 4.f;
 constexpr float kFxPLog2Scale = 8.f - kFxRescaleThreshold;
 template <bool F8>
@@ -526,9 +528,10 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
   if constexpr (F8) {
     // O^T(chunk c) += V^T P_hi^T + V^T P_lo^T over ceil(nv / 32) steps of 32
     // tokens: V^T of chunk c is block c of the raw rows, MN-major (128 value
-    // dims per swizzled row); P's terms are K-major, unswizzled
+    // dims per swizzled row); P's terms (e4m3, e5m2) are K-major, unswizzled
     constexpr int NS = num_stages<F8>();
     const uint32_t idesc_o = idesc_e4m3_f32(128, tp.npv, true, false);
+    const uint32_t idesc_o_lo = idesc_f8_f32(128, tp.npv, true, false, kFmtE4M3, kFmtE5M2);
     constexpr uint64_t kStageEnc = uint64_t(kFxStageBytes) >> 4;
     uint64_t dv0[2];
 #pragma unroll
@@ -558,7 +561,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
             const uint32_t dcol = tmem + kColO + 64 * (2 * half + cc);
             const uint64_t dv = dv0[cc] + st * kStageEnc + ((ks * 4 * 1024) >> 4);
             mma_f8_ss(dcol, dv, dp + ((ks * 2 * kFxPLbo) >> 4), idesc_o, !(fresh && ks == 0));
-            mma_f8_ss(dcol, dv, dp + ((kFxPTerm + ks * 2 * kFxPLbo) >> 4), idesc_o, 1u);
+            mma_f8_ss(dcol, dv, dp + ((kFxPTerm + ks * 2 * kFxPLbo) >> 4), idesc_o_lo, 1u);
           }
         }
       }
@@ -864,7 +867,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
       // P = 2^(s cs - m), rounded as the MMAs will read it (bf16; two e4m3
       // terms for e4m3 caches); the sum takes the rounded values
       if constexpr (F8) {
-        // P scaled by 2^kFxPLog2Scale as hi + lo, two e4m3 terms; the sum
+        // P scaled by 2^kFxPLog2Scale as hi + lo, hi in e4m3 and lo in e5m2; the sum
         // takes the values the MMAs will read.  Token pair (8j + pair, + 1)
         // of head r: core matrix (r / 8, (8j + pair) / 16), row r % 8, byte
         // (8j + pair) % 16
@@ -881,8 +884,8 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
             const float e0 = ex2(arg.x), e1 = ex2(arg.y);
             const uint16_t hi = float2_to_e4m3x2(e0, e1);
             const float2 bh = e4m3x2_to_float2(hi);
-            const uint16_t lo = float2_to_e4m3x2(e0 - bh.x, e1 - bh.y);
-            const float2 bl = e4m3x2_to_float2(lo);
+            const uint16_t lo = float2_to_e5m2x2(e0 - bh.x, e1 - bh.y);
+            const float2 bl = e5m2x2_to_float2(lo);
             lsum = add2(lsum, add2(bh, bl));
             xsum = add2(xsum, make_float2(e0, e1));
             const int off = (j >> 1) * int(kFxPLbo) + 8 * (j & 1);

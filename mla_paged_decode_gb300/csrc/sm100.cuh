@@ -204,10 +204,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
   return idesc_f32acc(M, N, a_mn, b_mn, true);
 }
 
-// kind::f8f6f4 instruction descriptor: A and B both e4m3 (format 0), fp32 D.
+// kind::f8f6f4 instruction descriptor with an fp32 D; A and B each e4m3
+// (format 0) or e5m2 (format 1), independently.
+constexpr uint32_t kFmtE4M3 = 0, kFmtE5M2 = 1;
+__host__ __device__ constexpr uint32_t idesc_f8_f32(int M, int N, bool a_mn, bool b_mn, uint32_t a_fmt,
+                                                    uint32_t b_fmt) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | (uint32_t(N >> 3) << 17) |
-         (uint32_t(M >> 4) << 24);
+  return idesc_f8_f32(M, N, a_mn, b_mn, kFmtE4M3, kFmtE4M3);
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

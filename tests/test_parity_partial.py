@@ -272,10 +272,11 @@ def test_growing_scores_take_the_rescale_path(num_parts):
 @pytest.mark.parametrize("num_parts", [1, 4])
 @pytest.mark.parametrize("q_shift", [16, -24])
 def test_fp8_query_far_outside_f16_range(q_shift, num_parts):
-    """An e4m3 cache runs its MMAs on f16 operands: Q is rescaled by a power of
-    two first, so a query of magnitude 2^16 (past f16's maximum) or 2^-24 (in
-    its subnormals) gives the same attention as the unscaled one; sm_scale
-    carries the opposite power so that the scores are ordinary."""
+    """An e4m3 cache runs its MMAs on e4m3 operands: Q is rescaled by a power of
+    two and split into two e4m3 terms, so a query of magnitude 2^16 (past the
+    e4m3 maximum) or 2^-24 (far below its subnormals) gives the same
+    attention as the unscaled one; sm_scale carries the opposite power so
+    that the scores are ordinary."""
     case = workloads.make_decode_case("fp8_qshift", 64, [700, 65, 1300], seed=30 + q_shift,
                                       device="cuda", kv_dtype="e4m3", num_parts=num_parts)
     case.q = (case.q.float() * 2.0 ** q_shift).to(torch.bfloat16)
@@ -287,7 +288,7 @@ def test_fp8_query_far_outside_f16_range(q_shift, num_parts):
 def test_fp8_cache_of_subnormal_codes(num_parts):
     """Every cached code has a zero exponent field: OCP e4m3 subnormals,
     (m / 8) * 2^-6 times the scale.  With a scale of 64 they are ordinary
-    keys and values, and the kernel's f16 expansion must keep them exact; a
+    keys and values, and the kernel's e4m3 MMAs must take them as stored; a
     flush to zero anywhere would show in the relative-norm bound, which
     holds for outputs of any magnitude."""
     case = workloads.make_decode_case("fp8_subnormal", 64, [700, 65, 1300], seed=41,
@@ -295,3 +296,24 @@ def test_fp8_cache_of_subnormal_codes(num_parts):
     case.kv_pages &= 0x87
     case.kv_scale = 64.0
     _check_all(case, bases=(0, 1), atol=FP8_ATOL)
+
+
+@pytest.mark.parametrize("num_parts", [1, 3])
+def test_fp8_attention_sink_with_a_long_tail(num_parts):
+    """Each request's first token scores 10 nats above all the others, so
+    every other weight is e^-10 (about 2^-14.4) of the maximum, yet the
+    20,000-token tail holds nearly half of the softmax mass.  P enters the
+    e4m3 MMAs as two terms; weights that small must keep a value (its lo
+    term is e5m2) or the output collapses onto the first token's row."""
+    case = workloads.make_decode_case("fp8_sink", 64, [20000, 3000], seed=52, device="cuda",
+                                      kv_dtype="e4m3", num_parts=num_parts)
+    kv = case.kv_pages.clone()
+    kv[:, :, 512:] = 0                       # rope codes: +0, so every score is 0 ...
+    bt = case.block_table.cpu()
+    for b in range(case.batch):
+        kv[int(bt[b, 0]), 0, 512:] = 0x78    # ... but token 0's: e4m3 code of 256
+    case.kv_pages = kv
+    q = torch.zeros_like(case.q, dtype=torch.float32)
+    q[..., 512:] = 10.0 / (case.sm_scale * 64 * 256.0 * case.kv_scale)
+    case.q = q.to(torch.bfloat16)
+    _check_all(case, bases=(0,), atol=FP8_ATOL)
