@@ -807,7 +807,7 @@ def measure_fp8(args, world, rank, mla, dev, stream):
     """--op fp8: the e4m3-cache workload (B=128, H=128, lognormal lengths with
     median 8192, per-tensor scale, P=1) through mla_decode_partial.  Its
     roofline is the tensor pipe: the MMAs run on e4m3 operands, the cache's
-    raw rows with Q and P each as two e4m3 terms (so every product is two
+    raw rows with Q and P each as two fp8 terms (so every product is two
     MMAs, and the executed MMA flops are twice the algorithmic ones); the
     two 64-head groups of a request walk its pages side by side on two SMs,
     so the second read of a page is served by L2."""
@@ -867,7 +867,7 @@ def measure_fp8(args, world, rank, mla, dev, stream):
                                "timed together per call (e4m3 MMAs on the raw cache rows; real "
                                "heads' flops, QK^T over 576 dims and PV over 512)",
                      "mma_tflops": 2.0 * tflops, "mma_frac": 2.0 * tflops / tpeak,
-                     "mma_note": "Q and P enter the MMAs as two e4m3 terms each (hi + lo), so "
+                     "mma_note": "Q and P enter the MMAs as two fp8 terms each (hi + lo), so "
                                  "the MMAs execute twice the algorithmic flops",
                      "hbm_achieved_gbs": kv_bytes / per_s / 1e9, "hbm_peak_gbs": peak,
                      "hbm_frac": kv_bytes / per_s / 1e9 / peak, "hbm_peak_source": peak_kind},

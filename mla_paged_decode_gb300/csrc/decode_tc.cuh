@@ -29,9 +29,9 @@
 // the score issuers take one term each (S = Q_hi K^T + Q_lo K^T, 18 K-steps
 // of 32 dims), the scores carry sm_scale * kv_scale * 2^-k, and the softmax
 // writes P, scaled by 2^4 (with the O rescale threshold lowered to 2^4), as
-// two terms as well (hi e4m3, lo e5m2), so that each PV step is two MMAs; the output is
-// normalised by the sum of P as stored, the LSE takes the sum before
-// rounding.  V^T is the raw rows read MN-major.
+// two terms as well (hi e4m3, lo e5m2), so that each PV step is two MMAs;
+// the output is normalised by the sum of P as stored, the LSE takes the sum
+// before rounding.  V^T is the raw rows read MN-major.
 //
 // Partitions: P divides 8 here (64/P owned rows per page), or P in
 // {3, 5, 6, 7}: the strided gather (MULTI == 2, DecodeParams::strided), where
