@@ -27,6 +27,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -113,16 +114,27 @@ def measured_bf16_tflops():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+_COMMENT = re.compile(r"/\*.*?\*/|//[^\n]*", re.S)
+
+
+def code_tokens(text: str) -> str:
+    """C++/CUDA source with its comments removed and its whitespace collapsed:
+    what the compiler sees of it (the sources carry no `//` or `/*` inside
+    string literals)."""
+    return " ".join(_COMMENT.sub(" ", text).split())
+
+
 def kernel_digest(sources=None) -> str:
-    """Digest of the kernel sources: the named files of csrc/ (those one
-    kernel and its launch are built from), else all of them."""
+    """Digest of the kernel sources' code (comments and layout left out): the
+    named files of csrc/ (those one kernel and its launch are built from),
+    else all of them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_paged_decode_gb300", "csrc")
     names = sorted(sources) if sources else sorted(
         n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
     for name in names:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name)) as f:
+            h.update((name + "\n" + code_tokens(f.read())).encode())
     return h.hexdigest()[:16]
 
 
