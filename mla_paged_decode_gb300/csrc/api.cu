@@ -204,6 +204,17 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 strided blocks", r);
+    // blocks 0..3 of an atom in one box, landing [block][8 rows][128 B]:
+    // (128 bytes, 64 page rows, 4 blocks, pages).  It takes the Q map's slot,
+    // which an e4m3 cache does not use (the kernel splits Q itself).
+    cuuint64_t gdims[4] = {128, cuuint64_t(mla::kPage), 4, cuuint64_t(d->num_pages)};
+    cuuint64_t gstrides[3] = {row8, 128, cuuint64_t(mla::kPage) * row8};
+    cuuint32_t gbox[4] = {128, 8 * P, 4, 1};
+    cuuint32_t ges[4] = {1, P, 1, 1};
+    r = enc(tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(kv), gdims, gstrides, gbox, ges,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 strided grouped blocks", r);
   } else if (d->kv_dtype == MLA_KV_E4M3) {
     const cuuint64_t P = cuuint64_t(num_parts);
     const cuuint32_t R = cuuint32_t(mla::kPage / num_parts);
@@ -229,6 +240,21 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
             fstrides, fbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 blocks", r);
+    if (!(num_parts == 1 && !all_parts)) {
+      // a tile of several pages: blocks 0..3 of a page's owned atoms in one
+      // box, landing [atom][block][8 rows][128 B]: (128 bytes, 8 rows, 4
+      // blocks, 8-row atoms, partitions).  It takes the Q map's slot, which
+      // an e4m3 cache does not use (the kernel splits Q itself).
+      const cuuint64_t G = 8 / P;
+      cuuint64_t gdims[5] = {128, 8, 4, cuuint64_t(d->num_pages) * G, P};
+      cuuint64_t gstrides[4] = {P * row8, 128, 8 * P * row8, row8};
+      cuuint32_t gbox[5] = {128, 8, 4, cuuint32_t(G), 1};
+      cuuint32_t ges[5] = {1, 1, 1, 1, 1};
+      r = enc(tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, all_parts ? 5 : 4, const_cast<char *>(base), gdims,
+              gstrides, gbox, ges, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 grouped blocks", r);
+    }
   } else if (strided) {
     // (64 dims, 64 page rows, 9 blocks of 64 dims, pages): one box is one
     // atom, rows c, c + P, ..., c + 7P of a page (traversal stride P), which

@@ -28,8 +28,8 @@
 // down to 2^-2 of the scaled values (k puts the largest |q| in [2^7, 2^8));
 // the score issuers take one term each (S = Q_hi K^T + Q_lo K^T, 18 K-steps
 // of 32 dims), the scores carry sm_scale * kv_scale * 2^-k, and the softmax
-// writes P, scaled by 2^4 (with the O rescale threshold lowered to 2^4), as
-// two terms as well (hi e4m3, lo e5m2), so that each PV step is two MMAs;
+// writes P as two terms as well (hi e4m3, lo e5m2: P <= 2^8 stays below
+// e4m3's maximum), so that each PV step is two MMAs;
 // the output is normalised by the sum of P as stored, the LSE takes the sum
 // before rounding.  V^T is the raw rows read MN-major.
 //
@@ -46,7 +46,7 @@
 // accumulators so consecutive MMAs are independent) -> s_full -> softmax
 // reads S_i, frees it (s_free), waits for PV_{i-1} (p_free) and rescales
 // O^T only when some head's running max grew by more than the threshold
-// (2^8; e4m3: 2^4), writes P_i -> p_full -> MMA PV_i (4 independent
+// (2^8), writes P_i -> p_full -> MMA PV_i (4 independent
 // value-dim chunks) -> kv_empty + p_free.  The score issuers start S_{i+1} as
 // soon as tile i+1 lands, so the score MMAs of the next tile overlap this
 // tile's softmax, and the producer keeps the pages of the next tile (two
@@ -83,8 +83,10 @@ constexpr int kStageBytes = 8 * kAtomBytes;  // 64 tokens
 // e4m3 stage is filled by the converter).  P [64 heads][64 tokens] reuses
 // the rope block (dims 512..575) of the tile's own stage, dead once S is
 // computed.
+// (e4m3: blocks of 128 dims per landing group, 1 when a tile is one page,
+// else 4: blocks 0..3 of an atom together, block 4 apart)
 template <bool F8, int AHEAD>
-constexpr int stage_kbg() { return !F8 && AHEAD == 1 ? 3 : kKb; }
+constexpr int stage_kbg() { return F8 ? (AHEAD == 1 ? 1 : 4) : AHEAD == 1 ? 3 : kKb; }
 template <int KBG>
 constexpr int num_groups() { return kKb / KBG; }
 template <int KBG>
@@ -101,24 +103,32 @@ constexpr int kOffMisc = kOffKv + 2 * kStageBytes;
 
 // e4m3 caches, read by fp8 MMAs straight from the raw rows: Q as two e4m3
 // terms, hi and lo, each [5 blocks of 128 dims][64 rows][128 B], swizzled
-// K-major; three stages of the raw rows as landed, [5 blocks][8 atoms][8
-// rows][128 B] (dims 576..639 of block 4 are the copy's zero fill).  Block 4
-// (the rope dims), dead once the scores are computed, then holds P as two
-// terms [64 heads][64 tokens] of 4 KB each, hi in e4m3 and lo in e5m2,
-// unswizzled: 8-head x 16-token core matrices of 128 B.
+// K-major; three stages of the raw rows as landed: blocks 0..3 as [block][8
+// atoms][8 rows][128 B] when a tile is one page (one box and barrier per
+// block), else as [8 atoms][block][8 rows][128 B] (one box per page for all
+// four), and block 4 as [64 rows][128 B] after them (dims 576..639 are the
+// copy's zero fill).  Block 4 (the rope dims), dead once the scores are
+// computed, then holds P as two terms [64 heads][64 tokens] of 4 KB each, hi
+// in e4m3 and lo in e5m2, unswizzled: 8-head x 16-token core matrices of 128 B.
 constexpr int kFxBlocks = 5;
 constexpr int kFxBlock = 64 * 128;                   // one block of 64 rows
 constexpr int kFxQTerm = kFxBlocks * kFxBlock;       // 40 KB
 constexpr int kFxStageBytes = kFxBlocks * kFxBlock;  // 40 KB
 constexpr uint32_t kFxPLbo = 128, kFxPSbo = 512;     // P core matrices along tokens / heads
+// strides of the raw-row layout: between blocks 0..3, and between 8-row atoms
+template <int KBG>
+constexpr uint32_t fx_blk() { return KBG == 1 ? uint32_t(kFxBlock) : 1024u; }
+template <int KBG>
+constexpr uint32_t fx_atom() { return KBG == 1 ? 1024u : 4096u; }
 constexpr int kFxPTerm = 4096;                       // P lo after P hi
 // P is stored as 2^(8 - threshold) p (p <= 2^threshold), below the e4m3
 // maximum (448).  Its lo term is e5m2, whose subnormals reach 2^-16: weights
-// down to 2^-20 of the running maximum keep a value (e4m3's floor, 2^-9,
-// would drop those below 2^-13, and a long context's tail of such weights
-// can hold much of the mass).  The sum that normalises the output takes P
-// as stored; the LSE takes the sum of P before rounding.
-constexpr float kFxRescaleThreshold = 4.f;
+// down to 2^-16 of the running maximum keep a value (e4m3's floor, 2^-9,
+// would drop those below 2^-9, and a long context's tail of such weights can
+// hold much of the mass).  The sum that normalises the output takes P as
+// stored; the LSE takes the sum of P before rounding.  (A lower threshold
+// would lower that floor further but rescales O far more often.)
+constexpr float kFxRescaleThreshold = 8.f;
 constexpr float kFxPLog2Scale = 8.f - kFxRescaleThreshold;
 template <bool F8>
 constexpr int num_stages() { return F8 ? 3 : 2; }
@@ -284,7 +294,8 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   // block of 128 dims (one barrier each), one swizzled box of the page's
   // 8 * groups_per_page owned rows (the strided gather: of one atom's rows)
   const int rows_per_page = 8 * tp.groups_per_page;
-  constexpr int KBG = stage_kbg<F8, AHEAD>(), kG = F8 ? kFxBlocks : num_groups<KBG>();
+  constexpr int KBG = stage_kbg<F8, AHEAD>();
+  constexpr int kG = F8 ? (KBG == 1 ? kFxBlocks : 2) : num_groups<KBG>();
   // bytes one page lands per barrier: its rows of one block, or one column group
   const uint32_t page_bytes = F8 ? uint32_t(tp.groups_per_page) * 1024u
                                  : uint32_t(tp.groups_per_page) * atom_stride<KBG>();
@@ -362,23 +373,37 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
       ok = false;
       break;
     }
-    if (lane < kG) mbar_arrive_expect_tx(bar_addr(m.kv_full[s][lane]), bytes);
+    // (e4m3 with blocks 0..3 grouped: four blocks' bytes on the first barrier)
+    if (lane < kG)
+      mbar_arrive_expect_tx(bar_addr(m.kv_full[s][lane]), F8 && KBG == 4 && lane == 0 ? 4 * bytes : bytes);
     __syncwarp();
     if (load) {
       const uint32_t dst = sKv + s * stage_bytes<F8>() + lane * page_bytes;
-      if (F8) {
-        // block g: dims [128 g, 128 g + 128) (block 4 runs past the row: zero
-        // fill) of this lane's rows: its page's owned rows, or one atom of the
-        // strided gather, rows row0 + iP of page pg (traversal stride P)
+      if (F8 && KBG == 1) {
+        // one page a tile: block g, dims [128 g, 128 g + 128) of its 64 rows
+        // (block 4 runs past the row: zero fill)
 #pragma unroll
-        for (int g = 0; g < kFxBlocks; ++g) {
-          const uint32_t dg = dst + uint32_t(g) * kFxBlock;
-          if (STRIDED)
-            tma_load_3d(dg, tm_kvg, bar_addr(m.kv_full[s][g]), 128 * g, row0, pg);
-          else if (FUSED)
-            tma_load_3d(dg, tm_kvg, bar_addr(m.kv_full[s][g]), 128 * g, pg * rows_per_page, cur.w.pc);
-          else
-            tma_load_2d(dg, tm_kvg, bar_addr(m.kv_full[s][g]), 128 * g, pg * rows_per_page);
+        for (int g = 0; g < kFxBlocks; ++g)
+          tma_load_2d(sKv + s * stage_bytes<F8>() + uint32_t(g) * kFxBlock, tm_kvg, bar_addr(m.kv_full[s][g]),
+                      128 * g, pg * rows_per_page);
+      } else if (F8) {
+        // this lane's rows (its page's owned rows, or one atom of the strided
+        // gather: rows row0 + iP of page pg, traversal stride P): blocks 0..3
+        // as [atom][block][8 rows][128 B] through the grouped map (in the Q
+        // map's slot: an e4m3 cache's Q is read by warps 9..11), block 4
+        // after all four
+        const CUtensorMap *tm_kvb = tm_q;
+        const uint32_t d0 = sKv + s * stage_bytes<F8>() + lane * page_bytes * 4;
+        const uint32_t d4 = sKv + s * stage_bytes<F8>() + 4 * kFxBlock + lane * page_bytes;
+        if (STRIDED) {
+          tma_load_4d(d0, tm_kvb, bar_addr(m.kv_full[s][0]), 0, row0, 0, pg);
+          tma_load_3d(d4, tm_kvg, bar_addr(m.kv_full[s][1]), 512, row0, pg);
+        } else if (FUSED) {
+          tma_load_5d(d0, tm_kvb, bar_addr(m.kv_full[s][0]), 0, 0, 0, pg * tp.groups_per_page, cur.w.pc);
+          tma_load_3d(d4, tm_kvg, bar_addr(m.kv_full[s][1]), 512, pg * rows_per_page, cur.w.pc);
+        } else {
+          tma_load_4d(d0, tm_kvb, bar_addr(m.kv_full[s][0]), 0, 0, 0, pg * tp.groups_per_page);
+          tma_load_2d(d4, tm_kvg, bar_addr(m.kv_full[s][1]), 512, pg * rows_per_page);
         }
       } else if (STRIDED) {
         // one atom: rows row0 + iP (traversal stride P) of page pg, all dims
@@ -436,7 +461,8 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
     constexpr int NS = num_stages<F8>();
     const uint32_t idesc_s = idesc_e4m3_f32(64, 64, false, false);
     const uint64_t dq = smem_desc_sw128(sQ + uint32_t(chain) * kFxQTerm, 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(sKv, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sKv, 16, fx_atom<KBG>());      // blocks 0..3
+    const uint64_t dk4 = smem_desc_sw128(sKv + 4 * kFxBlock, 16, 1024);  // block 4
     constexpr uint64_t kStageEnc = uint64_t(kFxStageBytes) >> 4;
     uint32_t s_it = 0, q_it = 0;
     bool ok = true;
@@ -451,18 +477,20 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
         ok = false;
         break;
       }
-      const uint64_t dk = dk0 + st * kStageEnc;
       const uint32_t d = tmem + kColS + 64 * (2 * sb + chain);
       bool landed = true;
 #pragma unroll
       for (int kb = 0; kb < kFxBlocks; ++kb) {
-        landed = mbar_wait(bar_addr(m.kv_full[st][kb]), ph, abort, kTimeoutNs);
-        if (!landed) break;
-        tc_fence_after();
+        if (KBG == 1 || kb == 0 || kb == 4) {  // the block's landing group
+          landed = mbar_wait(bar_addr(m.kv_full[st][KBG == 1 ? kb : kb / 4]), ph, abort, kTimeoutNs);
+          if (!landed) break;
+          tc_fence_after();
+        }
+        const uint64_t dk = (kb < 4 ? dk0 + ((kb * fx_blk<KBG>()) >> 4) : dk4) + st * kStageEnc;
 #pragma unroll
         for (int ks = 0; ks < (kb < 4 ? 4 : 2); ++ks)
-          mma_f8_ss(d, dq + ((kb * kFxBlock + ks * 32) >> 4), dk + ((kb * kFxBlock + ks * 32) >> 4),
-                    idesc_s, kb > 0 || ks > 0);
+          mma_f8_ss(d, dq + ((kb * kFxBlock + ks * 32) >> 4), dk + ((ks * 32) >> 4), idesc_s,
+                    kb > 0 || ks > 0);
       }
       if (!landed) { ok = false; break; }
       mma_commit(bar_addr(m.s_full[sb]));
@@ -535,7 +563,8 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
     constexpr uint64_t kStageEnc = uint64_t(kFxStageBytes) >> 4;
     uint64_t dv0[2];
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) dv0[cc] = smem_desc_sw128(sKv + (2 * half + cc) * kFxBlock, kFxBlock, 1024);
+    for (int cc = 0; cc < 2; ++cc)
+      dv0[cc] = smem_desc_sw128(sKv + (2 * half + cc) * fx_blk<KBG>(), kFxBlock, fx_atom<KBG>());
     const uint64_t dp0 = smem_desc_noswz(sKv + 4 * kFxBlock, kFxPLbo, kFxPSbo);
     uint32_t pv_it = 0, o_it = 0;
     bool ok = true;
@@ -559,7 +588,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const uint32_t dcol = tmem + kColO + 64 * (2 * half + cc);
-            const uint64_t dv = dv0[cc] + st * kStageEnc + ((ks * 4 * 1024) >> 4);
+            const uint64_t dv = dv0[cc] + st * kStageEnc + ((ks * 4 * fx_atom<KBG>()) >> 4);
             mma_f8_ss(dcol, dv, dp + ((ks * 2 * kFxPLbo) >> 4), idesc_o, !(fresh && ks == 0));
             mma_f8_ss(dcol, dv, dp + ((kFxPTerm + ks * 2 * kFxPLbo) >> 4), idesc_o_lo, 1u);
           }
@@ -679,13 +708,14 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Value rows [nv, roundup32(nv)) of a raw e4m3 stage (512 B of value dims
 // each, blocks 0..3), zeroed by the softmax warpgroup (rank gt).
+template <int KBG>
 static __device__ __noinline__ void zero_value_tail_fx(unsigned char *stage, int nv, int gt) {
   using namespace tc;
   const int nrow = ((nv + 31) & ~31) - nv;
   for (int i = gt; i < nrow * 32; i += 128) {
     const int rr = nv + (i >> 5), kb = (i >> 3) & 3, ch = i & 7;
-    *reinterpret_cast<uint4 *>(stage + kb * kFxBlock + (rr >> 3) * 1024 + (rr & 7) * 128 + ch * 16) =
-        make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4 *>(stage + kb * fx_blk<KBG>() + (rr >> 3) * fx_atom<KBG>() + (rr & 7) * 128 +
+                               ch * 16) = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -896,7 +926,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
           ellx[h] = ellx[h] * alpha[h] + (xsum.x + xsum.y);
           mrun[h] = mnew[h];
         }
-        if (nv & 31) zero_value_tail_fx(smem + off_kv<F8>() + st * kFxStageBytes, nv, gt);
+        if (nv & 31) zero_value_tail_fx<KBG>(smem + off_kv<F8>() + st * kFxStageBytes, nv, gt);
       } else {
         // bf16 P [head][token] in the stage's rope block, swizzled K-major:
         // each lane writes 4-byte token pairs
@@ -1042,6 +1072,44 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
 // down to 2^-2 (below that e4m3's subnormal step, 2^-9, bounds the error), so
 // the scores keep bf16 Q's precision; 2^-k goes to the softmax through a
 // slot tagged with the request.
+// The largest |q| (as bf16 bits without the sign) of a piece's Q rows: the
+// three warps' loads go out 16 at a time.  (Asking L2 to keep these lines
+// for the split that reads them again measured slower: they crowd out the
+// KV lines the other head group reads from L2.)
+template <bool FUSED, int MULTI>
+__device__ __forceinline__ uint32_t piece_q_max(const DecodeParams &p, const Walk<FUSED, MULTI> &w,
+                                                TcMisc<3> &m, int ct) {
+  using namespace tc;
+  constexpr int kRowChunks = kDqk / 8;
+  const int hn = min(kHeads, p.heads - w.g * kHeads), n = hn * kRowChunks;
+  const uint4 *qg =
+      reinterpret_cast<const uint4 *>(p.q + (size_t(w.rb) * p.heads + size_t(w.g) * kHeads) * kDqk);
+  uint32_t mx = 0;
+  for (int i0 = ct; i0 < n; i0 += 16 * kConvThreads) {
+    uint4 v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = i0 + u * kConvThreads;
+      v[u] = i < n ? __ldg(qg + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      mx = __vmaxu2(mx, v[u].x & 0x7fff7fffu);
+      mx = __vmaxu2(mx, v[u].y & 0x7fff7fffu);
+      mx = __vmaxu2(mx, v[u].z & 0x7fff7fffu);
+      mx = __vmaxu2(mx, v[u].w & 0x7fff7fffu);
+    }
+  }
+  mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
+  if ((ct & 31) == 0) m.conv_max[ct >> 5] = mx;
+  named_sync(3, kConvThreads);
+  return max(m.conv_max[0], max(m.conv_max[1], m.conv_max[2]));
+}
+
+// Warps 9..11, once per request piece: the piece's largest |q| is taken
+// while the previous piece runs (its rows are then in L2 as well); after the
+// previous piece's score MMAs have read Q (q_empty), the rows are read again,
+// 16 loads at a time, split and stored.
 template <bool FUSED, int MULTI>
 __device__ __forceinline__ void tc_split_q(const TcParams &tp, const CtaRange &r, TcMisc<3> &m,
                                            unsigned char *smem, int *err) {
@@ -1049,54 +1117,60 @@ __device__ __forceinline__ void tc_split_q(const TcParams &tp, const CtaRange &r
   const DecodeParams &p = tp.p;
   volatile int *abort = &m.abort;
   const int ct = int(threadIdx.x) - kConvWarp0 * 32;  // 0 .. 95
-  const int cw = ct >> 5, lane = ct & 31;
+  const int lane = ct & 31;
   constexpr int kRowChunks = kDqk / 8;                // 72 chunks of 8 dims per row
+  constexpr int kPer = kHeads * kRowChunks / kConvThreads;  // 48 chunks per thread
+  static_assert(kHeads * kRowChunks % (16 * kConvThreads) == 0, "Q split batches");
   uint32_t q_it = 0;
   bool ok = true;
-  Walk<FUSED, MULTI> w(p, r);
+  Walk<FUSED, MULTI> w(p, r), wa(p, r);  // wa: the piece after w
+  bool ahead = wa.next();
+  uint32_t mx = ahead ? piece_q_max(p, wa, m, ct) : 0u;
+  if (ahead) {
+    wa.advance();
+    ahead = wa.next();
+  }
   for (; w.next(); w.advance(), ++q_it) {
     const bool got = mbar_wait(bar_addr(m.q_empty), (q_it & 1) ^ 1, abort, kTimeoutNs);
     if (!named_sync_and(3, kConvThreads, got)) { ok = false; break; }
     const int hn = min(kHeads, p.heads - w.g * kHeads);
     const uint4 *qg =
         reinterpret_cast<const uint4 *>(p.q + (size_t(w.rb) * p.heads + size_t(w.g) * kHeads) * kDqk);
-    uint32_t mx = 0;
-    for (int i = ct; i < hn * kRowChunks; i += kConvThreads) {
-      const uint4 v = qg[i];
-      mx = __vmaxu2(mx, v.x & 0x7fff7fffu);
-      mx = __vmaxu2(mx, v.y & 0x7fff7fffu);
-      mx = __vmaxu2(mx, v.z & 0x7fff7fffu);
-      mx = __vmaxu2(mx, v.w & 0x7fff7fffu);
-    }
-    mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
-    if (lane == 0) m.conv_max[cw] = mx;
-    named_sync(3, kConvThreads);
-    mx = max(m.conv_max[0], max(m.conv_max[1], m.conv_max[2]));
     // |q| bits are ordered like magnitudes; an Inf or NaN keeps k = 0
     int k = 0;
     if (mx < 0x7f80u) k = min(126, max(-126, 134 - int(mx >> 7)));
     const float sc = __int_as_float((127 + k) << 23);
-    for (int i = ct; i < kHeads * kRowChunks; i += kConvThreads) {
-      const int rr = i / kRowChunks, c = i - kRowChunks * rr;
-      const uint4 v = rr < hn ? qg[i] : make_uint4(0, 0, 0, 0);
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-      uint32_t hw[2] = {0, 0}, lw[2] = {0, 0};
+#pragma unroll 1
+    for (int u0 = 0; u0 < kPer; u0 += 16) {
+      uint4 v[16];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float f0 = __uint_as_float(wv[e] << 16) * sc, f1 = __uint_as_float(wv[e] & 0xffff0000u) * sc;
-        const uint16_t h = float2_to_e4m3x2(f0, f1);
-        const float2 bh = e4m3x2_to_float2(h);
-        const uint16_t l = float2_to_e4m3x2(f0 - bh.x, f1 - bh.y);
-        hw[e >> 1] |= uint32_t(h) << (16 * (e & 1));
-        lw[e >> 1] |= uint32_t(l) << (16 * (e & 1));
+      for (int u = 0; u < 16; ++u) {
+        const int i = ct + (u0 + u) * kConvThreads;
+        v[u] = i / kRowChunks < hn ? __ldg(qg + i) : make_uint4(0, 0, 0, 0);
       }
-      // dims 8c .. 8c + 7: block c / 16, bytes 8 (c % 16) of the 128-byte row,
-      // 16-byte chunk (c % 16) / 2 at its swizzled place
-      const int b = c & 15;
-      const int off = (c >> 4) * kFxBlock + (rr >> 3) * 1024 + (rr & 7) * 128 + (((b >> 1) ^ (rr & 7)) << 4) +
-                      8 * (b & 1);
-      *reinterpret_cast<uint2 *>(smem + off) = make_uint2(hw[0], hw[1]);
-      *reinterpret_cast<uint2 *>(smem + kFxQTerm + off) = make_uint2(lw[0], lw[1]);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int i = ct + (u0 + u) * kConvThreads;
+        const int rr = i / kRowChunks, c = i - kRowChunks * rr;
+        const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t hw[2] = {0, 0}, lw[2] = {0, 0};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float f0 = __uint_as_float(wv[e] << 16) * sc, f1 = __uint_as_float(wv[e] & 0xffff0000u) * sc;
+          const uint16_t h = float2_to_e4m3x2(f0, f1);
+          const float2 bh = e4m3x2_to_float2(h);
+          const uint16_t l = float2_to_e4m3x2(f0 - bh.x, f1 - bh.y);
+          hw[e >> 1] |= uint32_t(h) << (16 * (e & 1));
+          lw[e >> 1] |= uint32_t(l) << (16 * (e & 1));
+        }
+        // dims 8c .. 8c + 7: block c / 16, bytes 8 (c % 16) of the 128-byte
+        // row, 16-byte chunk (c % 16) / 2 at its swizzled place
+        const int b = c & 15;
+        const int off = (c >> 4) * kFxBlock + (rr >> 3) * 1024 + (rr & 7) * 128 +
+                        (((b >> 1) ^ (rr & 7)) << 4) + 8 * (b & 1);
+        *reinterpret_cast<uint2 *>(smem + off) = make_uint2(hw[0], hw[1]);
+        *reinterpret_cast<uint2 *>(smem + kFxQTerm + off) = make_uint2(lw[0], lw[1]);
+      }
     }
     if (ct == 0) {
       m.qinv[q_it & 3] = __int_as_float((127 - k) << 23);
@@ -1106,6 +1180,12 @@ __device__ __forceinline__ void tc_split_q(const TcParams &tp, const CtaRange &r
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_addr(m.q_ready));
+    // the next piece's largest |q|, while this one runs
+    mx = ahead ? piece_q_max(p, wa, m, ct) : 0u;
+    if (ahead) {
+      wa.advance();
+      ahead = wa.next();
+    }
   }
   if (!ok) atomicOr(err, kErrTimeout);
 }
