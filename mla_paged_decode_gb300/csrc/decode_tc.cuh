@@ -65,26 +65,25 @@ using namespace sm100;
 
 namespace tc {
 constexpr int kThreads = 288;                // bf16 cache
-constexpr int kThreadsF8 = 384;              // e4m3 cache: + 3 converter warps
-constexpr int kConvWarp0 = 9;
+constexpr int kThreadsF8 = 384;              // e4m3 cache: + 3 warps that split Q
+constexpr int kConvWarp0 = 9;                // the first of them
 constexpr int kConvThreads = 96;
 constexpr int kHeads = 64;                   // heads per virtual request (M of S)
 constexpr int kKb = kDqk / 64;               // 9 blocks of 64 bf16 = 128 B
 constexpr int kQBytes = kKb * 64 * 128;      // [kb][64 rows][128 B]
 constexpr int kAtomBytes = kKb * 1024;       // 8 tokens x 576 dims
 constexpr int kStageBytes = 8 * kAtomBytes;  // 64 tokens
-// Stage layout: column groups of KBG dim blocks each,
+// bf16 stage layout: column groups of KBG dim blocks each,
 // [group][atom (8 rows)][dim block within the group][8 rows][128 B].
-// KBG = 3 (bf16 cache, P = 1: a tile is one page): three groups (dims
-// 0..191, 192..383, 384..575), each landed by its own TMA box and barrier,
-// so the score MMAs start on the first group while the others are in
-// flight.  KBG = 9 otherwise: one group, one box per page (a tile of P > 1
-// gathers P pages, and three boxes per page cost more than they gain; an
-// e4m3 stage is filled by the converter).  P [64 heads][64 tokens] reuses
-// the rope block (dims 512..575) of the tile's own stage, dead once S is
-// computed.
-// (e4m3: blocks of 128 dims per landing group, 1 when a tile is one page,
-// else 4: blocks 0..3 of an atom together, block 4 apart)
+// KBG = 3 (P = 1: a tile is one page): three groups (dims 0..191, 192..383,
+// 384..575), each landed by its own TMA box and barrier, so the score MMAs
+// start on the first group while the others are in flight.  KBG = 9
+// otherwise: one group, one box per page (a tile of P > 1 gathers P pages,
+// and three boxes per page cost more than they gain).  P [64 heads][64
+// tokens] reuses the rope block (dims 512..575) of the tile's own stage,
+// dead once S is computed.  (e4m3: KBG is the number of 128-dim blocks per
+// landing group, 1 when a tile is one page, else 4: blocks 0..3 of an atom
+// together, block 4 apart; the layouts are below.)
 template <bool F8, int AHEAD>
 constexpr int stage_kbg() { return F8 ? (AHEAD == 1 ? 1 : 4) : AHEAD == 1 ? 3 : kKb; }
 template <int KBG>
