@@ -27,7 +27,8 @@ cudaError_t launch_kv_append(const void *kv_new, void *kv_pages, const int32_t *
                              int32_t *error_word, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
                              const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
-                             const CUtensorMap &tm_kvg, int grid, cudaStream_t stream);
+                             const CUtensorMap &tm_kvg, const CUtensorMap &tm_kvb, int grid,
+                             cudaStream_t stream);
 cudaError_t launch_lse_combine(const void *partials, const float *lses, int num_parts, void *out,
                                float *out_lse, int rows, int dim, int base2, cudaStream_t stream);
 int combine_max_parts();
@@ -162,7 +163,7 @@ bool fused_path(const mla_decode_desc *d, int num_parts) {
 // of one row (5-D / 3-D maps, coordinate r).
 int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, int part_id,
                      int num_parts, bool all_parts, bool strided, CUtensorMap *tm_q,
-                     CUtensorMap *tm_kv, CUtensorMap *tm_kvg) {
+                     CUtensorMap *tm_kv, CUtensorMap *tm_kvg, CUtensorMap *tm_kvb) {
   EncodeTiled enc = encode_tiled();
   if (!enc) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled unavailable");
@@ -205,13 +206,12 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 strided blocks", r);
     // blocks 0..3 of an atom in one box, landing [block][8 rows][128 B]:
-    // (128 bytes, 64 page rows, 4 blocks, pages).  It takes the Q map's slot,
-    // which an e4m3 cache does not use (the kernel splits Q itself).
+    // (128 bytes, 64 page rows, 4 blocks, pages)
     cuuint64_t gdims[4] = {128, cuuint64_t(mla::kPage), 4, cuuint64_t(d->num_pages)};
     cuuint64_t gstrides[3] = {row8, 128, cuuint64_t(mla::kPage) * row8};
     cuuint32_t gbox[4] = {128, 8 * P, 4, 1};
     cuuint32_t ges[4] = {1, P, 1, 1};
-    r = enc(tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(kv), gdims, gstrides, gbox, ges,
+    r = enc(tm_kvb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(kv), gdims, gstrides, gbox, ges,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 strided grouped blocks", r);
@@ -243,14 +243,13 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
     if (!(num_parts == 1 && !all_parts)) {
       // a tile of several pages: blocks 0..3 of a page's owned atoms in one
       // box, landing [atom][block][8 rows][128 B]: (128 bytes, 8 rows, 4
-      // blocks, 8-row atoms, partitions).  It takes the Q map's slot, which
-      // an e4m3 cache does not use (the kernel splits Q itself).
+      // blocks, 8-row atoms, partitions)
       const cuuint64_t G = 8 / P;
       cuuint64_t gdims[5] = {128, 8, 4, cuuint64_t(d->num_pages) * G, P};
       cuuint64_t gstrides[4] = {P * row8, 128, 8 * P * row8, row8};
       cuuint32_t gbox[5] = {128, 8, 4, cuuint32_t(G), 1};
       cuuint32_t ges[5] = {1, 1, 1, 1, 1};
-      r = enc(tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, all_parts ? 5 : 4, const_cast<char *>(base), gdims,
+      r = enc(tm_kvb, CU_TENSOR_MAP_DATA_TYPE_UINT8, all_parts ? 5 : 4, const_cast<char *>(base), gdims,
               gstrides, gbox, ges, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 grouped blocks", r);
@@ -293,6 +292,8 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv column group", r);
   }
+  if (!(d->kv_dtype == MLA_KV_E4M3 && !(num_parts == 1 && !all_parts && !strided)))
+    *tm_kvb = *tm_kv;  // unused: only e4m3 tiles of several pages take grouped boxes
   return MLA_OK;
 }
 
@@ -390,13 +391,14 @@ int enqueue_decode(const void *q, const void *kv_pages, const int32_t *block_tab
   p.lse_base2 = lse_base == MLA_LSE_BASE2;
   cudaError_t e;
   if (tc) {
-    CUtensorMap tm_q, tm_kv, tm_kvg;
+    CUtensorMap tm_q, tm_kv, tm_kvg, tm_kvb;
     int st = make_tensor_maps(q, kv_pages, d, p.part_id, p.num_parts, fused, strided, &tm_q,
-                              &tm_kv, &tm_kvg);
+                              &tm_kv, &tm_kvg, &tm_kvb);
     if (st != MLA_OK) return st;
     const int h = rows < kTcHeadsPerGroup ? rows : kTcHeadsPerGroup;
     const int npv = ((h + 15) / 16) * 16;
-    e = mla::launch_decode_tc(p, npv, h, strided ? 1 : 8 / p.num_parts, tm_q, tm_kv, tm_kvg, grid, s);
+    e = mla::launch_decode_tc(p, npv, h, strided ? 1 : 8 / p.num_parts, tm_q, tm_kv, tm_kvg, tm_kvb,
+                              grid, s);
   } else {
     e = mla::launch_decode_simt(p, grid, s);
   }

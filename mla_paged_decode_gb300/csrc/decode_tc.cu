@@ -7,22 +7,23 @@
 namespace mla {
 
 extern template cudaError_t launch_tc_variants<false>(
-    const TcParams &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, int,
-    cudaStream_t);
+    const TcParams &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+    const CUtensorMap &, int, cudaStream_t);
 extern template cudaError_t launch_tc_variants<true>(
-    const TcParams &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, int,
-    cudaStream_t);
+    const TcParams &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+    const CUtensorMap &, int, cudaStream_t);
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int npv, int q_rows, int groups_per_page,
                              const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
-                             const CUtensorMap &tm_kvg, int grid, cudaStream_t stream) {
+                             const CUtensorMap &tm_kvg, const CUtensorMap &tm_kvb, int grid,
+                             cudaStream_t stream) {
   TcParams tp;
   tp.p = p;
   tp.npv = npv;
   tp.q_rows = q_rows;
   tp.groups_per_page = groups_per_page;
-  cudaError_t e = p.kv_e4m3 ? launch_tc_variants<true>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
-                            : launch_tc_variants<false>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
+  cudaError_t e = p.kv_e4m3 ? launch_tc_variants<true>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream)
+                            : launch_tc_variants<false>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream);
   if (e != cudaSuccess) return e;
   // all partitions in one launch: the split merge also combines the partitions
   return p.fused && p.comb_out ? launch_dcp_merge_combine(p, grid, stream)

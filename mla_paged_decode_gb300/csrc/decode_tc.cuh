@@ -278,7 +278,7 @@ __device__ __forceinline__ bool lane_page(const DecodeParams &p, int part, long 
 template <bool F8, bool FUSED, int MULTI, int AHEAD>
 __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMiscFor<F8> &m,
                             uint32_t sQ, uint32_t sKv, const CUtensorMap *tm_q, const CUtensorMap *tm_kv,
-                            const CUtensorMap *tm_kvg, int *err) {
+                            const CUtensorMap *tm_kvg, const CUtensorMap *tm_kvb, int *err) {
   using namespace tc;
   constexpr bool STRIDED = MULTI == 2;
   constexpr int NS = num_stages<F8>();
@@ -388,10 +388,8 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
       } else if (F8) {
         // this lane's rows (its page's owned rows, or one atom of the strided
         // gather: rows row0 + iP of page pg, traversal stride P): blocks 0..3
-        // as [atom][block][8 rows][128 B] through the grouped map (in the Q
-        // map's slot: an e4m3 cache's Q is read by warps 9..11), block 4
+        // as [atom][block][8 rows][128 B] through the grouped map, block 4
         // after all four
-        const CUtensorMap *tm_kvb = tm_q;
         const uint32_t d0 = sKv + s * stage_bytes<F8>() + lane * page_bytes * 4;
         const uint32_t d4 = sKv + s * stage_bytes<F8>() + 4 * kFxBlock + lane * page_bytes;
         if (STRIDED) {
@@ -1195,7 +1193,8 @@ template <bool F8, bool FUSED, int MULTI, int AHEAD>
 __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     decode_tc_kernel(const __grid_constant__ TcParams tp, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_kv,
-                     const __grid_constant__ CUtensorMap tm_kvg) {
+                     const __grid_constant__ CUtensorMap tm_kvg,
+                     const __grid_constant__ CUtensorMap tm_kvb) {
   using namespace tc;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -1244,7 +1243,8 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
-    if (KBG != kKb) tma_prefetch_desc(&tm_kvg);
+    if (F8 || KBG != kKb) tma_prefetch_desc(&tm_kvg);
+    if (F8 && KBG == 4) tma_prefetch_desc(&tm_kvb);
   }
   // While the previous kernel finishes, pull the lengths and the head of the
   // block table into L2 (the KV stream of a previous call evicted them): a
@@ -1272,7 +1272,8 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
   if (r.start < r.end) {
     const uint32_t sKv = sbase + off_kv<F8>();
     if (warp == 0) {
-      tc_producer<F8, FUSED, MULTI, AHEAD>(tp, r, m, sbase + kOffQ, sKv, &tm_q, &tm_kv, &tm_kvg, err);
+      tc_producer<F8, FUSED, MULTI, AHEAD>(tp, r, m, sbase + kOffQ, sKv, &tm_q, &tm_kv, &tm_kvg, &tm_kvb,
+                                           err);
     } else if (warp == 1 || warp == 2) {
       if (lane == 0) tc_mma_s<F8, FUSED, MULTI, KBG>(tp, r, m, sbase + kOffQ, sKv, tmem, warp - 1, err);
     } else if (warp == 3 || warp == 8) {
@@ -1296,7 +1297,8 @@ cudaError_t launch_dcp_merge_combine(const DecodeParams &p, int grid, cudaStream
 
 template <bool F8, bool FUSED, int MULTI, int AHEAD>
 static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const CUtensorMap &tm_kv,
-                             const CUtensorMap &tm_kvg, int grid, cudaStream_t stream) {
+                             const CUtensorMap &tm_kvg, const CUtensorMap &tm_kvb, int grid,
+                             cudaStream_t stream) {
   static SmemLimitOnce smem_limit;
   const cudaError_t e = smem_limit.ensure(decode_tc_kernel<F8, FUSED, MULTI, AHEAD>, tc::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1310,7 +1312,8 @@ static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<F8, FUSED, MULTI, AHEAD>, tp, tm_q, tm_kv, tm_kvg);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<F8, FUSED, MULTI, AHEAD>, tp, tm_q, tm_kv, tm_kvg,
+                            tm_kvb);
 }
 
 // The variants of one cache dtype: one partition alone with P = 1 (a tile is
@@ -1319,20 +1322,20 @@ static cudaError_t launch_tc(const TcParams &tp, const CUtensorMap &tm_q, const 
 // strided gather (one partition or all).
 template <bool F8>
 cudaError_t launch_tc_variants(const TcParams &tp, const CUtensorMap &tm_q,
-                               const CUtensorMap &tm_kv, const CUtensorMap &tm_kvg, int grid,
-                               cudaStream_t stream) {
+                               const CUtensorMap &tm_kv, const CUtensorMap &tm_kvg,
+                               const CUtensorMap &tm_kvb, int grid, cudaStream_t stream) {
   if (tp.p.strided)
-    return tp.p.fused ? launch_tc<F8, true, 2, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
-                      : launch_tc<F8, false, 2, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
+    return tp.p.fused ? launch_tc<F8, true, 2, 2>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream)
+                      : launch_tc<F8, false, 2, 2>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream);
   const bool multi = multi_rows(tp.p);
   if (tp.p.fused)
-    return multi ? launch_tc<F8, true, true, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
-                 : launch_tc<F8, true, false, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
+    return multi ? launch_tc<F8, true, true, 2>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream)
+                 : launch_tc<F8, true, false, 2>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream);
   if (tp.p.num_parts == 1)
-    return multi ? launch_tc<F8, false, true, 1>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
-                 : launch_tc<F8, false, false, 1>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
-  return multi ? launch_tc<F8, false, true, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream)
-               : launch_tc<F8, false, false, 2>(tp, tm_q, tm_kv, tm_kvg, grid, stream);
+    return multi ? launch_tc<F8, false, true, 1>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream)
+                 : launch_tc<F8, false, false, 1>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream);
+  return multi ? launch_tc<F8, false, true, 2>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream)
+               : launch_tc<F8, false, false, 2>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream);
 }
 
 }  // namespace mla

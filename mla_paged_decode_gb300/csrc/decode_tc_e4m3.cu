@@ -4,5 +4,5 @@
 namespace mla {
 template cudaError_t launch_tc_variants<true>(const TcParams &, const CUtensorMap &,
                                                const CUtensorMap &, const CUtensorMap &,
-                                               int, cudaStream_t);
+                                               const CUtensorMap &, int, cudaStream_t);
 }  // namespace mla
