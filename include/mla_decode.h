@@ -138,6 +138,16 @@ size_t mla_decode_workspace_size(const mla_decode_desc *d, int num_sms);
  * partitions own (reading num_parts / g times the partition's own bytes).
  * Larger ratios run a CUDA-core kernel.
  *
+ * Arithmetic (tensor-core path): fp32 accumulation throughout.  A bf16
+ * cache is multiplied as stored by bf16 q and by the softmax weights rounded
+ * to bf16.  An e4m3 cache is also multiplied as stored, by e4m3 MMAs:
+ *  - q enters as two e4m3 terms of 2^k q, exact for elements down to 2^-9
+ *    of the largest |q| of the request's 64-row head group;
+ *  - the weights enter as an e4m3 term plus an e5m2 term, relative error
+ *    <= 2^-7; weights below 2^-16 of the running maximum drop out of `out`;
+ *  - `out` is normalised by the weights as multiplied, and `lse` by their
+ *    unrounded sum.
+ *
  * Several query tokens (q_len = T > 1; tensor-core path only, else
  * MLA_ERR_SHAPE): the request's queries are its last T tokens, and query
  * token i attends causally to the owned tokens t < L_b - T + i + 1; a query
