@@ -144,7 +144,8 @@ size_t mla_decode_workspace_size(const mla_decode_desc *d, int num_sms);
  *  - q enters as two e4m3 terms of 2^k q, exact for elements down to 2^-9
  *    of the largest |q| of the request's 64-row head group;
  *  - the weights enter as an e4m3 term plus an e5m2 term, relative error
- *    <= 2^-7; weights below 2^-16 of the running maximum drop out of `out`;
+ *    <= 2^-7 for weights down to 2^-6 of the running maximum, 2 to 3 bits
+ *    below that; weights below 2^-16 of it drop out of `out`;
  *  - `out` is normalised by the weights as multiplied, and `lse` by their
  *    unrounded sum.
  *
