@@ -74,7 +74,8 @@ def test_metadata_flags_a_slot_inside_a_page():
 
 
 @pytest.mark.parametrize("kv_dtype,heads,num_parts", [("bf16", 16, 8), ("bf16", 64, 2),
-                                                       ("bf16", 128, 4), ("e4m3", 16, 4)])
+                                                       ("bf16", 128, 4), ("e4m3", 16, 4),
+                                                       ("e4m3", 64, 2), ("e4m3", 128, 8)])
 def test_rank_decode_equals_the_global_partition_bit_for_bit(kv_dtype, heads, num_parts):
     lens = [1, 7, 64 * num_parts, 3000, 129, 0, 20000]
     case = workloads.make_decode_case("rank", heads, lens, seed=heads, device="cuda",
