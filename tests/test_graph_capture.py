@@ -19,11 +19,12 @@ def _library():
     mla.load_library()
 
 
-def test_decode_partials_and_combine_replay_bit_identical():
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_decode_partials_and_combine_replay_bit_identical(kv_dtype):
     case = workloads.make_decode_case("graph", 64, [3000, 65, 1, 900], num_parts=2, seed=5,
-                                      device="cuda")
+                                      device="cuda", kv_dtype=kv_dtype)
     B, H = case.batch, case.heads
-    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table)
+    ws = mla.make_workspace(case.q, case.kv_pages, case.block_table, case.kv_scale)
     outs = torch.empty(2, B, 1, H, 512, dtype=torch.bfloat16, device="cuda")
     lses = torch.empty(2, B, 1, H, dtype=torch.float32, device="cuda")
     merged = torch.empty(B, H, 512, dtype=torch.bfloat16, device="cuda")
@@ -31,7 +32,8 @@ def test_decode_partials_and_combine_replay_bit_identical():
     def step(stream):
         for r in range(2):
             mla.decode_partial(case.q, case.kv_pages, case.block_table, case.seq_lens, r, 2,
-                               case.sm_scale, 1, outs[r], lses[r], workspace=ws, stream=stream)
+                               case.sm_scale, 1, outs[r], lses[r], kv_scale=case.kv_scale,
+                               workspace=ws, stream=stream)
         mla.lse_combine(outs.view(2, B, H, 512), lses.view(2, B, H), 2, merged, lse_base=1,
                         stream=stream)
 

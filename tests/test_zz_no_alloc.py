@@ -16,7 +16,7 @@ import torch
 
 import mla_paged_decode_gb300 as mla
 import workloads
-from gpu_helpers import assert_lse_close, assert_out_close, run_partial
+from gpu_helpers import FP8_ATOL, assert_lse_close, assert_out_close, run_partial
 
 pytestmark = pytest.mark.gpu
 
@@ -48,18 +48,20 @@ def _call(lib, case, part_id, base, out, lse):
         out.data_ptr(), lse.data_ptr(), ctypes.byref(d), stream)
 
 
-@pytest.mark.parametrize("num_parts", [2, 3])  # a gather of 64/P rows per page; the strided gather
-def test_noalloc_matches_the_workspace_entry_point_twice_in_a_row(lib, num_parts):
+# a gather of 64/P rows per page; the strided gather; an e4m3 cache alone and gathered
+@pytest.mark.parametrize("num_parts,kv_dtype", [(2, "bf16"), (3, "bf16"), (1, "e4m3"), (4, "e4m3")])
+def test_noalloc_matches_the_workspace_entry_point_twice_in_a_row(lib, num_parts, kv_dtype):
     case = workloads.make_decode_case("noalloc", 64, [5000, 77, 12000, 1, 0], num_parts=num_parts,
-                                      seed=31, device="cuda", pool_pages=400)
-    for call, (part_id, base) in enumerate([(0, 0), (1, 1)]):
+                                      seed=31, device="cuda", pool_pages=400, kv_dtype=kv_dtype)
+    for call, (part_id, base) in enumerate([(0, 0), (1 % num_parts, 1)]):
         ref_out, ref_lse = run_partial(case, part_id, base)
         out = torch.full_like(ref_out, float("nan"))
         lse = torch.full_like(ref_lse, float("nan"))
         assert _call(lib, case, part_id, base, out, lse) == 0
         torch.cuda.synchronize()
         ref = ref_out.double().cpu().numpy()
-        assert_out_close(out, ref, what=f"no-alloc call {call}")
+        assert_out_close(out, ref, **({"atol": FP8_ATOL} if kv_dtype == "e4m3" else {}),
+                         what=f"no-alloc call {call}")
         assert_lse_close(lse, ref_lse.double().cpu().numpy(), base, what=f"no-alloc call {call}")
         # the same tensor-core kernels on the same grid (the no-alloc grid is
         # capped at 152 CTAs: with more SMs the split points differ)
