@@ -15,6 +15,12 @@ constexpr int kDv = 512;         // latent = value
 constexpr int kPage = 64;        // tokens per cache page
 constexpr int kTile = 64;        // partition-local tokens per KV tile
 constexpr int kSlotHeads = 64;   // heads per split-partial slot in the workspace
+// Schedule cost of a request piece's boundary (its Q, the pipeline refill,
+// the epilogue), in tiles: an e4m3 piece also splits its Q into two terms,
+// and its tiles are shorter, so its boundary weighs more tiles (each value
+// the measured best of 4, 8 and 12 on that dtype's workloads).
+constexpr int kPieceCost = 4;
+constexpr int kPieceCostE4m3 = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -261,17 +267,18 @@ __device__ __forceinline__ int request_tiles(const DecodeParams &p, int v) {
 //
 // Cost-weighted stream-K split of the concatenated tile sequence of all
 // virtual requests v = g * batch + b (tiles_v = ceil(local_len / 64)).
-// Every request with tiles costs tiles_v + kPieceCost: the extra units stand
-// for the per-piece work (Q load, pipeline refill, epilogue), so a CTA whose
-// range crosses a request boundary gets fewer tiles.  Request v occupies cost
-// units [P_v, P_v + tiles_v) followed by a gap of kPieceCost; C = total cost.
+// Every request with tiles costs tiles_v + PC: the extra units stand for the
+// per-piece work (Q load, pipeline refill, epilogue), so a CTA whose range
+// crosses a request boundary gets fewer tiles.  Request v occupies cost units
+// [P_v, P_v + tiles_v) followed by a gap of PC; C = total cost.  PC is a
+// compile-time constant of each kernel variant (kPieceCost, or kPieceCostE4m3
+// for the e4m3 tensor-core variants): read from the launch parameters instead
+// it measured slower.
 // G_eff = min(gridDim.x, C) CTAs; CTA c owns the tiles whose cost lies in
 // [c*C/G_eff, (c+1)*C/G_eff).  A request crossing a boundary is split; each
 // split writes a normalised fp32 partial into slot 2c (the CTA's first
 // request) or 2c+1 (its last); the request's first CTA records {itself,
 // split count, its slot} and a second kernel merges the splits.
-
-constexpr int kPieceCost = 4;
 
 struct CtaRange {
   long long start, end;   // cost range of this CTA
@@ -290,19 +297,19 @@ __device__ __forceinline__ int sched_owner(long long x, long long C, int g_eff) 
   return int(((x + 1) * g_eff - 1) / C);
 }
 
-__device__ __forceinline__ long long request_cost(int tiles) {
-  return tiles > 0 ? tiles + kPieceCost : 0;
+__device__ __forceinline__ long long request_cost(int tiles, int piece_cost) {
+  return tiles > 0 ? tiles + piece_cost : 0;
 }
 
 // Block-wide: computes this CTA's range.  All threads must call it.
 // `scratch` needs blockDim.x / 32 + 1 long longs of shared memory.
-template <int MULTI = 0>
+template <int MULTI = 0, int PC = kPieceCost>
 __device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long long *scratch) {
   const int V = p.batch * p.head_groups;
   const int tid = threadIdx.x, nw = blockDim.x / 32, lane = tid & 31, warp = tid >> 5;
   // pass 1: total cost
   long long mine = 0;
-  for (int v = tid; v < V; v += blockDim.x) mine += request_cost(request_tiles<MULTI>(p, v));
+  for (int v = tid; v < V; v += blockDim.x) mine += request_cost(request_tiles<MULTI>(p, v), PC);
   for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
   if (lane == 0) scratch[warp] = mine;
   __syncthreads();
@@ -324,12 +331,12 @@ __device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long lon
   const long long start = r->start, end = r->end;
   if (start >= end) return;
   // pass 2: the first request whose tiles end after `start` (chunked block
-  // scan of the costs); its predecessor ends at P_v - kPieceCost
+  // scan of the costs); its predecessor ends at P_v - PC
   long long base = 0;
   for (int v0 = 0; v0 < V; v0 += blockDim.x) {
     int v = v0 + tid;
     const int tiles = v < V ? request_tiles<MULTI>(p, v) : 0;
-    const long long cst = request_cost(tiles);
+    const long long cst = request_cost(tiles, PC);
     long long incl = cst;
     for (int o = 1; o < 32; o <<= 1) {
       long long y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -344,7 +351,7 @@ __device__ inline void cta_schedule(const DecodeParams &p, CtaRange *r, long lon
       chunk += scratch[w];
     }
     const long long excl = base + wbase + incl - cst;
-    if (tiles > 0 && excl + tiles > start && excl - kPieceCost <= start) {
+    if (tiles > 0 && excl + tiles > start && excl - PC <= start) {
       r->v_begin = v;
       r->p_begin = excl;
     }

@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) decode_simt_kernel(DecodePara
       }
     }
     if (tid == 0) record_split(p, v, si);
-    pv += request_cost(tiles);
+    pv += request_cost(tiles, kPieceCost);
     ++v;
   }
 }

@@ -181,10 +181,14 @@ static_assert(sizeof(TcMisc<3>) + 1024 <= tc::kSmemBytes - tc::off_misc<true>(),
 template <bool F8>
 using TcMiscFor = TcMisc<tc::num_stages<F8>()>;
 
+// The split schedule's cost of a request piece's boundary, per cache dtype.
+template <bool F8>
+constexpr int piece_cost() { return F8 ? kPieceCostE4m3 : kPieceCost; }
+
 // The requests (and tile ranges) this CTA owns, in order; every role walks it.
 // FUSED: all partitions in one launch (output row b = partition * B + input
 // request); otherwise one partition, p.part_id, and row b is request b.
-template <bool FUSED, int MULTI>
+template <bool FUSED, int MULTI, int PC>
 struct Walk {
   const DecodeParams &p;
   const CtaRange &r;
@@ -212,13 +216,13 @@ struct Walk {
     }
     return false;
   }
-  __device__ void advance() { pv += request_cost(tiles); ++v; }
+  __device__ void advance() { pv += request_cost(tiles, PC); ++v; }
 };
 
 // One position in the walk: request + tile.
-template <bool FUSED, int MULTI>
+template <bool FUSED, int MULTI, int PC>
 struct TileCursor {
-  Walk<FUSED, MULTI> w;
+  Walk<FUSED, MULTI, PC> w;
   long long t;
   bool live;
   __device__ TileCursor(const DecodeParams &p, const CtaRange &r) : w(p, r), t(0) {
@@ -306,7 +310,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   // one or two tiles early, when the page is prefetched into L2 (the
   // 129 MB L2 gives the two shared-memory stages more HBM requests in
   // flight), and carried in `ring` until its tile is loaded.
-  TileCursor<FUSED, MULTI> ahead(p, r);
+  TileCursor<FUSED, MULTI, piece_cost<F8>()> ahead(p, r);
   auto next_ahead = [&]() {
     int pg = -1;
     if (ahead.live) {
@@ -340,7 +344,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
 #pragma unroll
   for (int i = 0; i < AHEAD; ++i) ring[i] = next_ahead();
 
-  TileCursor<FUSED, MULTI> cur(p, r);
+  TileCursor<FUSED, MULTI, piece_cost<F8>()> cur(p, r);
   while (cur.live) {
     if (!F8 && cur.first()) {  // (e4m3: warps 9..11 load and split Q)
       checked_len(p, cur.w.rb, err);
@@ -463,7 +467,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
     constexpr uint64_t kStageEnc = uint64_t(kFxStageBytes) >> 4;
     uint32_t s_it = 0, q_it = 0;
     bool ok = true;
-    for (TileCursor<FUSED, MULTI> sc(p, r); sc.live; sc.step(), ++s_it) {
+    for (TileCursor<FUSED, MULTI, piece_cost<F8>()> sc(p, r); sc.live; sc.step(), ++s_it) {
       const int st = s_it % NS, sb = s_it & 1;
       const uint32_t ph = (s_it / NS) & 1;
       if (sc.first()) {
@@ -504,7 +508,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
   uint32_t s_it = 0, q_it = 0;
   bool ok = true;
-  for (TileCursor<FUSED, MULTI> sc(p, r); sc.live; sc.step(), ++s_it) {
+  for (TileCursor<FUSED, MULTI, piece_cost<F8>()> sc(p, r); sc.live; sc.step(), ++s_it) {
     const int st = s_it & 1;
     const uint32_t ph = (s_it >> 1) & 1;
     if (!mbar_wait(bar_addr(m.kv_full[st][0]), ph, abort, kTimeoutNs)) {
@@ -565,7 +569,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
     const uint64_t dp0 = smem_desc_noswz(sKv + 4 * kFxBlock, kFxPLbo, kFxPSbo);
     uint32_t pv_it = 0, o_it = 0;
     bool ok = true;
-    for (TileCursor<FUSED, MULTI> pc(p, r); pc.live; pc.step(), ++pv_it) {
+    for (TileCursor<FUSED, MULTI, piece_cost<F8>()> pc(p, r); pc.live; pc.step(), ++pv_it) {
       const int st = pv_it % NS;
       if (!mbar_wait(bar_addr(m.p_full[st]), (pv_it / NS) & 1, abort, kTimeoutNs)) {
         ok = false;
@@ -616,7 +620,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
   constexpr uint64_t kStageEnc = uint64_t(kStageBytes) >> 4;
   uint32_t pv_it = 0, o_it = 0;
   bool ok = true;
-  for (TileCursor<FUSED, MULTI> pc(p, r); pc.live; pc.step(), ++pv_it) {
+  for (TileCursor<FUSED, MULTI, piece_cost<F8>()> pc(p, r); pc.live; pc.step(), ++pv_it) {
     if (!mbar_wait(bar_addr(m.p_full[pv_it & 1]), (pv_it >> 1) & 1, abort, kTimeoutNs)) {
       ok = false;
       break;
@@ -755,7 +759,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
   if (masked) own = owner_mask_of(p);
 
   uint32_t piece = 0;
-  Walk<FUSED, MULTI> w(p, r);
+  Walk<FUSED, MULTI, piece_cost<F8>()> w(p, r);
   for (; ok && w.next(); w.advance(), ++piece) {
     const int hn = min(kHeads, p.heads - w.g * kHeads);
     if (F8) {
@@ -1074,7 +1078,8 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
 // for the split that reads them again measured slower: they crowd out the
 // KV lines the other head group reads from L2.)
 template <bool FUSED, int MULTI>
-__device__ __forceinline__ uint32_t piece_q_max(const DecodeParams &p, const Walk<FUSED, MULTI> &w,
+__device__ __forceinline__ uint32_t piece_q_max(const DecodeParams &p,
+                                                const Walk<FUSED, MULTI, kPieceCostE4m3> &w,
                                                 TcMisc<3> &m, int ct) {
   using namespace tc;
   constexpr int kRowChunks = kDqk / 8;
@@ -1120,7 +1125,7 @@ __device__ __forceinline__ void tc_split_q(const TcParams &tp, const CtaRange &r
   static_assert(kHeads * kRowChunks % (16 * kConvThreads) == 0, "Q split batches");
   uint32_t q_it = 0;
   bool ok = true;
-  Walk<FUSED, MULTI> w(p, r), wa(p, r);  // wa: the piece after w
+  Walk<FUSED, MULTI, kPieceCostE4m3> w(p, r), wa(p, r);  // wa: the piece after w
   bool ahead = wa.next();
   uint32_t mx = ahead ? piece_q_max(p, wa, m, ct) : 0u;
   if (ahead) {
@@ -1262,7 +1267,7 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
   // launch's own dependent, the split merge, early as well measured slower.)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   write_empty_requests<MULTI>(p);
-  cta_schedule<MULTI>(p, &m.range, m.scratch);
+  cta_schedule<MULTI, piece_cost<F8>()>(p, &m.range, m.scratch);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
