@@ -240,10 +240,10 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
             fstrides, fbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 blocks", r);
-    if (!(num_parts == 1 && !all_parts)) {
-      // a tile of several pages: blocks 0..3 of a page's owned atoms in one
-      // box, landing [atom][block][8 rows][128 B]: (128 bytes, 8 rows, 4
-      // blocks, 8-row atoms, partitions)
+    {
+      // blocks 0..3 of a page's owned atoms in one box, landing
+      // [atom][block][8 rows][128 B]: (128 bytes, 8 rows, 4 blocks, 8-row
+      // atoms, partitions)
       const cuuint64_t G = 8 / P;
       cuuint64_t gdims[5] = {128, 8, 4, cuuint64_t(d->num_pages) * G, P};
       cuuint64_t gstrides[4] = {P * row8, 128, 8 * P * row8, row8};
@@ -292,8 +292,7 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv column group", r);
   }
-  if (!(d->kv_dtype == MLA_KV_E4M3 && !(num_parts == 1 && !all_parts && !strided)))
-    *tm_kvb = *tm_kv;  // unused: only e4m3 tiles of several pages take grouped boxes
+  if (d->kv_dtype != MLA_KV_E4M3) *tm_kvb = *tm_kv;  // unused: only e4m3 caches take grouped boxes
   return MLA_OK;
 }
 

@@ -81,11 +81,10 @@ constexpr int kStageBytes = 8 * kAtomBytes;  // 64 tokens
 // otherwise: one group, one box per page (a tile of P > 1 gathers P pages,
 // and three boxes per page cost more than they gain).  P [64 heads][64
 // tokens] reuses the rope block (dims 512..575) of the tile's own stage,
-// dead once S is computed.  (e4m3: KBG is the number of 128-dim blocks per
-// landing group, 1 when a tile is one page, else 4: blocks 0..3 of an atom
-// together, block 4 apart; the layouts are below.)
+// dead once S is computed.  (e4m3: KBG = 4, blocks 0..3 of an atom land
+// together and block 4 apart; the layout is below.)
 template <bool F8, int AHEAD>
-constexpr int stage_kbg() { return F8 ? (AHEAD == 1 ? 1 : 4) : AHEAD == 1 ? 3 : kKb; }
+constexpr int stage_kbg() { return F8 ? 4 : AHEAD == 1 ? 3 : kKb; }
 template <int KBG>
 constexpr int num_groups() { return kKb / KBG; }
 template <int KBG>
@@ -102,23 +101,19 @@ constexpr int kOffMisc = kOffKv + 2 * kStageBytes;
 
 // e4m3 caches, read by fp8 MMAs straight from the raw rows: Q as two e4m3
 // terms, hi and lo, each [5 blocks of 128 dims][64 rows][128 B], swizzled
-// K-major; three stages of the raw rows as landed: blocks 0..3 as [block][8
-// atoms][8 rows][128 B] when a tile is one page (one box and barrier per
-// block), else as [8 atoms][block][8 rows][128 B] (one box per page for all
-// four), and block 4 as [64 rows][128 B] after them (dims 576..639 are the
-// copy's zero fill).  Block 4 (the rope dims), dead once the scores are
-// computed, then holds P as two terms [64 heads][64 tokens] of 4 KB each, hi
-// in e4m3 and lo in e5m2, unswizzled: 8-head x 16-token core matrices of 128 B.
+// K-major; three stages of the raw rows as landed, blocks 0..3 as [8
+// atoms][block][8 rows][128 B] (one box per page, or per atom for the strided
+// gather) and block 4 as [64 rows][128 B] after them (another box; dims
+// 576..639 are the copy's zero fill).  Block 4 (the rope dims), dead once the
+// scores are computed, then holds P as two terms [64 heads][64 tokens] of 4 KB
+// each, hi in e4m3 and lo in e5m2, unswizzled: 8-head x 16-token core
+// matrices of 128 B.
 constexpr int kFxBlocks = 5;
 constexpr int kFxBlock = 64 * 128;                   // one block of 64 rows
 constexpr int kFxQTerm = kFxBlocks * kFxBlock;       // 40 KB
 constexpr int kFxStageBytes = kFxBlocks * kFxBlock;  // 40 KB
 constexpr uint32_t kFxPLbo = 128, kFxPSbo = 512;     // P core matrices along tokens / heads
-// strides of the raw-row layout: between blocks 0..3, and between 8-row atoms
-template <int KBG>
-constexpr uint32_t fx_blk() { return KBG == 1 ? uint32_t(kFxBlock) : 1024u; }
-template <int KBG>
-constexpr uint32_t fx_atom() { return KBG == 1 ? 1024u : 4096u; }
+constexpr uint32_t kFxBlkStride = 1024, kFxAtomStride = 4096;  // raw rows: blocks 0..3, 8-row atoms
 constexpr int kFxPTerm = 4096;                       // P lo after P hi
 // P is stored as 2^(8 - threshold) p (p <= 2^threshold), below the e4m3
 // maximum (448).  Its lo term is e5m2, whose subnormals reach 2^-16: weights
@@ -276,8 +271,7 @@ __device__ __forceinline__ bool lane_page(const DecodeParams &p, int part, long 
 // ------------------------------------------------------------------ producer
 
 // AHEAD: tiles whose pages are pulled into L2 ahead of the stage.  1 when a
-// tile is one page (P = 1), 2 when it gathers P pages of 64/P rows (each the
-// measured best of 0..4).  It is a template parameter because the same choice
+// bf16 tile is one page (P = 1), else 2 (each the measured best of 0..4).  It is a template parameter because the same choice
 // made at run time costs more than it gains.
 template <bool F8, bool FUSED, int MULTI, int AHEAD>
 __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &r, TcMiscFor<F8> &m,
@@ -298,7 +292,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
   // 8 * groups_per_page owned rows (the strided gather: of one atom's rows)
   const int rows_per_page = 8 * tp.groups_per_page;
   constexpr int KBG = stage_kbg<F8, AHEAD>();
-  constexpr int kG = F8 ? (KBG == 1 ? kFxBlocks : 2) : num_groups<KBG>();
+  constexpr int kG = F8 ? 2 : num_groups<KBG>();
   // bytes one page lands per barrier: its rows of one block, or one column group
   const uint32_t page_bytes = F8 ? uint32_t(tp.groups_per_page) * 1024u
                                  : uint32_t(tp.groups_per_page) * atom_stride<KBG>();
@@ -376,20 +370,13 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
       ok = false;
       break;
     }
-    // (e4m3 with blocks 0..3 grouped: four blocks' bytes on the first barrier)
+    // (e4m3: blocks 0..3 on the first barrier, four blocks' bytes)
     if (lane < kG)
-      mbar_arrive_expect_tx(bar_addr(m.kv_full[s][lane]), F8 && KBG == 4 && lane == 0 ? 4 * bytes : bytes);
+      mbar_arrive_expect_tx(bar_addr(m.kv_full[s][lane]), F8 && lane == 0 ? 4 * bytes : bytes);
     __syncwarp();
     if (load) {
       const uint32_t dst = sKv + s * stage_bytes<F8>() + lane * page_bytes;
-      if (F8 && KBG == 1) {
-        // one page a tile: block g, dims [128 g, 128 g + 128) of its 64 rows
-        // (block 4 runs past the row: zero fill)
-#pragma unroll
-        for (int g = 0; g < kFxBlocks; ++g)
-          tma_load_2d(sKv + s * stage_bytes<F8>() + uint32_t(g) * kFxBlock, tm_kvg, bar_addr(m.kv_full[s][g]),
-                      128 * g, pg * rows_per_page);
-      } else if (F8) {
+      if (F8) {
         // this lane's rows (its page's owned rows, or one atom of the strided
         // gather: rows row0 + iP of page pg, traversal stride P): blocks 0..3
         // as [atom][block][8 rows][128 B] through the grouped map, block 4
@@ -462,7 +449,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
     constexpr int NS = num_stages<F8>();
     const uint32_t idesc_s = idesc_e4m3_f32(64, 64, false, false);
     const uint64_t dq = smem_desc_sw128(sQ + uint32_t(chain) * kFxQTerm, 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(sKv, 16, fx_atom<KBG>());      // blocks 0..3
+    const uint64_t dk0 = smem_desc_sw128(sKv, 16, kFxAtomStride);        // blocks 0..3
     const uint64_t dk4 = smem_desc_sw128(sKv + 4 * kFxBlock, 16, 1024);  // block 4
     constexpr uint64_t kStageEnc = uint64_t(kFxStageBytes) >> 4;
     uint32_t s_it = 0, q_it = 0;
@@ -482,12 +469,12 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
       bool landed = true;
 #pragma unroll
       for (int kb = 0; kb < kFxBlocks; ++kb) {
-        if (KBG == 1 || kb == 0 || kb == 4) {  // the block's landing group
-          landed = mbar_wait(bar_addr(m.kv_full[st][KBG == 1 ? kb : kb / 4]), ph, abort, kTimeoutNs);
+        if (kb == 0 || kb == 4) {  // blocks 0..3, then block 4
+          landed = mbar_wait(bar_addr(m.kv_full[st][kb / 4]), ph, abort, kTimeoutNs);
           if (!landed) break;
           tc_fence_after();
         }
-        const uint64_t dk = (kb < 4 ? dk0 + ((kb * fx_blk<KBG>()) >> 4) : dk4) + st * kStageEnc;
+        const uint64_t dk = (kb < 4 ? dk0 + ((kb * kFxBlkStride) >> 4) : dk4) + st * kStageEnc;
 #pragma unroll
         for (int ks = 0; ks < (kb < 4 ? 4 : 2); ++ks)
           mma_f8_ss(d, dq + ((kb * kFxBlock + ks * 32) >> 4), dk + ((ks * 32) >> 4), idesc_s,
@@ -565,7 +552,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
     uint64_t dv0[2];
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc)
-      dv0[cc] = smem_desc_sw128(sKv + (2 * half + cc) * fx_blk<KBG>(), kFxBlock, fx_atom<KBG>());
+      dv0[cc] = smem_desc_sw128(sKv + (2 * half + cc) * kFxBlkStride, kFxBlock, kFxAtomStride);
     const uint64_t dp0 = smem_desc_noswz(sKv + 4 * kFxBlock, kFxPLbo, kFxPSbo);
     uint32_t pv_it = 0, o_it = 0;
     bool ok = true;
@@ -589,7 +576,7 @@ __device__ __forceinline__ void tc_mma_pv(const TcParams &tp, const CtaRange &r,
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const uint32_t dcol = tmem + kColO + 64 * (2 * half + cc);
-            const uint64_t dv = dv0[cc] + st * kStageEnc + ((ks * 4 * fx_atom<KBG>()) >> 4);
+            const uint64_t dv = dv0[cc] + st * kStageEnc + ((ks * 4 * kFxAtomStride) >> 4);
             mma_f8_ss(dcol, dv, dp + ((ks * 2 * kFxPLbo) >> 4), idesc_o, !(fresh && ks == 0));
             mma_f8_ss(dcol, dv, dp + ((kFxPTerm + ks * 2 * kFxPLbo) >> 4), idesc_o_lo, 1u);
           }
@@ -709,13 +696,12 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Value rows [nv, roundup32(nv)) of a raw e4m3 stage (512 B of value dims
 // each, blocks 0..3), zeroed by the softmax warpgroup (rank gt).
-template <int KBG>
 static __device__ __noinline__ void zero_value_tail_fx(unsigned char *stage, int nv, int gt) {
   using namespace tc;
   const int nrow = ((nv + 31) & ~31) - nv;
   for (int i = gt; i < nrow * 32; i += 128) {
     const int rr = nv + (i >> 5), kb = (i >> 3) & 3, ch = i & 7;
-    *reinterpret_cast<uint4 *>(stage + kb * fx_blk<KBG>() + (rr >> 3) * fx_atom<KBG>() + (rr & 7) * 128 +
+    *reinterpret_cast<uint4 *>(stage + kb * kFxBlkStride + (rr >> 3) * kFxAtomStride + (rr & 7) * 128 +
                                ch * 16) = make_uint4(0, 0, 0, 0);
   }
 }
@@ -927,7 +913,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams &tp, const CtaRange &r
           ellx[h] = ellx[h] * alpha[h] + (xsum.x + xsum.y);
           mrun[h] = mnew[h];
         }
-        if (nv & 31) zero_value_tail_fx<KBG>(smem + off_kv<F8>() + st * kFxStageBytes, nv, gt);
+        if (nv & 31) zero_value_tail_fx(smem + off_kv<F8>() + st * kFxStageBytes, nv, gt);
       } else {
         // bf16 P [head][token] in the stage's rope block, swizzled K-major:
         // each lane writes 4-byte token pairs
@@ -1249,7 +1235,7 @@ __global__ void __launch_bounds__(tc_threads<F8>(), 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
     if (F8 || KBG != kKb) tma_prefetch_desc(&tm_kvg);
-    if (F8 && KBG == 4) tma_prefetch_desc(&tm_kvb);
+    if (F8) tma_prefetch_desc(&tm_kvb);
   }
   // While the previous kernel finishes, pull the lengths and the head of the
   // block table into L2 (the KV stream of a previous call evicted them): a
@@ -1336,7 +1322,8 @@ cudaError_t launch_tc_variants(const TcParams &tp, const CUtensorMap &tm_q,
   if (tp.p.fused)
     return multi ? launch_tc<F8, true, true, 2>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream)
                  : launch_tc<F8, true, false, 2>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream);
-  if (tp.p.num_parts == 1)
+  // (a bf16 tile of one page takes distance 1; e4m3 tiles always take 2)
+  if (tp.p.num_parts == 1 && !F8)
     return multi ? launch_tc<F8, false, true, 1>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream)
                  : launch_tc<F8, false, false, 1>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream);
   return multi ? launch_tc<F8, false, true, 2>(tp, tm_q, tm_kv, tm_kvg, tm_kvb, grid, stream)
