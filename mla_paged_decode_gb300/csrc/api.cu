@@ -195,14 +195,14 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 strided", r);
-    // the kernel's loads (the box above serves the L2 prefetch): (576 bytes,
-    // 64 page rows, pages), one swizzled box of 128 dims of an atom's rows c,
-    // c + P, ..., c + 7P
+    // block 4 of the kernel's loads (the box above serves the L2 prefetch):
+    // (576 bytes, 64 page rows, pages), a box of dims 512..575 of an atom's
+    // rows c, c + P, ..., c + 7P with the 64-byte swizzle
     cuuint64_t fdims[3] = {row8, cuuint64_t(mla::kPage), cuuint64_t(d->num_pages)};
     cuuint64_t fstrides[2] = {row8, cuuint64_t(mla::kPage) * row8};
-    cuuint32_t fbox[3] = {128, 8 * P, 1};
+    cuuint32_t fbox[3] = {64, 8 * P, 1};
     r = enc(tm_kvg, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(kv), fdims, fstrides, fbox, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 strided blocks", r);
     // blocks 0..3 of an atom in one box, landing [block][8 rows][128 B]:
@@ -229,15 +229,14 @@ int make_tensor_maps(const void *q, const void *kv, const mla_decode_desc *d, in
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3", r);
-    // the kernel's loads (the box above serves the L2 prefetch): (576 bytes,
-    // owned rows, partitions) with a swizzled box of 128 dims of a page's
-    // 64/P owned rows; block 4 (dims 512..639) runs past the row and reads
-    // zeros there
+    // block 4 of the kernel's loads (the box above serves the L2 prefetch):
+    // (576 bytes, owned rows, partitions), a box of dims 512..575 of a page's
+    // 64/P owned rows with the 64-byte swizzle
     cuuint64_t fdims[3] = {row8, cuuint64_t(d->num_pages) * R, P};
     cuuint64_t fstrides[2] = {P * row8, row8};
-    cuuint32_t fbox[3] = {128, R, 1};
+    cuuint32_t fbox[3] = {64, R, 1};
     r = enc(tm_kvg, CU_TENSOR_MAP_DATA_TYPE_UINT8, all_parts ? 3 : 2, const_cast<char *>(base), fdims,
-            fstrides, fbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            fstrides, fbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return tensor_map_fail("kv e4m3 blocks", r);
     {

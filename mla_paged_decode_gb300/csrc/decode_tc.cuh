@@ -103,9 +103,10 @@ constexpr int kOffMisc = kOffKv + 2 * kStageBytes;
 // terms, hi and lo, each [5 blocks of 128 dims][64 rows][128 B], swizzled
 // K-major; three stages of the raw rows as landed, blocks 0..3 as [8
 // atoms][block][8 rows][128 B] (one box per page, or per atom for the strided
-// gather) and block 4 as [64 rows][128 B] after them (another box; dims
-// 576..639 are the copy's zero fill).  Block 4 (the rope dims), dead once the
-// scores are computed, then holds P as two terms [64 heads][64 tokens] of 4 KB
+// gather) and block 4, dims 512..575, as [64 rows][64 B] with the 64-byte
+// swizzle after them (a box of its own, issued first: it is the small one, and
+// the score MMAs start on it).  The 8 KB block-4 area, dead once the scores
+// are computed, then holds P as two terms [64 heads][64 tokens] of 4 KB
 // each, hi in e4m3 and lo in e5m2, unswizzled: 8-head x 16-token core
 // matrices of 128 B.
 constexpr int kFxBlocks = 5;
@@ -370,28 +371,29 @@ __device__ __forceinline__ void tc_producer(const TcParams &tp, const CtaRange &
       ok = false;
       break;
     }
-    // (e4m3: blocks 0..3 on the first barrier, four blocks' bytes)
+    // (e4m3: blocks 0..3 on the first barrier, four blocks' bytes; block 4,
+    // 64 bytes a row, on the second)
     if (lane < kG)
-      mbar_arrive_expect_tx(bar_addr(m.kv_full[s][lane]), F8 && lane == 0 ? 4 * bytes : bytes);
+      mbar_arrive_expect_tx(bar_addr(m.kv_full[s][lane]), F8 ? (lane == 0 ? 4 * bytes : bytes / 2) : bytes);
     __syncwarp();
     if (load) {
       const uint32_t dst = sKv + s * stage_bytes<F8>() + lane * page_bytes;
       if (F8) {
         // this lane's rows (its page's owned rows, or one atom of the strided
-        // gather: rows row0 + iP of page pg, traversal stride P): blocks 0..3
-        // as [atom][block][8 rows][128 B] through the grouped map, block 4
-        // after all four
+        // gather: rows row0 + iP of page pg, traversal stride P): block 4 (64
+        // bytes a row) first, then blocks 0..3 as [atom][block][8 rows][128 B]
+        // through the grouped map
         const uint32_t d0 = sKv + s * stage_bytes<F8>() + lane * page_bytes * 4;
-        const uint32_t d4 = sKv + s * stage_bytes<F8>() + 4 * kFxBlock + lane * page_bytes;
+        const uint32_t d4 = sKv + s * stage_bytes<F8>() + 4 * kFxBlock + lane * (page_bytes / 2);
         if (STRIDED) {
-          tma_load_4d(d0, tm_kvb, bar_addr(m.kv_full[s][0]), 0, row0, 0, pg);
           tma_load_3d(d4, tm_kvg, bar_addr(m.kv_full[s][1]), 512, row0, pg);
+          tma_load_4d(d0, tm_kvb, bar_addr(m.kv_full[s][0]), 0, row0, 0, pg);
         } else if (FUSED) {
-          tma_load_5d(d0, tm_kvb, bar_addr(m.kv_full[s][0]), 0, 0, 0, pg * tp.groups_per_page, cur.w.pc);
           tma_load_3d(d4, tm_kvg, bar_addr(m.kv_full[s][1]), 512, pg * rows_per_page, cur.w.pc);
+          tma_load_5d(d0, tm_kvb, bar_addr(m.kv_full[s][0]), 0, 0, 0, pg * tp.groups_per_page, cur.w.pc);
         } else {
-          tma_load_4d(d0, tm_kvb, bar_addr(m.kv_full[s][0]), 0, 0, 0, pg * tp.groups_per_page);
           tma_load_2d(d4, tm_kvg, bar_addr(m.kv_full[s][1]), 512, pg * rows_per_page);
+          tma_load_4d(d0, tm_kvb, bar_addr(m.kv_full[s][0]), 0, 0, 0, pg * tp.groups_per_page);
         }
       } else if (STRIDED) {
         // one atom: rows row0 + iP (traversal stride P) of page pg, all dims
@@ -450,7 +452,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
     const uint32_t idesc_s = idesc_e4m3_f32(64, 64, false, false);
     const uint64_t dq = smem_desc_sw128(sQ + uint32_t(chain) * kFxQTerm, 16, 1024);
     const uint64_t dk0 = smem_desc_sw128(sKv, 16, kFxAtomStride);        // blocks 0..3
-    const uint64_t dk4 = smem_desc_sw128(sKv + 4 * kFxBlock, 16, 1024);  // block 4
+    const uint64_t dk4 = smem_desc_sw64(sKv + 4 * kFxBlock, 16, 512);  // block 4
     constexpr uint64_t kStageEnc = uint64_t(kFxStageBytes) >> 4;
     uint32_t s_it = 0, q_it = 0;
     bool ok = true;
@@ -468,9 +470,10 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
       const uint32_t d = tmem + kColS + 64 * (2 * sb + chain);
       bool landed = true;
 #pragma unroll
-      for (int kb = 0; kb < kFxBlocks; ++kb) {
-        if (kb == 0 || kb == 4) {  // blocks 0..3, then block 4
-          landed = mbar_wait(bar_addr(m.kv_full[st][kb / 4]), ph, abort, kTimeoutNs);
+      for (int j = 0; j < kFxBlocks; ++j) {
+        const int kb = (j + 4) % kFxBlocks;  // block 4 first, then blocks 0..3
+        if (j < 2) {
+          landed = mbar_wait(bar_addr(m.kv_full[st][1 - j]), ph, abort, kTimeoutNs);
           if (!landed) break;
           tc_fence_after();
         }
@@ -478,7 +481,7 @@ __device__ __forceinline__ void tc_mma_s(const TcParams &tp, const CtaRange &r, 
 #pragma unroll
         for (int ks = 0; ks < (kb < 4 ? 4 : 2); ++ks)
           mma_f8_ss(d, dq + ((kb * kFxBlock + ks * 32) >> 4), dk + ((ks * 32) >> 4), idesc_s,
-                    kb > 0 || ks > 0);
+                    j > 0 || ks > 0);
       }
       if (!landed) { ok = false; break; }
       mma_commit(bar_addr(m.s_full[sb]));

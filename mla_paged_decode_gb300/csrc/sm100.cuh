@@ -181,6 +181,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
          (uint64_t((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same for a K-major operand of 64-byte rows with the 64-byte swizzle
+// (layout type 4): 8-row atoms of 512 bytes, `sbo` between atoms.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo & 0x3FFFFu) >> 4) << 16) |
+         (uint64_t((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (4ull << 61);
+}
+
 // The same for an unswizzled K-major operand (layout type 0): 8-row x 16-byte
 // core matrices stored as 128 contiguous bytes; `lbo` is the distance between
 // core matrices adjacent along K, `sbo` between those adjacent along M / N.
